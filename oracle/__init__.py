@@ -1,0 +1,199 @@
+"""CPU oracle for the fine-grained FP8 block-scaled GEMM path.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  The product
+library (``fp8_fine_grained_26_b300``) never imports, links or loads it, and
+the two share no code: this is a ctypes wrapper over ``fp8_oracle.c``, a plain
+C restatement of the method (see that file's header for the passages it
+follows).
+
+All arrays are numpy arrays on the host:
+  * bf16 inputs are passed as ``uint16`` bit patterns,
+  * E4M3 codes are ``uint8``,
+  * scales are ``float32``, GEMM results ``float64``.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        i64, p = ctypes.c_int64, ctypes.c_void_p
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = ctypes.c_double
+        lib.oracle_e4m3_encode_n.argtypes = [p, i64, p]
+        lib.oracle_e4m3_encode_n.restype = None
+        lib.oracle_quant_act_1x128.argtypes = [p, i64, i64, i64, p, i64, p]
+        lib.oracle_quant_w_128x128.argtypes = [p, i64, i64, i64, p, i64, p]
+        lib.oracle_gemm_f64.argtypes = [p, p, i64, p, p, i64, ctypes.c_int, i64, i64, i64, p, i64]
+        lib.oracle_gemm_f64_at.argtypes = [p, p, i64, p, p, i64, ctypes.c_int, i64, i64, i64,
+                                           p, p, i64, p]
+        lib.oracle_grouped_gemm_f64.argtypes = [p, p, i64, p, p, p, ctypes.c_int, i64, i64, i64,
+                                                p, i64]
+        lib.oracle_act_row_norms.argtypes = [p, p, i64, i64, i64, p]
+        lib.oracle_act_row_norms.restype = None
+        lib.oracle_b_row_norms.argtypes = [p, p, i64, ctypes.c_int, i64, i64, p]
+        lib.oracle_b_row_norms.restype = None
+        for f in ("oracle_quant_act_1x128", "oracle_quant_w_128x128", "oracle_gemm_f64",
+                  "oracle_gemm_f64_at", "oracle_grouped_gemm_f64"):
+            getattr(lib, f).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what} rejected its arguments (status {rc})")
+
+
+def _as_c(a, dtype):
+    a = np.asarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    return np.ascontiguousarray(a)
+
+
+def e4m3_encode(v: float) -> int:
+    """E4M3 code of one finite fp32 value (RNE, saturating to +-448)."""
+    return int(_load().oracle_e4m3_encode(ctypes.c_float(v)))
+
+
+def e4m3_decode(c: int) -> float:
+    """Exact value of one E4M3 code (NaN for S.1111.111)."""
+    return float(_load().oracle_e4m3_decode(ctypes.c_uint8(c)))
+
+
+def e4m3_encode_array(v) -> np.ndarray:
+    """Element-wise ``e4m3_encode`` of a float32 array."""
+    v = np.ascontiguousarray(np.asarray(v, dtype=np.float32).ravel())
+    out = np.empty(v.shape[0], np.uint8)
+    _load().oracle_e4m3_encode_n(_ptr(v), v.shape[0], _ptr(out))
+    return out
+
+
+def e4m3_decode_table() -> np.ndarray:
+    """float64 value of every code 0..255."""
+    lib = _load()
+    return np.array([lib.oracle_e4m3_decode(ctypes.c_uint8(c)) for c in range(256)])
+
+
+def quant_act_1x128(x_bf16_bits):
+    """1x128 tile quantisation of a bf16 ``[M, K]`` matrix (given as uint16 bits).
+
+    Returns ``(q uint8 [M, K], sA float32 [K/128, M])``."""
+    x = _as_c(x_bf16_bits, np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((K // 128, M), np.float32)
+    _check(_load().oracle_quant_act_1x128(_ptr(x), M, K, K, _ptr(q), K, _ptr(s)), "quant_act")
+    return q, s
+
+
+def quant_w_128x128(w_bf16_bits):
+    """128x128 block quantisation of a bf16 ``[R, C]`` matrix (uint16 bits).
+
+    Returns ``(q uint8 [R, C], sW float32 [ceil(R/128), C/128])``."""
+    w = _as_c(w_bf16_bits, np.uint16)
+    R, C = w.shape
+    q = np.empty((R, C), np.uint8)
+    s = np.empty(((R + 127) // 128, C // 128), np.float32)
+    _check(_load().oracle_quant_w_128x128(_ptr(w), R, C, C, _ptr(q), C, _ptr(s)), "quant_w")
+    return q, s
+
+
+def _gemm_shapes(qA, qB, b_major):
+    M, K = qA.shape
+    if b_major == 0:
+        N, Kb = qB.shape
+    else:
+        Kb, N = qB.shape
+    if Kb != K:
+        raise ValueError("K mismatch")
+    return M, N, K
+
+
+def gemm_f64(qA, sA, qB, sB, b_major: int = 0) -> np.ndarray:
+    """float64 ``C = A^ . B^T`` over the dequantised operands.
+
+    ``b_major`` 0: ``qB`` is ``[N, K]`` with ``sB [ceil(N/128), K/128]``;
+    ``b_major`` 1: ``qB`` is ``[K, N]`` with ``sB [K/128, ceil(N/128)]``."""
+    qA, sA = _as_c(qA, np.uint8), _as_c(sA, np.float32)
+    qB, sB = _as_c(qB, np.uint8), _as_c(sB, np.float32)
+    M, N, K = _gemm_shapes(qA, qB, b_major)
+    C = np.empty((M, N), np.float64)
+    ldb = qB.shape[1]
+    _check(_load().oracle_gemm_f64(_ptr(qA), _ptr(sA), K, _ptr(qB), _ptr(sB), ldb, b_major,
+                                   M, N, K, _ptr(C), N), "gemm")
+    return C
+
+
+def gemm_f64_at(qA, sA, qB, sB, rows, cols, b_major: int = 0) -> np.ndarray:
+    """The float64 GEMM evaluated only at positions ``(rows[i], cols[i])``."""
+    qA, sA = _as_c(qA, np.uint8), _as_c(sA, np.float32)
+    qB, sB = _as_c(qB, np.uint8), _as_c(sB, np.float32)
+    rows = _as_c(np.asarray(rows, np.int64), np.int64)
+    cols = _as_c(np.asarray(cols, np.int64), np.int64)
+    M, N, K = _gemm_shapes(qA, qB, b_major)
+    out = np.empty(rows.shape[0], np.float64)
+    ldb = qB.shape[1]
+    _check(_load().oracle_gemm_f64_at(_ptr(qA), _ptr(sA), K, _ptr(qB), _ptr(sB), ldb, b_major,
+                                      M, N, K, _ptr(rows), _ptr(cols), rows.shape[0], _ptr(out)),
+           "gemm_at")
+    return out
+
+
+def grouped_gemm_f64(qA, sA, qB, sB, offsets) -> np.ndarray:
+    """Per-expert float64 GEMM: rows ``[off[e], off[e+1])`` of ``A`` times
+    expert ``e``'s ``qB[e] [N, K]`` (scales ``sB[e] [ceil(N/128), K/128]``)."""
+    qA, sA = _as_c(qA, np.uint8), _as_c(sA, np.float32)
+    qB, sB = _as_c(qB, np.uint8), _as_c(sB, np.float32)
+    off = _as_c(np.asarray(offsets, np.int32), np.int32)
+    M, K = qA.shape
+    E, N, Kb = qB.shape
+    if Kb != K or off.shape[0] != E + 1 or off[0] != 0 or off[-1] != M:
+        raise ValueError("bad grouped shapes/offsets")
+    C = np.zeros((M, N), np.float64)
+    _check(_load().oracle_grouped_gemm_f64(_ptr(qA), _ptr(sA), K, _ptr(qB), _ptr(sB), _ptr(off),
+                                           E, M, N, K, _ptr(C), N), "grouped_gemm")
+    return C
+
+
+def act_row_norms(qA, sA) -> np.ndarray:
+    """||A^[m, :]||_2 of the dequantised activation rows."""
+    qA, sA = _as_c(qA, np.uint8), _as_c(sA, np.float32)
+    M, K = qA.shape
+    out = np.empty(M, np.float64)
+    _load().oracle_act_row_norms(_ptr(qA), _ptr(sA), K, M, K, _ptr(out))
+    return out
+
+
+def b_row_norms(qB, sB, b_major: int = 0) -> np.ndarray:
+    """||B^[n, :]||_2 of the dequantised weight rows (rows of B^T's transpose)."""
+    qB, sB = _as_c(qB, np.uint8), _as_c(sB, np.float32)
+    if b_major == 0:
+        N, K = qB.shape
+    else:
+        K, N = qB.shape
+    out = np.empty(N, np.float64)
+    _load().oracle_b_row_norms(_ptr(qB), _ptr(sB), qB.shape[1], b_major, N, K, _ptr(out))
+    return out
+
+
+__all__ = ["e4m3_encode", "e4m3_decode", "e4m3_encode_array", "e4m3_decode_table",
+           "quant_act_1x128", "quant_w_128x128", "gemm_f64", "gemm_f64_at",
+           "grouped_gemm_f64", "act_row_norms", "b_row_norms"]

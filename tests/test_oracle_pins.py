@@ -1,0 +1,436 @@
+"""Pins for the CPU oracle (no GPU).
+
+The oracle is checked against things other than itself:
+  * torch's own float8_e4m3fn conversion (an independent E4M3 implementation)
+    for decoding every code and for encoding values below the rounding
+    boundary to 480;
+  * closed forms: saturation, ties-to-even midpoints, exact power-of-two
+    scales, constant and all-zero tiles, the E4M3 rounding-error bound;
+  * invariants the method fixes: the amax element maps to +-448, locality of
+    each 1x128 tile / 128x128 block (tile sizes read from the golden fixture
+    that cites the pages), quantise-then-gather == gather-then-quantise,
+    transposing a weight transposes its block grid;
+  * numpy float64 matmul on dequantised operands decoded by torch (brute force
+    on tiny shapes), and exact-arithmetic cases.
+Each group is chosen so that a plausible slip in the oracle (wrong exponent
+bias, rounding direction, subnormal formula, scale index, transposed operand,
+dropped block) fails at least one test here.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import bf16_bits, dense_case, normal_bf16, generator
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "fine_grained_tiling.txt")
+
+
+def golden_tiling():
+    vals = {}
+    with open(GOLDEN) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = int(v)
+    return vals
+
+
+def torch_decode(codes: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def torch_encode(v: np.ndarray) -> np.ndarray:
+    """torch float32 -> float8_e4m3fn (round to nearest even; NaN above 464)."""
+    t = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def f32_bits_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """fp32 values that are exactly representable in bf16 -> bf16 bit patterns."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0), "value not representable in bf16"
+    return (u >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
+    return (h.astype(np.uint32) << 16).view(np.float32)
+
+
+# ---------------------------------------------------------------- E4M3 codec
+def test_decode_matches_torch_for_all_codes():
+    ours = oracle.e4m3_decode_table()
+    ref = torch_decode(np.arange(256, dtype=np.uint8))
+    nan_codes = {0x7F, 0xFF}
+    for c in range(256):
+        if c in nan_codes:
+            assert np.isnan(ours[c]) and np.isnan(ref[c])
+        else:
+            assert ours[c] == ref[c], hex(c)
+    assert ours[0x7E] == 448.0 and ours[0xFE] == -448.0
+    assert ours[0x01] == 2.0 ** -9 and ours[0x08] == 2.0 ** -6
+
+
+def test_roundtrip_every_finite_code():
+    table = oracle.e4m3_decode_table()
+    for c in range(256):
+        if c in (0x7F, 0xFF):
+            continue
+        v = np.float32(table[c])
+        if c == 0x80:
+            v = np.float32(-0.0)
+        assert oracle.e4m3_encode(float(v)) == c, hex(c)
+
+
+def _structured_values():
+    """Every finite E4M3 value, every midpoint between neighbours, and the
+    fp32 values one and two ulps either side of each midpoint."""
+    table = oracle.e4m3_decode_table()
+    pos = np.array(sorted({table[c] for c in range(0x7F)}))      # 0 .. 448
+    mids = (pos[:-1] + pos[1:]) / 2.0                             # exact in fp32
+    vals = [pos.astype(np.float32), mids.astype(np.float32)]
+    m32 = mids.astype(np.float32)
+    for k in (1, 2):
+        up, dn = m32.copy(), m32.copy()
+        for _ in range(k):
+            up = np.nextafter(up, np.float32(np.inf))
+            dn = np.nextafter(dn, np.float32(0))
+        vals += [up, dn]
+    # below the smallest subnormal's half, around it, and the 448..464 band
+    vals.append(np.array([2.0 ** -10, 2.0 ** -11, 3 * 2.0 ** -11, 1e-30, 1e-45,
+                          448.0, 449.0, 456.0, 463.9], np.float32))
+    v = np.concatenate(vals)
+    return np.concatenate([v, -v])
+
+
+def test_encode_matches_torch_structured():
+    v = _structured_values()
+    assert np.all(np.abs(v) < 464)
+    np.testing.assert_array_equal(oracle.e4m3_encode_array(v), torch_encode(v))
+
+
+def test_encode_matches_torch_random_fp32():
+    rng = np.random.default_rng(1234)
+    # random bit patterns over the whole finite range below 464, incl. fp32 subnormals
+    bits = rng.integers(0, 0x43E80000, size=2_000_000, dtype=np.uint32)
+    v = bits.view(np.float32)
+    v = np.concatenate([v, -v, rng.uniform(-464, 464, 500_000).astype(np.float32)])
+    v = v[np.abs(v) < 464]
+    np.testing.assert_array_equal(oracle.e4m3_encode_array(v), torch_encode(v))
+
+
+def test_encode_saturates_finite():
+    big = np.array([448.0, 450.0, 463.99, 464.0, 470.0, 480.0, 1e6, 3.4e38], np.float32)
+    assert np.all(oracle.e4m3_encode_array(big) == 0x7E)
+    assert np.all(oracle.e4m3_encode_array(-big) == 0xFE)
+
+
+def test_ties_go_to_even_code():
+    table = oracle.e4m3_decode_table()
+    for c in range(0, 0x7E):
+        lo, hi = table[c], table[c + 1]
+        mid = np.float32((lo + hi) / 2)
+        want = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_encode(float(mid)) == want, hex(c)
+        assert oracle.e4m3_encode(float(-mid)) == (want | 0x80)
+
+
+def test_signed_zero_and_underflow_keep_sign():
+    assert oracle.e4m3_encode(0.0) == 0x00
+    assert oracle.e4m3_encode(-0.0) == 0x80
+    assert oracle.e4m3_encode(-1e-30) == 0x80
+    assert oracle.e4m3_encode(2.0 ** -10) == 0x00          # tie between 0 and 2^-9 -> even
+    assert oracle.e4m3_encode(np.nextafter(np.float32(2.0 ** -10), np.float32(1))) == 0x01
+
+
+# ---------------------------------------------------------------- quantisers
+def _random_act(M, K, seed=0, std=1.0):
+    g = generator(seed, "cpu")
+    return bf16_bits(normal_bf16((M, K), std, g, "cpu", outlier_p=0.01, outlier_scale=50.0))
+
+
+def test_scale_is_ieee_fp32_division_of_amax():
+    x = _random_act(64, 512)
+    q, s = oracle.quant_act_1x128(x)
+    xf = bf16_bits_to_f32(x).reshape(64, 4, 128)
+    amax = np.abs(xf).max(axis=2).T                       # [KB, M]
+    np.testing.assert_array_equal(s, amax / np.float32(448.0))
+    # binary64 then one rounding to binary32 is the same correctly-rounded
+    # quotient for binary32 operands (53 >= 2*24 + 2)
+    np.testing.assert_array_equal(s, (amax.astype(np.float64) / 448.0).astype(np.float32))
+
+
+def test_quant_act_matches_numpy_division_and_torch_encoder():
+    x = _random_act(96, 384, seed=3)
+    q, s = oracle.quant_act_1x128(x)
+    xf = bf16_bits_to_f32(x).reshape(96, 3, 128)
+    y = xf / s.T[:, :, None]                                # numpy IEEE fp32 division
+    assert np.all(np.abs(y) < 464)
+    np.testing.assert_array_equal(q.reshape(96, 3, 128), torch_encode(y).reshape(96, 3, 128))
+
+
+def test_amax_element_maps_to_448():
+    x = _random_act(128, 1024, seed=5)
+    q, s = oracle.quant_act_1x128(x)
+    xf = bf16_bits_to_f32(x).reshape(128, 8, 128)
+    idx = np.abs(xf).argmax(axis=2)
+    qm = np.take_along_axis(q.reshape(128, 8, 128), idx[:, :, None], axis=2)[:, :, 0]
+    sign = np.take_along_axis(xf, idx[:, :, None], axis=2)[:, :, 0] < 0
+    assert np.all(qm == np.where(sign, 0xFE, 0x7E))
+
+
+def test_constant_and_zero_tiles():
+    M, K = 4, 256
+    x = np.zeros((M, K), np.float32)
+    x[0, :128] = 3.0
+    x[1, :128] = -0.15625
+    x[2, 128:] = -0.0                                      # all-zero tile with -0
+    x[3, :] = 0.0
+    h = f32_bits_to_bf16_bits(x)
+    q, s = oracle.quant_act_1x128(h)
+    assert s[0, 0] == np.float32(3.0) / np.float32(448.0) and np.all(q[0, :128] == 0x7E)
+    assert s[0, 1] == np.float32(0.15625) / np.float32(448.0) and np.all(q[1, :128] == 0xFE)
+    assert s[1, 2] == 0.0 and np.all(q[2, 128:] == 0x80)
+    assert s[0, 3] == 0.0 and s[1, 3] == 0.0 and np.all(q[3] == 0x00)
+    assert np.all(q[0, 128:] == 0x00) and s[1, 0] == 0.0
+
+
+@pytest.mark.parametrize("k", [-20, -7, -1, 0, 3, 12])
+def test_power_of_two_amax_gives_exact_scale(k):
+    g = generator(7 + k + 20, "cpu")
+    xf = bf16_bits_to_f32(bf16_bits(normal_bf16((8, 128), 2.0 ** k * 100.0, g, "cpu")))
+    xf = np.clip(xf, -(448.0 * 2.0 ** k) * 0.999, 448.0 * 2.0 ** k * 0.999).astype(np.float32)
+    xf = bf16_bits_to_f32(f32_bits_to_bf16_bits(
+        (np.ascontiguousarray(xf).view(np.uint32) & 0xFFFF0000).view(np.float32)))
+    xf[:, 17] = np.float32(448.0 * 2.0 ** k)
+    xf[3, 17] = np.float32(-448.0 * 2.0 ** k)
+    q, s = oracle.quant_act_1x128(f32_bits_to_bf16_bits(xf))
+    assert np.all(s == np.float32(2.0 ** k))
+    np.testing.assert_array_equal(q, torch_encode(xf * np.float32(2.0 ** -k)).reshape(q.shape))
+
+
+def test_dequantised_error_within_e4m3_bound():
+    x = _random_act(64, 512, seed=11, std=3.0)
+    q, s = oracle.quant_act_1x128(x)
+    xf = bf16_bits_to_f32(x).astype(np.float64)
+    deq = torch_decode(q) * np.repeat(s.T, 128, axis=1).astype(np.float64)
+    sc = np.repeat(s.T, 128, axis=1).astype(np.float64)
+    bound = (2.0 ** -4 * np.abs(xf) + 2.0 ** -10 * sc) * (1 + 2.0 ** -20)
+    assert np.all(np.abs(deq - xf) <= bound)
+
+
+def test_subnormal_scales_are_kept():
+    x = np.zeros((2, 128), np.float32)
+    x[0, 5] = np.float32(2.0 ** -130)                      # bf16 subnormal
+    x[1, 9] = np.float32(-1.5 * 2.0 ** -120)
+    q, s = oracle.quant_act_1x128(f32_bits_to_bf16_bits(x))
+    assert s[0, 0] > 0 and s[0, 1] > 0
+    assert s[0, 0] == np.float32(2.0 ** -130) / np.float32(448.0)
+    assert s[0, 1] == np.float32(1.5 * 2.0 ** -120) / np.float32(448.0)
+    assert q[0, 5] == 0x7E and q[1, 9] == 0xFE
+
+
+def test_act_tile_locality_matches_golden_geometry():
+    geo = golden_tiling()
+    tc = geo["act_tile_cols"]
+    assert geo["act_tile_rows"] == 1
+    x = _random_act(8, 4 * tc, seed=21)
+    q0, s0 = oracle.quant_act_1x128(x)
+    assert s0.shape == (4, 8)
+    for col in (tc - 1, tc, 3 * tc - 1):
+        x1 = x.copy()
+        x1[5, col] = f32_bits_to_bf16_bits(np.array([1000.0], np.float32))[0]
+        q1, s1 = oracle.quant_act_1x128(x1)
+        kb = col // tc
+        changed_s = np.argwhere(s1 != s0)
+        assert changed_s.tolist() == [[kb, 5]]
+        rows, cols = np.nonzero(q1 != q0)
+        assert set(rows.tolist()) == {5}
+        assert cols.min() >= kb * tc and cols.max() < (kb + 1) * tc
+
+
+def test_quantise_then_gather_equals_gather_then_quantise():
+    x = _random_act(50, 256, seed=31)
+    rows = np.array([7, 7, 0, 49, 13, 2, 13, 30])
+    q, s = oracle.quant_act_1x128(x)
+    qg, sg = oracle.quant_act_1x128(x[rows])
+    np.testing.assert_array_equal(qg, q[rows])
+    np.testing.assert_array_equal(sg, s[:, rows])
+
+
+def _random_w(R, C, seed=0):
+    g = generator(seed, "cpu")
+    return bf16_bits(normal_bf16((R, C), 0.02, g, "cpu", outlier_p=0.001, outlier_scale=30.0))
+
+
+def test_weight_block_geometry_scale_and_locality():
+    geo = golden_tiling()
+    br, bc = geo["weight_block_rows"], geo["weight_block_cols"]
+    w = _random_w(3 * br, 2 * bc, seed=41)
+    q, s = oracle.quant_w_128x128(w)
+    wf = bf16_bits_to_f32(w).reshape(3, br, 2, bc)
+    amax = np.abs(wf).max(axis=(1, 3))
+    np.testing.assert_array_equal(s, amax / np.float32(448.0))
+    y = wf / s[:, None, :, None]
+    np.testing.assert_array_equal(q.reshape(3, br, 2, bc), torch_encode(y).reshape(3, br, 2, bc))
+    w1 = w.copy()
+    w1[br, bc - 1] = f32_bits_to_bf16_bits(np.array([5.0], np.float32))[0]
+    q1, s1 = oracle.quant_w_128x128(w1)
+    assert np.argwhere(s1 != s).tolist() == [[1, 0]]
+    r, c = np.nonzero(q1 != q)
+    assert r.min() >= br and r.max() < 2 * br and c.max() < bc
+
+
+def test_weight_partial_row_block_uses_existing_rows_only():
+    w = _random_w(200, 256, seed=43)
+    q, s = oracle.quant_w_128x128(w)
+    assert s.shape == (2, 2)
+    pad = np.zeros((256, 256), np.uint16)                   # +0 padding leaves amax unchanged
+    pad[:200] = w
+    qp, sp = oracle.quant_w_128x128(pad)
+    np.testing.assert_array_equal(s, sp)
+    np.testing.assert_array_equal(q, qp[:200])
+    tail = np.abs(bf16_bits_to_f32(w[128:])).reshape(72, 2, 128).max(axis=(0, 2))
+    np.testing.assert_array_equal(s[1], tail / np.float32(448.0))
+
+
+def test_weight_transpose_invariance():
+    w = _random_w(256, 384, seed=47)
+    q, s = oracle.quant_w_128x128(w)
+    qt, st = oracle.quant_w_128x128(np.ascontiguousarray(w.T))
+    np.testing.assert_array_equal(qt, q.T)
+    np.testing.assert_array_equal(st, s.T)
+
+
+# ---------------------------------------------------------------- GEMM
+def _deq_np(q, s_rows_by_k):
+    return torch_decode(q) * s_rows_by_k
+
+
+def _tiny_operands(M, N, K, seed):
+    c = dense_case("pin", M, N, K, seed=seed)
+    qa, sa = oracle.quant_act_1x128(bf16_bits(c.a))
+    qb, sb = oracle.quant_w_128x128(bf16_bits(c.w))
+    return qa, sa, qb, sb
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 128), (3, 5, 128), (8, 8, 256), (5, 130, 256)])
+def test_gemm_matches_numpy_matmul_of_torch_dequantised(M, N, K):
+    qa, sa, qb, sb = _tiny_operands(M, N, K, seed=M * 100 + N)
+    A = torch_decode(qa) * np.repeat(sa.T, 128, axis=1).astype(np.float64)
+    sb_full = np.repeat(np.repeat(sb, 128, axis=0)[:N], 128, axis=1).astype(np.float64)
+    B = torch_decode(qb) * sb_full
+    ref = A @ B.T
+    got = oracle.gemm_f64(qa, sa, qb, sb)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-300)
+    # brute-force triple loop over the torch-decoded values
+    for m in range(min(M, 3)):
+        for n in range(min(N, 3)):
+            acc = 0.0
+            for k in range(K):
+                acc += A[m, k] * B[n, k]
+            assert abs(got[m, n] - acc) <= 1e-12 * max(1.0, abs(acc))
+
+
+def test_gemm_constant_blocks_closed_form():
+    # every 1x128 tile of A constant and every 128x128 block of B constant in
+    # magnitude: all codes are +-448, so C = sum_kb 128 * 448^2 * sA*sB*sign
+    M, N, K = 3, 4, 384
+    a = np.zeros((M, K), np.float32)
+    b = np.zeros((N, K), np.float32)
+    av = [0.5, -2.0, 3.0]
+    bv = [0.25, -1.0, 0.75]
+    for kb in range(3):
+        for m in range(M):
+            a[m, kb * 128:(kb + 1) * 128] = av[(m + kb) % 3] * (m + 1)
+        for n in range(N):
+            b[n, kb * 128:(kb + 1) * 128] = bv[kb] * (-1.0 if n % 2 else 1.0)
+    qa, sa = oracle.quant_act_1x128(f32_bits_to_bf16_bits(a))
+    qb, sb = oracle.quant_w_128x128(f32_bits_to_bf16_bits(b))
+    got = oracle.gemm_f64(qa, sa, qb, sb)
+    for m in range(M):
+        for n in range(N):
+            want = 0.0
+            for kb in range(3):
+                sgn = float(np.sign(a[m, kb * 128]) * np.sign(b[n, kb * 128]))
+                want += 128 * 448.0 * 448.0 * float(sa[kb, m]) * float(sb[0, kb]) * sgn
+            assert got[m, n] == pytest.approx(want, rel=1e-14)
+
+
+def test_gemm_exact_powers_of_two():
+    # codes in {0, +-2^j}, power-of-two data: the result is an exact small integer
+    rng = np.random.default_rng(5)
+    M, N, K = 6, 7, 256
+    a = rng.choice([0.0, 1.0, -1.0, 2.0, -0.5, 448.0], size=(M, K)).astype(np.float32)
+    b = rng.choice([0.0, 1.0, -1.0, 4.0, -0.25, 448.0], size=(N, K)).astype(np.float32)
+    a[:, 0] = 448.0
+    a[:, 128] = 448.0
+    b[:, 0] = 448.0
+    b[:, 128] = 448.0
+    qa, sa = oracle.quant_act_1x128(f32_bits_to_bf16_bits(a))
+    qb, sb = oracle.quant_w_128x128(f32_bits_to_bf16_bits(b))
+    assert np.all(sa == 1.0) and np.all(sb == 1.0)
+    got = oracle.gemm_f64(qa, sa, qb, sb)
+    want = a.astype(np.float64) @ b.astype(np.float64).T
+    np.testing.assert_array_equal(got, want)
+
+
+def test_gemm_mn_major_b_equals_k_major():
+    qa, sa, qb, sb = _tiny_operands(4, 256, 256, seed=77)
+    c_k = oracle.gemm_f64(qa, sa, qb, sb, b_major=0)
+    qbt, sbt = np.ascontiguousarray(qb.T), np.ascontiguousarray(sb.T)
+    c_mn = oracle.gemm_f64(qa, sa, qbt, sbt, b_major=1)
+    np.testing.assert_array_equal(c_k, c_mn)
+
+
+def test_gemm_at_matches_full():
+    qa, sa, qb, sb = _tiny_operands(9, 140, 256, seed=13)
+    full = oracle.gemm_f64(qa, sa, qb, sb)
+    rows = np.array([0, 8, 3, 4])
+    cols = np.array([139, 0, 128, 77])
+    np.testing.assert_array_equal(oracle.gemm_f64_at(qa, sa, qb, sb, rows, cols), full[rows, cols])
+
+
+def test_grouped_equals_per_expert_dense():
+    rng = np.random.default_rng(9)
+    counts = [3, 0, 5, 1, 0]
+    E, N, K = len(counts), 136, 256
+    M = sum(counts)
+    qa, sa = oracle.quant_act_1x128(_random_act(M, K, seed=2))
+    qbs, sbs = [], []
+    for e in range(E):
+        qb, sb = oracle.quant_w_128x128(_random_w(N, K, seed=100 + e))
+        qbs.append(qb)
+        sbs.append(sb)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    got = oracle.grouped_gemm_f64(qa, sa, np.stack(qbs), np.stack(sbs), off)
+    for e in range(E):
+        r0, r1 = off[e], off[e + 1]
+        if r1 == r0:
+            continue
+        A = torch_decode(qa[r0:r1]) * np.repeat(sa[:, r0:r1].T, 128, axis=1)
+        sbf = np.repeat(np.repeat(sbs[e], 128, axis=0)[:N], 128, axis=1)
+        B = torch_decode(qbs[e]) * sbf
+        np.testing.assert_allclose(got[r0:r1], A @ B.T, rtol=1e-12, atol=1e-300)
+    del rng
+
+
+def test_row_norms_match_numpy():
+    qa, sa, qb, sb = _tiny_operands(5, 200, 256, seed=17)
+    A = torch_decode(qa) * np.repeat(sa.T, 128, axis=1)
+    B = torch_decode(qb) * np.repeat(np.repeat(sb, 128, axis=0)[:200], 128, axis=1)
+    np.testing.assert_allclose(oracle.act_row_norms(qa, sa), np.linalg.norm(A, axis=1), rtol=1e-13)
+    np.testing.assert_allclose(oracle.b_row_norms(qb, sb), np.linalg.norm(B, axis=1), rtol=1e-13)
+    np.testing.assert_allclose(oracle.b_row_norms(np.ascontiguousarray(qb.T),
+                                                  np.ascontiguousarray(sb.T), b_major=1),
+                               np.linalg.norm(B, axis=1), rtol=1e-13)
+
+
+def test_oracle_rejects_k_not_multiple_of_128():
+    with pytest.raises(ValueError):
+        oracle.quant_act_1x128(np.zeros((2, 100), np.uint16))
