@@ -1,0 +1,489 @@
+"""Benchmark of the fine-grained FP8 GEMM path on one node.
+
+One step = one pass of the whole path over one batch of synthetic input:
+    quantise A per 1x128 tile, quantise W per 128x128 block, block-scaled
+    FP8 GEMM with per-128-K promotion -> C (BF16)
+on the MLA query up-projection shape (A 4096x1536 with 0.1% x50 outliers,
+W 24576x1536, C 4096x24576) by default.  ``--workload`` selects another
+shape (mla_kv, dgrad, experts, tiny); for ``experts`` a step is the
+activation quantisation plus the grouped GEMM (expert weights are quantised
+once, before timing, as they are once per weight update).
+
+Printed (rank 0, one JSON line): whole-job GEMM TFLOP/s over the step time,
+per-kernel times from CUDA events on the launching stream, the GEMM's
+roofline fraction against the measured peaks, quantiser GB/s against HBM,
+an end-to-end number through the same C-ABI calls with pinned host buffers
+(host<->device copies inside the timed region), the oracle timed on a
+bounded sample on the host cores, and SM clocks sampled during the timed
+region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+Multi-GPU: launched by torch.distributed.run, each rank runs an independent
+replica (the path has no exchange step); the time is the max over ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 block-scaled GEMM TFLOP/s & % dense-FP8 peak; quantiser GB/s & % HBM"
+L2_BYTES = 126 * 1024 * 1024
+FP8_OVER_BF16 = 2.0          # nominal dense FP8 : BF16 tensor ratio (4.5 : 2.25 PFLOP/s)
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, every 200 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workloads
+def make_workload(name, device):
+    import synthetic
+    if name == "mla_q":
+        return synthetic.mla_q(device=device)
+    if name == "mla_kv":
+        return synthetic.mla_kv(device=device)
+    if name == "dgrad":
+        return synthetic.dgrad(device=device)
+    if name == "tiny":
+        return synthetic.tiny(device=device)
+    if name == "experts":
+        return synthetic.experts(device=device)
+    raise ValueError(name)
+
+
+class DenseStep:
+    """quant_act(A) + quant_w(W) + GEMM, over rotating input sets (> 2x L2)."""
+
+    def __init__(self, case, fp8, torch):
+        self.fp8, self.torch, self.case = fp8, torch, case
+        M, K, N = case.M, case.K, case.N
+        self.M, self.N, self.K, self.b_major = M, N, K, case.b_major
+        self.out_dtype = torch.float32 if case.out_fp32 else torch.bfloat16
+        in_bytes = (case.a.numel() + case.w.numel()) * 2
+        self.nsets = max(1, min(8, -(-2 * L2_BYTES // in_bytes) + 1))
+        self.sets = [(case.a, case.w)] + [(case.a.clone(), case.w.clone())
+                                          for _ in range(self.nsets - 1)]
+        dev = case.a.device
+        self.qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        self.sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+        self.qb = torch.empty(tuple(case.w.shape), dtype=torch.uint8, device=dev)
+        R, C = case.w.shape
+        self.sb = torch.empty(((R + 127) // 128, C // 128), dtype=torch.float32, device=dev)
+        self.c = torch.empty((M, N), dtype=self.out_dtype, device=dev)
+        self.flops = 2.0 * M * N * K
+        self.kernels = ["quant_act", "quant_w", "gemm"]
+        self.kernel_bytes = {
+            "quant_act": M * K * 3 + (K // 128) * M * 4,
+            "quant_w": R * C * 3 + self.sb.numel() * 4,
+            "gemm": M * K + R * C + (self.sa.numel() + self.sb.numel()) * 4 +
+                    M * N * self.c.element_size(),
+        }
+        self.h2d_bytes = in_bytes
+        self.d2h_bytes = M * N * self.c.element_size()
+        self.launches_per_step = 3
+
+    def run(self, i, events=None):
+        a, w = self.sets[i % self.nsets]
+        f = self.fp8
+        if events: events[0].record()
+        f.fp8_quant_act_1x128(a, self.qa, self.sa)
+        if events: events[1].record()
+        f.fp8_quant_w_128x128(w, self.qb, self.sb)
+        if events: events[2].record()
+        f.fp8_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major,
+                               C=self.c)
+        if events: events[3].record()
+
+    def run_host(self, host_a, host_w, host_c, dev_a, dev_w):
+        """End-to-end step from pinned host buffers through the C-ABI calls."""
+        dev_a.copy_(host_a, non_blocking=True)
+        dev_w.copy_(host_w, non_blocking=True)
+        f = self.fp8
+        f.fp8_quant_act_1x128(dev_a, self.qa, self.sa)
+        f.fp8_quant_w_128x128(dev_w, self.qb, self.sb)
+        f.fp8_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major,
+                               C=self.c)
+        host_c.copy_(self.c, non_blocking=True)
+
+
+class ExpertsStep:
+    """quant_act(X_sorted) + grouped GEMM (weights quantised once, untimed)."""
+
+    def __init__(self, case, fp8, torch):
+        self.fp8, self.torch, self.case = fp8, torch, case
+        E, N, K = case.w.shape
+        M = case.x_sorted.shape[0]
+        self.M, self.N, self.K, self.E = M, N, K, E
+        dev = case.x_sorted.device
+        qb, sb = fp8.fp8_quant_w_128x128(case.w.view(E * N, K))
+        self.qb, self.sb = qb.view(E, N, K), sb.view(E, -1, K // 128)
+        case.w = None                       # the BF16 weights are not needed any more
+        torch.cuda.empty_cache()
+        self.x = case.x_sorted
+        self.qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        self.sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+        self.c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.nsets = 1                      # 3.76 GB of expert weights stream per step (> L2)
+        self.flops = 2.0 * M * N * K
+        self.kernels = ["quant_act", "grouped_gemm"]
+        self.kernel_bytes = {
+            "quant_act": M * K * 3 + (K // 128) * M * 4,
+            "grouped_gemm": M * K + E * N * K + (self.sa.numel() + self.sb.numel()) * 4 + M * N * 2,
+        }
+        self.h2d_bytes = M * K * 2
+        self.d2h_bytes = M * N * 2
+        self.launches_per_step = 2
+
+    def run(self, i, events=None):
+        f = self.fp8
+        if events: events[0].record()
+        f.fp8_quant_act_1x128(self.x, self.qa, self.sa)
+        if events: events[1].record()
+        f.fp8_grouped_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, self.case.offsets,
+                                       C=self.c)
+        if events: events[2].record()
+
+    def run_host(self, host_a, host_w, host_c, dev_a, dev_w):
+        dev_a.copy_(host_a, non_blocking=True)
+        f = self.fp8
+        f.fp8_quant_act_1x128(dev_a, self.qa, self.sa)
+        f.fp8_grouped_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, self.case.offsets,
+                                       C=self.c)
+        host_c.copy_(self.c, non_blocking=True)
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(workload_name, case_cpu_fn, rows=8):
+    """The oracle, as it stands, on a bounded sample of the workload: quantise
+    `rows` rows of A and the whole weight, then the float64 GEMM of those rows
+    against every column.  Returns (flops, seconds, description)."""
+    import numpy as np
+    import oracle
+    import synthetic
+    a_bits, w_bits, b_major = case_cpu_fn()
+    t0 = time.perf_counter()
+    qa, sa = oracle.quant_act_1x128(a_bits[:rows])
+    qb, sb = oracle.quant_w_128x128(w_bits)
+    c = oracle.gemm_f64(qa, sa, qb, sb, b_major=b_major)
+    dt = time.perf_counter() - t0
+    K = a_bits.shape[1]
+    N = c.shape[1]
+    del np, synthetic
+    return 2.0 * rows * N * K, dt, (f"{rows} rows of A x all {N} columns (quantise those rows and "
+                                    f"the whole {w_bits.shape[0]}x{w_bits.shape[1]} weight, "
+                                    f"float64 GEMM), single-threaded C")
+
+
+def dense_host_inputs(case):
+    import synthetic
+    return synthetic.bf16_bits(case.a), synthetic.bf16_bits(case.w), case.b_major
+
+
+# ---------------------------------------------------------------- main arms
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    import fp8_fine_grained_26_b300 as fp8
+    device = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+
+    case = make_workload(args.workload, device)
+    step = ExpertsStep(case, fp8, torch) if args.workload == "experts" else DenseStep(case, fp8, torch)
+    stream = torch.cuda.current_stream()
+
+    for i in range(args.warmup):
+        step.run(i)
+    if fp8.fp8bs_last_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    nk = len(step.kernels)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)                         # the sampler's first sample lands in the region
+    t_start.record(stream)
+    for i in range(args.steps):
+        step.run(i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    if fp8.fp8bs_last_error() != 0:
+        raise RuntimeError("device error in the timed region")
+
+    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks(elapsed_ms, world, device)
+    per_kernel = {}
+    for j, name in enumerate(step.kernels):
+        per_kernel[name] = sum(e[j].elapsed_time(e[j + 1]) for e in evs) / args.steps
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step.flops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end-to-end through the same C-ABI calls from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        if args.workload == "experts":
+            host_a = step.x.cpu().pin_memory()
+            host_w = None
+            dev_a, dev_w = torch.empty_like(step.x), None
+        else:
+            host_a = case.a.cpu().pin_memory()
+            host_w = case.w.cpu().pin_memory()
+            dev_a, dev_w = torch.empty_like(case.a), torch.empty_like(case.w)
+        host_c = torch.empty(tuple(step.c.shape), dtype=step.c.dtype).pin_memory()
+        for _ in range(2):
+            step.run_host(host_a, host_w, host_c, dev_a, dev_w)
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 20))
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n_e2e):
+            step.run_host(host_a, host_w, host_c, dev_a, dev_w)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device) / n_e2e
+        e2e = {"value": round(world * step.flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "ms_per_step": round(e2e_ms, 4), "steps": n_e2e,
+               "h2d_bytes_per_step": int(step.h2d_bytes), "d2h_bytes_per_step": int(step.d2h_bytes)}
+
+    # ---- roofline of the dominant kernel (the GEMM) and the quantisers
+    gemm_name = step.kernels[-1]
+    gemm_ms = per_kernel[gemm_name]
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    fp8_peak_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP8_OVER_BF16
+    achieved = step.flops / (gemm_ms * 1e-3) / 1e12
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            tr = json.load(f).get(f"{gemm_name}:{args.workload}")
+        if tr is not None:
+            traffic = tr
+    roofline = {"kernel": gemm_name, "bound": "tensor", "achieved": round(achieved, 1),
+                "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
+                "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 burst x {FP8_OVER_BF16} (nominal FP8:BF16)",
+                "frac_of_sustained": round(achieved / fp8_peak_sust, 4)}
+    hbm = peaks["hbm_gbs"]
+    kernels = {}
+    for name in step.kernels:
+        ms = per_kernel[name]
+        gbs = step.kernel_bytes[name] / (ms * 1e-3) / 1e9
+        entry = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
+        if name in ("gemm", "grouped_gemm"):
+            entry["TFLOP/s"] = round(achieved, 1)
+            entry["frac_fp8_peak"] = round(achieved / fp8_peak, 4)
+        kernels[name] = entry
+
+    # ---- CPU baseline (oracle) on a bounded sample, rank 0 at N=1 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu and args.workload != "experts":
+        flops, secs, desc = oracle_sample(args.workload, lambda: dense_host_inputs(case))
+        cpu = {"value": round(flops / secs / 1e12, 9), "unit": "TFLOP/s", "cores": 1,
+               "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
+            "config": {"workload": case.name if hasattr(case, "name") else args.workload,
+                       "M": step.M, "N": step.N, "K": step.K,
+                       "step": " + ".join(step.kernels),
+                       "out": "bf16" if step.c.dtype == torch.bfloat16 else "fp32",
+                       "l2": (f"inputs rotate over {step.nsets} sets (> 2x the 126 MB L2)"
+                              if step.nsets > 1 else "inputs larger than L2"),
+                       "parallelism": f"replicas x{world}"},
+            "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": step.launches_per_step * args.steps * world,
+            "clocks": clk,
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step a bounded sample -- one row
+    of A and one 128-column block of the weight quantised, and their 1x128
+    float64 GEMM block."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    if args.workload == "experts":
+        print(json.dumps({"impl": "reference", "unavailable":
+                          "the oracle arm samples the dense workloads only"}), flush=True)
+        return
+    import numpy as np
+    import oracle
+    import synthetic
+    case = make_workload(args.workload, "cpu")
+    a_bits, w_bits = synthetic.bf16_bits(case.a), synthetic.bf16_bits(case.w)
+    b_major, K, N = case.b_major, case.K, case.N
+    NB = (N + 127) // 128
+
+    def one(i):
+        m = i % a_bits.shape[0]
+        nb = i % NB
+        qa, sa = oracle.quant_act_1x128(a_bits[m:m + 1])
+        if b_major == 0:
+            blk = np.ascontiguousarray(w_bits[nb * 128:(nb + 1) * 128])
+        else:
+            blk = np.ascontiguousarray(w_bits[:, nb * 128:(nb + 1) * 128])
+        qb, sb = oracle.quant_w_128x128(blk)
+        c = oracle.gemm_f64(qa, sa, qb, sb, b_major)
+        return 2.0 * K * c.shape[1]
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for i in range(args.steps):
+        flops += one(i)
+    dt = time.perf_counter() - t0
+    v = flops / dt / 1e12
+    out = {"metric": METRIC, "impl": "reference", "value": round(v, 9), "unit": "TFLOP/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+           "config": {"workload": case.name, "M": case.M, "N": case.N, "K": case.K},
+           "cpu_baseline": {"value": round(v, 9), "unit": "TFLOP/s", "kind": "oracle", "cores": 1,
+                            "sample": "per step: one row of A and one 128-column block of the "
+                                      "weight quantised, and their 1x128 float64 GEMM block"},
+           "e2e": {"value": round(v, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="mla_q",
+                    choices=["mla_q", "mla_kv", "dgrad", "experts", "tiny"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end run")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+"""Python binding of the fine-grained FP8 block-scaled GEMM library.
+
+Argument marshalling only: every function here checks tensor dtypes, shapes
+and devices, allocates outputs with torch when the caller did not pass them,
+and calls the same-named C entry point of ``libfp8bs.so`` (declared in
+``include/fp8bs.h``) on the current torch CUDA stream.  All arithmetic runs
+in the library's CUDA kernels; there is no fallback of any kind.  Importing
+this package fails if the library has not been built.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
+
+FP8BS_OK = 0
+FP8BS_ERR_NULL = -1
+FP8BS_ERR_SHAPE = -2
+FP8BS_ERR_ALIGN = -3
+FP8BS_ERR_ARG = -4
+FP8BS_ERR_LAUNCH = -5
+FP8BS_ERR_DEVICE = -6
+FP8BS_ERR_TIMEOUT = -7
+OUT_BF16, OUT_FP32 = 0, 1
+B_KMAJOR, B_MNMAJOR = 0, 1
+
+_STATUS_NAMES = {
+    FP8BS_ERR_NULL: "FP8BS_ERR_NULL", FP8BS_ERR_SHAPE: "FP8BS_ERR_SHAPE",
+    FP8BS_ERR_ALIGN: "FP8BS_ERR_ALIGN", FP8BS_ERR_ARG: "FP8BS_ERR_ARG",
+    FP8BS_ERR_LAUNCH: "FP8BS_ERR_LAUNCH", FP8BS_ERR_DEVICE: "FP8BS_ERR_DEVICE",
+    FP8BS_ERR_TIMEOUT: "FP8BS_ERR_TIMEOUT",
+}
+
+EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
+            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error")
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, status, call):
+        self.status = status
+        super().__init__(f"{call} returned {_STATUS_NAMES.get(status, status)}")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                          "(python -m fp8_fine_grained_26_b300.build)")
+    lib = ctypes.CDLL(LIB_PATH)
+    i64, p, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    sigs = {
+        "fp8_quant_act_1x128": [p, i64, i64, i64, p, i64, p, p],
+        "fp8_quant_w_128x128": [p, i64, i64, i64, p, i64, p, p],
+        "fp8_gemm_blockscaled": [p, p, p, p, i64, i64, i64, i32, p, i32, i64, p],
+        "fp8_grouped_gemm_blockscaled": [p, p, p, p, p, i32, i64, i64, i64, p, i32, i64, p],
+        "fp8bs_last_error": [p],
+    }
+    for name, args in sigs.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    return lib
+
+
+lib = _load()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else ctypes.c_void_p(0)
+
+
+def _check(status, call):
+    if status != FP8BS_OK:
+        raise Fp8bsError(status, call)
+
+
+def _need(t, dtype, name, ndim):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or t.dim() != ndim or not t.is_cuda:
+        raise TypeError(f"{name}: expected a {ndim}-D CUDA tensor of {dtype}")
+
+
+def _row_major(t, name):
+    if t.dim() >= 1 and t.numel() > 0 and t.stride(-1) != 1:
+        raise ValueError(f"{name}: innermost dimension must be contiguous")
+
+
+def fp8_quant_act_1x128(x, q=None, sA=None, stream=None):
+    """1x128 tile quantisation of BF16 ``x [M, K]`` (row stride may exceed K).
+
+    Returns ``(q uint8 [M, K], sA float32 [K/128, M])``; E4M3 codes are
+    returned as their bytes (view them as ``torch.float8_e4m3fn`` if wanted)."""
+    _need(x, torch.bfloat16, "x", 2)
+    _row_major(x, "x")
+    M, K = x.shape
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if sA is None:
+        sA = torch.empty((K // 128, M), dtype=torch.float32, device=x.device)
+    _need(q, torch.uint8, "q", 2)
+    _row_major(q, "q")
+    if tuple(q.shape) != (M, K) or not sA.is_contiguous() or sA.numel() != (K // 128) * M:
+        raise ValueError("output shapes do not match x")
+    ldx = x.stride(0) if M > 0 else K
+    ldq = q.stride(0) if M > 0 else K
+    _check(lib.fp8_quant_act_1x128(_ptr(x), M, K, ldx, _ptr(q), ldq, _ptr(sA), _stream(stream)),
+           "fp8_quant_act_1x128")
+    return q, sA
+
+
+def fp8_quant_w_128x128(w, q=None, sW=None, stream=None):
+    """128x128 block quantisation of BF16 ``w [R, C]``.
+
+    Returns ``(q uint8 [R, C], sW float32 [ceil(R/128), C/128])``."""
+    _need(w, torch.bfloat16, "w", 2)
+    _row_major(w, "w")
+    R, C = w.shape
+    if q is None:
+        q = torch.empty((R, C), dtype=torch.uint8, device=w.device)
+    if sW is None:
+        sW = torch.empty(((R + 127) // 128, C // 128), dtype=torch.float32, device=w.device)
+    _need(q, torch.uint8, "q", 2)
+    _row_major(q, "q")
+    if tuple(q.shape) != (R, C) or not sW.is_contiguous() or \
+            sW.numel() != ((R + 127) // 128) * (C // 128):
+        raise ValueError("output shapes do not match w")
+    ldw = w.stride(0) if R > 0 else C
+    ldq = q.stride(0) if R > 0 else C
+    _check(lib.fp8_quant_w_128x128(_ptr(w), R, C, ldw, _ptr(q), ldq, _ptr(sW), _stream(stream)),
+           "fp8_quant_w_128x128")
+    return q, sW
+
+
+def _out(C, M, N, out_dtype, device):
+    if C is None:
+        C = torch.empty((M, N), dtype=out_dtype, device=device)
+    if C.dtype not in (torch.bfloat16, torch.float32) or C.dim() != 2 or \
+            tuple(C.shape) != (M, N) or not C.is_cuda:
+        raise ValueError("C must be a [M, N] CUDA tensor of bfloat16 or float32")
+    _row_major(C, "C")
+    ldc = C.stride(0) if M > 0 else N
+    return C, (OUT_FP32 if C.dtype == torch.float32 else OUT_BF16), ldc
+
+
+def fp8_gemm_blockscaled(qA, sA, qB, sB, b_major=B_KMAJOR, out_dtype=torch.bfloat16, C=None,
+                         stream=None):
+    """``C = A . B^T`` from 1x128-quantised ``qA [M, K]`` / ``sA [K/128, M]`` and
+    128x128-quantised B: ``qB [N, K]`` / ``sB [ceil(N/128), K/128]`` (K-major),
+    or ``qB [K, N]`` / ``sB [K/128, N/128]`` (``b_major=B_MNMAJOR``)."""
+    _need(qA, torch.uint8, "qA", 2)
+    _need(qB, torch.uint8, "qB", 2)
+    _need(sA, torch.float32, "sA", 2)
+    _need(sB, torch.float32, "sB", 2)
+    for t, n in ((qA, "qA"), (qB, "qB"), (sA, "sA"), (sB, "sB")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    M, K = qA.shape
+    if b_major == B_KMAJOR:
+        N, Kb = qB.shape
+    else:
+        Kb, N = qB.shape
+    if Kb != K:
+        raise ValueError("qA and qB disagree on K")
+    C, cd, ldc = _out(C, M, N, out_dtype, qA.device)
+    _check(lib.fp8_gemm_blockscaled(_ptr(qA), _ptr(sA), _ptr(qB), _ptr(sB), M, N, K, b_major,
+                                    _ptr(C), cd, ldc, _stream(stream)), "fp8_gemm_blockscaled")
+    return C
+
+
+def fp8_grouped_gemm_blockscaled(qA, sA, qB, sB, seg_offsets, out_dtype=torch.bfloat16, C=None,
+                                 stream=None):
+    """Per-expert ``C[rows of e] = A[rows of e] . B_e^T`` with ``qB [E, N, K]``,
+    ``sB [E, ceil(N/128), K/128]`` and device ``seg_offsets int32 [E+1]``."""
+    _need(qA, torch.uint8, "qA", 2)
+    _need(qB, torch.uint8, "qB", 3)
+    _need(sA, torch.float32, "sA", 2)
+    _need(sB, torch.float32, "sB", 3)
+    _need(seg_offsets, torch.int32, "seg_offsets", 1)
+    for t, n in ((qA, "qA"), (qB, "qB"), (sA, "sA"), (sB, "sB"), (seg_offsets, "seg_offsets")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    M, K = qA.shape
+    E, N, Kb = qB.shape
+    if Kb != K or seg_offsets.numel() != E + 1:
+        raise ValueError("grouped GEMM shapes disagree")
+    C, cd, ldc = _out(C, M, N, out_dtype, qA.device)
+    _check(lib.fp8_grouped_gemm_blockscaled(_ptr(qA), _ptr(sA), _ptr(qB), _ptr(sB),
+                                            _ptr(seg_offsets), E, M, N, K, _ptr(C), cd, ldc,
+                                            _stream(stream)), "fp8_grouped_gemm_blockscaled")
+    return C
+
+
+def fp8bs_last_error(stream=None):
+    """Synchronise the stream and return (and clear) the device error status."""
+    return lib.fp8bs_last_error(_stream(stream))
+
+
+__all__ = ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
+           "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "Fp8bsError", "lib",
+           "LIB_PATH", "EXPORTED", "B_KMAJOR", "B_MNMAJOR", "OUT_BF16", "OUT_FP32"]

@@ -1,0 +1,330 @@
+// fp8bs.cu -- the C ABI of the library (see include/fp8bs.h): argument
+// validation, TMA tensor-map encoding and kernel launches.  One translation
+// unit so that the device error word is a single symbol per device.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "fp8bs.h"
+#include "ptx.cuh"
+#include "quant.cuh"
+#include "gemm.cuh"
+
+namespace {
+
+using namespace fp8bs;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool probed = false;
+    bool is_sm103 = false;
+    int num_sms = 0;
+    bool attrs_set = false;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Current device, checked to be sm_103; fills `info`.
+int current_device(DeviceInfo **info)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return FP8BS_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FP8BS_ERR_DEVICE;
+        d.is_sm103 = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        d.probed = true;
+    }
+    if (!d.is_sm103)
+        return FP8BS_ERR_DEVICE;
+    if (!d.attrs_set) {
+        if (cudaFuncSetAttribute(fp8_gemm_kernel<false, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 gemm_smem_bytes(false)) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 gemm_smem_bytes(false)) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<true, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 gemm_smem_bytes(true)) != cudaSuccess)
+            return FP8BS_ERR_LAUNCH;
+        d.attrs_set = true;
+    }
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return FP8BS_ERR_DEVICE;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *info = &d;
+    return FP8BS_OK;
+}
+
+int launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
+}
+
+// Row-major uint8 matrix [rows][cols] (row stride ld bytes) as a 2-D tensor
+// map with a box of box_cols x box_rows and 128-byte swizzle.
+bool encode_2d_u8(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld,
+                  uint32_t box_cols, uint32_t box_rows)
+{
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {ld};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_3d_u8(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                  uint32_t b0, uint32_t b1)
+{
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0, d0 * d1};
+    const cuuint32_t box[3] = {b0, b1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int c_vector_ok(const void *C, int c_dtype, int64_t ldc)
+{
+    const int64_t es = c_dtype == FP8BS_OUT_FP32 ? 4 : 2;
+    return aligned16(C) && (ldc * es) % 16 == 0;
+}
+
+int zero_output(void *C, int c_dtype, int64_t ldc, int64_t M, int64_t N, cudaStream_t stream)
+{
+    const size_t es = c_dtype == FP8BS_OUT_FP32 ? 4 : 2;
+    if (cudaMemset2DAsync(C, (size_t)ldc * es, 0, (size_t)N * es, (size_t)M, stream) != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    return FP8BS_OK;
+}
+
+int check_gemm_common(const void *qA, const float *sA, const void *qB, const float *sB,
+                      int64_t M, int64_t N, int64_t K, void *C, int c_dtype, int64_t ldc)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 128 != 0)
+        return FP8BS_ERR_SHAPE;
+    if (c_dtype != FP8BS_OUT_BF16 && c_dtype != FP8BS_OUT_FP32)
+        return FP8BS_ERR_ARG;
+    if (M == 0 || N == 0)
+        return FP8BS_OK;
+    if (!C || (K > 0 && (!qA || !sA || !qB || !sB)))
+        return FP8BS_ERR_NULL;
+    if (ldc < N)
+        return FP8BS_ERR_SHAPE;
+    const uintptr_t es = c_dtype == FP8BS_OUT_FP32 ? 4 : 2;
+    if ((reinterpret_cast<uintptr_t>(C) % es) != 0)
+        return FP8BS_ERR_ALIGN;
+    if (K > 0 && (!aligned16(qA) || !aligned16(qB) || !aligned4(sA) || !aligned4(sB)))
+        return FP8BS_ERR_ALIGN;
+    if (M > INT32_MAX || N > INT32_MAX - 2 * BN || K > INT32_MAX)
+        return FP8BS_ERR_SHAPE;
+    return FP8BS_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+int fp8_quant_act_1x128(const void *x_bf16, int64_t M, int64_t K, int64_t ldx, void *q_e4m3,
+                        int64_t ldq, float *sA, cudaStream_t stream)
+{
+    if (M < 0 || K < 0 || K % 128 != 0)
+        return FP8BS_ERR_SHAPE;
+    if (M == 0 || K == 0)
+        return FP8BS_OK;
+    if (!x_bf16 || !q_e4m3 || !sA)
+        return FP8BS_ERR_NULL;
+    if (ldx < K || ldq < K)
+        return FP8BS_ERR_SHAPE;
+    if (!aligned16(x_bf16) || !aligned16(q_e4m3) || !aligned4(sA) || (ldx * 2) % 16 != 0 ||
+        ldq % 16 != 0)
+        return FP8BS_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    const int64_t tiles = M * (K / 128);
+    const int64_t warps = (tiles + 1) / 2;
+    const int64_t max_blocks = (int64_t)dev->num_sms * 8;
+    const int blocks = (int)std::min<int64_t>((warps + 7) / 8, max_blocks);
+    quant_act_1x128_kernel<<<blocks, 256, 0, stream>>>(
+        static_cast<const uint16_t *>(x_bf16), M, K / 128, ldx, static_cast<uint8_t *>(q_e4m3),
+        ldq, sA);
+    return launch_status();
+}
+
+int fp8_quant_w_128x128(const void *w_bf16, int64_t R, int64_t C, int64_t ldw, void *q_e4m3,
+                        int64_t ldq, float *sW, cudaStream_t stream)
+{
+    if (R < 0 || C < 0 || C % 128 != 0)
+        return FP8BS_ERR_SHAPE;
+    if (R == 0 || C == 0)
+        return FP8BS_OK;
+    if (!w_bf16 || !q_e4m3 || !sW)
+        return FP8BS_ERR_NULL;
+    if (ldw < C || ldq < C)
+        return FP8BS_ERR_SHAPE;
+    if (!aligned16(w_bf16) || !aligned16(q_e4m3) || !aligned4(sW) || (ldw * 2) % 16 != 0 ||
+        ldq % 16 != 0)
+        return FP8BS_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    const int64_t RB = (R + 127) / 128, CB = C / 128;
+    if (RB * CB > INT32_MAX)
+        return FP8BS_ERR_SHAPE;
+    quant_w_128x128_kernel<<<(unsigned)(RB * CB), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(w_bf16), R, CB, ldw, static_cast<uint8_t *>(q_e4m3), ldq,
+        sW);
+    return launch_status();
+}
+
+int fp8_gemm_blockscaled(const void *qA, const float *sA, const void *qB, const float *sB,
+                         int64_t M, int64_t N, int64_t K, int b_major, void *C, int c_dtype,
+                         int64_t ldc, cudaStream_t stream)
+{
+    if (b_major != FP8BS_B_KMAJOR && b_major != FP8BS_B_MNMAJOR)
+        return FP8BS_ERR_ARG;
+    if (int st = check_gemm_common(qA, sA, qB, sB, M, N, K, C, c_dtype, ldc))
+        return st;
+    if (M == 0 || N == 0)
+        return FP8BS_OK;
+    if (b_major == FP8BS_B_MNMAJOR && N % 128 != 0)
+        return FP8BS_ERR_SHAPE;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    if (K == 0)
+        return zero_output(C, c_dtype, ldc, M, N, stream);
+
+    CUtensorMap tmA, tmB;
+    if (!encode_2d_u8(&tmA, qA, (uint64_t)K, (uint64_t)M, (uint64_t)K, BK, BM))
+        return FP8BS_ERR_ARG;
+    bool ok;
+    if (b_major == FP8BS_B_KMAJOR)
+        ok = encode_2d_u8(&tmB, qB, (uint64_t)K, (uint64_t)N, (uint64_t)K, BK, BN);
+    else
+        ok = encode_2d_u8(&tmB, qB, (uint64_t)N, (uint64_t)K, (uint64_t)N, 128, BK);
+    if (!ok)
+        return FP8BS_ERR_ARG;
+
+    GemmArgs g{};
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.ldc = ldc;
+    g.sA = sA;
+    g.sB = sB;
+    g.C = C;
+    g.offsets = nullptr;
+    g.E = 1;
+    g.c_fp32 = c_dtype == FP8BS_OUT_FP32;
+    g.c_vec = c_vector_ok(C, c_dtype, ldc);
+    g.num_m_blk = (int)((M + BM - 1) / BM);
+    g.num_n_blk = (int)((N + BN - 1) / BN);
+    g.KB = (int)(K / BK);
+    g.NB128 = (int)((N + 127) / 128);
+    g.num_tiles = (int64_t)g.num_m_blk * g.num_n_blk;
+    const int grid = (int)std::min<int64_t>(g.num_tiles, dev->num_sms);
+    if (b_major == FP8BS_B_KMAJOR)
+        fp8_gemm_kernel<false, false><<<grid, GEMM_THREADS, gemm_smem_bytes(false), stream>>>(tmA, tmB, g);
+    else
+        fp8_gemm_kernel<false, true><<<grid, GEMM_THREADS, gemm_smem_bytes(false), stream>>>(tmA, tmB, g);
+    return launch_status();
+}
+
+int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA, const void *qB,
+                                 const float *sB, const int32_t *seg_offsets, int E,
+                                 int64_t M_total, int64_t N, int64_t K, void *C, int c_dtype,
+                                 int64_t ldc, cudaStream_t stream)
+{
+    if (E < 1 || E > MAX_EXPERTS)
+        return FP8BS_ERR_ARG;
+    if (int st = check_gemm_common(qA, sA, qB, sB, M_total, N, K, C, c_dtype, ldc))
+        return st;
+    if (M_total == 0 || N == 0)
+        return FP8BS_OK;
+    if (!seg_offsets)
+        return FP8BS_ERR_NULL;
+    if (!aligned4(seg_offsets))
+        return FP8BS_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    if (K == 0)
+        return zero_output(C, c_dtype, ldc, M_total, N, stream);
+
+    CUtensorMap tmA, tmB;
+    if (!encode_2d_u8(&tmA, qA, (uint64_t)K, (uint64_t)M_total, (uint64_t)K, BK, BM))
+        return FP8BS_ERR_ARG;
+    if (!encode_3d_u8(&tmB, qB, (uint64_t)K, (uint64_t)N, (uint64_t)E, BK, BN))
+        return FP8BS_ERR_ARG;
+
+    GemmArgs g{};
+    g.M = M_total;
+    g.N = N;
+    g.K = K;
+    g.ldc = ldc;
+    g.sA = sA;
+    g.sB = sB;
+    g.C = C;
+    g.offsets = seg_offsets;
+    g.E = E;
+    g.c_fp32 = c_dtype == FP8BS_OUT_FP32;
+    g.c_vec = c_vector_ok(C, c_dtype, ldc);
+    g.num_m_blk = 0;
+    g.num_n_blk = (int)((N + BN - 1) / BN);
+    g.KB = (int)(K / BK);
+    g.NB128 = (int)((N + 127) / 128);
+    g.num_tiles = 0;
+    fp8_gemm_kernel<true, false><<<dev->num_sms, GEMM_THREADS, gemm_smem_bytes(true), stream>>>(tmA, tmB, g);
+    return launch_status();
+}
+
+int fp8bs_last_error(cudaStream_t stream)
+{
+    if (cudaStreamSynchronize(stream) != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    if (cudaGetLastError() != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof word) != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero) != cudaSuccess)
+            return FP8BS_ERR_LAUNCH;
+        return FP8BS_ERR_TIMEOUT;
+    }
+    return FP8BS_OK;
+}
+
+} // extern "C"

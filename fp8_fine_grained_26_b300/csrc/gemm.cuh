@@ -1,0 +1,475 @@
+// gemm.cuh -- block-scaled FP8 GEMM with per-128-K promotion (dense and
+// grouped-by-expert), sm_103a.
+//
+// What it computes ["DeepSeek-V3 Technical Report digest", section 3: all
+// GEMMs in FP8, partial results promoted to FP32 every 128 accumulated
+// elements; "DeepSeek-V3 training walkthrough", section 二(四): MMA
+// intermediate results accumulated in FP32 registers; qqstock.cn walkthrough,
+// report figure 7b]:
+//     C[m][n] = sum_kb sA[kb][m] * sB(n, kb) * P_kb[m][n],
+//     P_kb[m][n] = sum_{k in 128-wide slice kb} qA[m][k] * qB(n, k)   (exact FP8 products)
+//
+// Design (one persistent CTA per SM, 384 threads, 128 x 256 output tile):
+//   warp 0      TMA producer: one 128-K slice of A (128x128 B) and B (256x128 B)
+//               per pipeline stage, 128-byte swizzle, STAGES-deep ring.
+//   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) write a
+//               FRESH 128x256 FP32 partial P_kb into one of two TMEM buffers
+//               (2 x 256 columns = all 512), then tcgen05.commit frees the
+//               smem stage and signals the partial.
+//   warps 4-11  promote / epilogue: two warpgroups, each owning 128 of the
+//               256 columns; thread = tile row.  Per slice they load the
+//               partial from TMEM (tcgen05.ld 32x32b) and apply
+//               acc = fma(P, sA*sB, acc) in FP32 registers -- the pages'
+//               promotion, on CUDA cores -- then release the TMEM buffer so
+//               the MMA of slice kb+2 can start while slice kb+1 is promoted.
+//               After the last slice they round acc to BF16 (or keep FP32)
+//               and store the tile, masking rows >= M (or the expert's segment
+//               end) and columns >= N.
+//   warps 2-3   idle.
+// Every mbarrier wait is bounded (WAIT_LIMIT_NS); on expiry the kernel sets
+// the device error word, stops all roles, drains its own TMA copies and MMAs,
+// frees TMEM and returns.
+#pragma once
+#include "ptx.cuh"
+
+namespace fp8bs {
+
+__device__ unsigned int g_error_word;   // bit 0: a pipeline wait timed out
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK;                   // 16 KiB
+constexpr int B_STAGE_BYTES = BN * BK;                   // 32 KiB
+constexpr int GEMM_THREADS = 384;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;        // 2 s
+constexpr int MAX_EXPERTS = 4096;
+
+// Shared-memory layout (offsets from a 1024-byte aligned base).
+constexpr int SMEM_A = 0;
+constexpr int SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
+constexpr int SMEM_BAR = SMEM_B + STAGES * B_STAGE_BYTES;            // 8-byte barriers
+constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;                     // full, empty, pfull, pempty, drain
+constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;                   // tmem slot, abort flag
+constexpr int SMEM_TILES = SMEM_MISC + 16;                           // grouped: tile prefix [E+1]
+constexpr int gemm_smem_bytes(bool grouped)
+{
+    return 1024 + SMEM_TILES + (grouped ? (MAX_EXPERTS + 1) * 4 : 0);
+}
+
+struct GemmArgs {
+    int64_t M;          // rows of A (grouped: M_total)
+    int64_t N, K;
+    int64_t ldc;
+    const float *sA;    // [K/128][M]
+    const float *sB;    // K-major: [ceil(N/128)][K/128] (grouped: per expert); MN-major: [K/128][N/128]
+    void *C;
+    const int32_t *offsets;   // grouped: [E+1]
+    int E;
+    int c_fp32;
+    int c_vec;          // C base and row stride allow 16-byte vector stores
+    int num_m_blk;      // dense: ceil(M/128)
+    int num_n_blk;      // ceil(N/256)
+    int KB;             // K/128
+    int NB128;          // ceil(N/128)
+    int64_t num_tiles;  // dense: num_m_blk * num_n_blk
+};
+
+// tcgen05 instruction descriptor, kind::f8f6f4: D = F32 (bits 4-5 = 1),
+// A = B = E4M3 (bits 7-9, 10-12 = 0), A K-major (bit 15 = 0), B K- or
+// MN-major (bit 16), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool b_mn_major)
+{
+    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand: start
+// address >> 4 (bits 0-13), leading byte offset >> 4 (16-29), stride byte
+// offset >> 4 (32-45), descriptor version 1 (bit 46), swizzle mode
+// 128B = 2 (bits 61-63).
+__device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+struct Tile {
+    int64_t m0;         // first row of the tile in A / C
+    int64_t m_end;      // rows [m0, m_end) are stored (segment or matrix end)
+    int32_t n0;         // first column
+    int32_t expert;
+};
+
+struct SharedState {
+    uint32_t base;      // shared address of the aligned base
+    uint8_t *gbase;     // generic pointer to the same
+    __device__ uint32_t bar(int i) const { return base + SMEM_BAR + 8 * i; }
+    __device__ uint32_t full(int s) const { return bar(s); }
+    __device__ uint32_t empty(int s) const { return bar(STAGES + s); }
+    __device__ uint32_t pfull(int p) const { return bar(2 * STAGES + p); }
+    __device__ uint32_t pempty(int p) const { return bar(2 * STAGES + 2 + p); }
+    __device__ uint32_t drain() const { return bar(2 * STAGES + 4); }
+    __device__ volatile uint32_t *tmem_slot() const
+    {
+        return reinterpret_cast<volatile uint32_t *>(gbase + SMEM_MISC);
+    }
+    __device__ volatile uint32_t *abort_flag() const
+    {
+        return reinterpret_cast<volatile uint32_t *>(gbase + SMEM_MISC + 4);
+    }
+    __device__ int32_t *tile_prefix() const
+    {
+        return reinterpret_cast<int32_t *>(gbase + SMEM_TILES);
+    }
+};
+
+// Bounded wait on phase `parity` of barrier `bar`.  Returns false when the
+// wait gave up (time limit, or another role already aborted).
+__device__ __forceinline__ bool wait_bounded(const SharedState &ss, uint32_t bar, uint32_t parity)
+{
+    if (ptx::mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 15u) == 0) {
+            if (*ss.abort_flag())
+                return false;
+            if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                *ss.abort_flag() = 1u;
+                atomicOr(&g_error_word, 1u);
+                return false;
+            }
+        }
+    }
+}
+
+template <bool GROUPED>
+__device__ __forceinline__ int64_t total_tiles(const GemmArgs &g, const SharedState &ss)
+{
+    if constexpr (GROUPED)
+        return ss.tile_prefix()[g.E];
+    else
+        return g.num_tiles;
+}
+
+template <bool GROUPED>
+__device__ __forceinline__ Tile tile_at(const GemmArgs &g, const SharedState &ss, int64_t t)
+{
+    Tile tl;
+    if constexpr (GROUPED) {
+        // expert e owns tiles [prefix[e], prefix[e+1]); within an expert the
+        // M-blocks vary fastest so that the CTAs sharing one weight N-block
+        // run together and the block is read from HBM once.
+        const int32_t *pre = ss.tile_prefix();
+        int lo = 0, hi = g.E;                       // find e: pre[e] <= t < pre[e+1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pre[mid] <= t) lo = mid; else hi = mid;
+        }
+        const int e = lo;
+        const int64_t seg0 = min(max((int64_t)g.offsets[e], (int64_t)0), g.M);
+        const int64_t seg1 = min(max((int64_t)g.offsets[e + 1], seg0), g.M);
+        const int64_t mt = (seg1 - seg0 + BM - 1) / BM;
+        const int64_t local = t - pre[e];
+        const int64_t nb = local / mt;
+        tl.m0 = seg0 + (local - nb * mt) * BM;
+        tl.m_end = seg1;
+        tl.n0 = (int32_t)(nb * BN);
+        tl.expert = e;
+    } else {
+        const int64_t nb = t / g.num_m_blk;
+        tl.m0 = (t - nb * g.num_m_blk) * BM;
+        tl.m_end = g.M;
+        tl.n0 = (int32_t)(nb * BN);
+        tl.expert = 0;
+    }
+    return tl;
+}
+
+// Grouped: per-expert tile counts ceil(n_e / 128) * num_n_blk, exclusive
+// prefix over experts into shared memory.  Offsets are clamped into
+// [0, M_total] and made nondecreasing, so malformed offsets cannot move any
+// access out of bounds.
+__device__ void build_tile_prefix(const GemmArgs &g, const SharedState &ss)
+{
+    __shared__ int32_t chunk_sum[GEMM_THREADS];
+    int32_t *pre = ss.tile_prefix();
+    const int tid = threadIdx.x;
+    const int per = (g.E + GEMM_THREADS - 1) / GEMM_THREADS;
+    const int e0 = min(tid * per, g.E), e1 = min(e0 + per, g.E);
+    int32_t sum = 0;
+    for (int e = e0; e < e1; ++e) {
+        const int64_t a = min(max((int64_t)g.offsets[e], (int64_t)0), g.M);
+        const int64_t b = min(max((int64_t)g.offsets[e + 1], a), g.M);
+        const int32_t c = (int32_t)((b - a + BM - 1) / BM) * g.num_n_blk;
+        pre[e] = c;                                   // count, turned into a prefix below
+        sum += c;
+    }
+    chunk_sum[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {
+        int32_t run = 0;
+        for (int i = 0; i < GEMM_THREADS; ++i) {
+            const int32_t c = chunk_sum[i];
+            chunk_sum[i] = run;
+            run += c;
+        }
+        pre[g.E] = run;
+    }
+    __syncthreads();
+    int32_t run = chunk_sum[tid];
+    for (int e = e0; e < e1; ++e) {
+        const int32_t c = pre[e];
+        pre[e] = run;
+        run += c;
+    }
+    __syncthreads();
+}
+
+template <bool GROUPED, bool B_MN>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmArgs g)
+{
+    extern __shared__ uint8_t smem_raw[];
+    SharedState ss;
+    {
+        const uint32_t raw = ptx::smem_u32(smem_raw);
+        const uint32_t aligned = (raw + 1023u) & ~1023u;
+        ss.base = aligned;
+        ss.gbase = smem_raw + (aligned - raw);
+    }
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(ss.full(s), 1);
+            ptx::mbar_init(ss.empty(s), 1);
+        }
+        for (int p = 0; p < 2; ++p) {
+            ptx::mbar_init(ss.pfull(p), 1);
+            ptx::mbar_init(ss.pempty(p), 256);
+        }
+        ptx::mbar_init(ss.drain(), 1);
+        *ss.abort_flag() = 0u;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ss.base + SMEM_MISC, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if constexpr (GROUPED)
+        build_tile_prefix(g, ss);                    // ends with __syncthreads
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *ss.tmem_slot();
+    const int64_t ntiles = total_tiles<GROUPED>(g, ss);
+
+    // Register split, one setmaxnreg per warpgroup (same instruction for its
+    // four warps): 128 x 56 + 256 x 224 = 64512 = the launch's 384 x 168.
+    if (warp < 4) {
+    ptx::setmaxnreg_dec<56>();
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+                const Tile tl = tile_at<GROUPED>(g, ss, t);
+                for (int kb = 0; kb < g.KB; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!wait_bounded(ss, ss.empty(s), ph ^ 1u)) { ok = false; break; }
+                    const uint32_t fb = ss.full(s);
+                    ptx::mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
+                    const uint32_t sa = ss.base + SMEM_A + s * A_STAGE_BYTES;
+                    const uint32_t sb = ss.base + SMEM_B + s * B_STAGE_BYTES;
+                    ptx::tma_load_2d(sa, &tmA, fb, kb * BK, (int32_t)tl.m0);
+                    if constexpr (GROUPED) {
+                        ptx::tma_load_3d(sb, &tmB, fb, kb * BK, tl.n0, tl.expert);
+                    } else if constexpr (B_MN) {
+                        ptx::tma_load_2d(sb, &tmB, fb, tl.n0, kb * BK);
+                        ptx::tma_load_2d(sb + B_STAGE_BYTES / 2, &tmB, fb, tl.n0 + 128, kb * BK);
+                    } else {
+                        ptx::tma_load_2d(sb, &tmB, fb, kb * BK, tl.n0);
+                    }
+                }
+            }
+            // Drain: every copy this thread issued must land before exit.
+            const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+            for (uint32_t j = first; j < it; ++j) {
+                const uint64_t t0 = ptx::globaltimer_ns();
+                while (!ptx::mbar_try_wait(ss.full(j % STAGES), (j / STAGES) & 1u))
+                    if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) { atomicOr(&g_error_word, 1u); break; }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(BM, BN, B_MN);
+            uint32_t it = 0, pit = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+                for (int kb = 0; kb < g.KB; ++kb, ++it, ++pit) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    const int p = pit & 1;
+                    const uint32_t pph = (pit >> 1) & 1u;
+                    if (!wait_bounded(ss, ss.full(s), ph)) { ok = false; break; }
+                    if (!wait_bounded(ss, ss.pempty(p), pph ^ 1u)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint32_t d = tmem_base + (uint32_t)(p * BN);
+                    const uint32_t sa = ss.base + SMEM_A + s * A_STAGE_BYTES;
+                    const uint32_t sb = ss.base + SMEM_B + s * B_STAGE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 32; ++kk) {
+                        const uint64_t ad = make_sdesc_sw128(sa + kk * 32, 16, 1024);
+                        uint64_t bd;
+                        if constexpr (B_MN)
+                            bd = make_sdesc_sw128(sb + kk * 32 * 128, B_STAGE_BYTES / 2, 1024);
+                        else
+                            bd = make_sdesc_sw128(sb + kk * 32, 16, 1024);
+                        ptx::mma_f8f6f4(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(ss.empty(s));
+                    ptx::mma_commit(ss.pfull(p));
+                }
+            }
+            // Drain: all MMAs this thread issued complete before TMEM is freed.
+            ptx::mma_commit(ss.drain());
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(ss.drain(), 0))
+                if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) { atomicOr(&g_error_word, 1u); break; }
+        }
+        __syncwarp();
+    }
+    // warps 2-3: no role
+    } else {
+        ptx::setmaxnreg_inc<224>();
+        // ------------------------------------------------ promote + epilogue
+        const int wg = (warp - 4) >> 2;              // column half
+        const int quarter = warp & 3;                // TMEM lane quarter
+        const int row = quarter * 32 + lane;         // tile row owned by this thread
+        const int col_half = wg * 128;
+        uint32_t pit = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+            const Tile tl = tile_at<GROUPED>(g, ss, t);
+            const int64_t gm = tl.m0 + row;
+            const bool row_ok = gm < tl.m_end;
+            const int nblk = (tl.n0 + col_half) >> 7;              // 128-column scale block
+            const bool col_ok = nblk < g.NB128;
+            const float *sBrow;
+            int64_t sb_stride;
+            if constexpr (GROUPED) {
+                sBrow = g.sB + ((int64_t)tl.expert * g.NB128 + nblk) * g.KB;
+                sb_stride = 1;
+            } else if constexpr (B_MN) {
+                sBrow = g.sB + nblk;
+                sb_stride = g.NB128;
+            } else {
+                sBrow = g.sB + (int64_t)nblk * g.KB;
+                sb_stride = 1;
+            }
+            float acc[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j)
+                acc[j] = 0.0f;
+            for (int kb = 0; kb < g.KB; ++kb, ++pit) {
+                const float sa = row_ok ? __ldg(g.sA + (int64_t)kb * g.M + gm) : 0.0f;
+                const float sb = col_ok ? __ldg(sBrow + (int64_t)kb * sb_stride) : 0.0f;
+                const int p = pit & 1;
+                const uint32_t pph = (pit >> 1) & 1u;
+                if (!wait_bounded(ss, ss.pfull(p), pph)) { ok = false; break; }
+                ptx::tc_fence_after();
+                const float scale = sa * sb;
+                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                       (uint32_t)(p * BN + col_half);
+                uint32_t r0[32], r1[32];
+                ptx::tmem_ld_32x32b_x32(taddr, r0);
+                ptx::tmem_ld_32x32b_x32(taddr + 32, r1);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    acc[j] = fmaf(__uint_as_float(r0[j]), scale, acc[j]);
+                    acc[32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[32 + j]);
+                }
+                ptx::tmem_ld_32x32b_x32(taddr + 64, r0);
+                ptx::tmem_ld_32x32b_x32(taddr + 96, r1);
+                ptx::tmem_ld_wait();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(ss.pempty(p));
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    acc[64 + j] = fmaf(__uint_as_float(r0[j]), scale, acc[64 + j]);
+                    acc[96 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[96 + j]);
+                }
+            }
+            if (!ok)
+                break;
+            // ---- epilogue: this thread's row, 128 columns starting at n0 + col_half
+            if (row_ok && col_ok) {
+                const int64_t n_first = tl.n0 + col_half;
+                const bool full_cols = g.c_vec && n_first + 128 <= g.N;
+                if (g.c_fp32) {
+                    float *crow = reinterpret_cast<float *>(g.C) + gm * g.ldc + n_first;
+                    if (full_cols) {
+#pragma unroll
+                        for (int j = 0; j < 128; j += 4)
+                            ptx::st_v4(crow + j, __float_as_uint(acc[j]), __float_as_uint(acc[j + 1]),
+                                       __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 128; ++j)
+                            if (n_first + j < g.N)
+                                crow[j] = acc[j];
+                    }
+                } else {
+                    uint16_t *crow = reinterpret_cast<uint16_t *>(g.C) + gm * g.ldc + n_first;
+                    if (full_cols) {
+#pragma unroll
+                        for (int j = 0; j < 128; j += 8)
+                            ptx::st_v4(crow + j, ptx::cvt_bf16x2(acc[j], acc[j + 1]),
+                                       ptx::cvt_bf16x2(acc[j + 2], acc[j + 3]),
+                                       ptx::cvt_bf16x2(acc[j + 4], acc[j + 5]),
+                                       ptx::cvt_bf16x2(acc[j + 6], acc[j + 7]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 128; j += 2) {
+                            const uint32_t pr = ptx::cvt_bf16x2(acc[j], acc[j + 1]);
+                            if (n_first + j < g.N)
+                                crow[j] = (uint16_t)(pr & 0xFFFFu);
+                            if (n_first + j + 1 < g.N)
+                                crow[j + 1] = (uint16_t)(pr >> 16);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+} // namespace fp8bs

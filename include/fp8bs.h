@@ -1,0 +1,150 @@
+/*
+ * fp8bs.h -- fine-grained FP8 (E4M3) block-scaled quantisation and GEMMs for
+ * B300 (sm_103a).  C ABI; no C++ or framework types cross it.
+ *
+ * The method (from the pages describing DeepSeek-V3's FP8 training):
+ *   - activations are quantised in 1x128 tiles (per row, per 128 columns of
+ *     K) and weights in 128x128 blocks, each group with its own scale;
+ *     ["DeepSeek-V3 training walkthrough" (deepseek.csdn.net), section 二(四)
+ *      "FP8 low-precision training", fine-grained quantisation item;
+ *      "DeepSeek-V3 Technical Report digest" (sherconan.github.io), section 3
+ *      "FP8 mixed-precision training"; qqstock.cn walkthrough, FP8 section,
+ *      report figure 7a]
+ *   - the GEMM multiplies FP8 operands and, every 128 accumulated K-elements,
+ *     promotes the partial result into FP32 accumulators, applying the two
+ *     groups' scales; forward, data-gradient and weight-gradient GEMMs all
+ *     run in FP8.
+ *     [Technical Report digest, section 3, precision-promotion and
+ *      FP8-operations bullets; walkthrough 二(四), MMA-into-FP32 item;
+ *      qqstock.cn walkthrough, report figure 7b]
+ * The pages do not fix the FP8 format or the scale rule.  This library uses
+ * E4M3 ("FN": bias 7, largest finite +-448, no infinities), scale =
+ * fp32(amax / 448) (one IEEE binary32 division), and codes
+ * q = E4M3_round_to_nearest_even_saturating(fp32(x / scale)).  A group whose
+ * elements are all +-0 gets scale 0 and codes 0x00 / 0x80 by the sign of each
+ * zero.  Inputs must be finite (NaN / Inf inputs give unspecified codes).
+ *
+ * Conventions for every call:
+ *   - All pointers are DEVICE pointers (global memory of the current device)
+ *     unless stated.  The caller owns every buffer and stream; the library
+ *     keeps no reference to them after the call returns.
+ *   - Calls are asynchronous on `stream`: they validate their arguments on
+ *     the host, enqueue kernels and return.  They never synchronise and never
+ *     allocate device memory.
+ *   - Argument errors are returned synchronously and enqueue nothing.
+ *     Device-side errors (a pipeline wait that exceeded its time limit) are
+ *     recorded in a per-device error word and reported by fp8bs_last_error().
+ *   - Leading dimensions (ld*) are row strides in ELEMENTS of that array.
+ *   - Rows of every FP8 and BF16 INPUT and of the quantisers' outputs must
+ *     start on 16-byte boundaries: base pointers 16-byte aligned and
+ *     ld * element_size a multiple of 16.  GEMM outputs need only element
+ *     alignment.
+ *   - The device must be compute capability 10.3 (B300); else FP8BS_ERR_DEVICE.
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8BS_OK = 0,
+    FP8BS_ERR_NULL = -1,        /* a required pointer is NULL                        */
+    FP8BS_ERR_SHAPE = -2,       /* a size is negative, or K / C not a multiple of 128 */
+    FP8BS_ERR_ALIGN = -3,       /* a pointer or row stride breaks the 16-byte rule    */
+    FP8BS_ERR_ARG = -4,         /* an enum value is out of range, or bad offsets size */
+    FP8BS_ERR_LAUNCH = -5,      /* the CUDA runtime refused a launch                  */
+    FP8BS_ERR_DEVICE = -6,      /* the current device is not sm_103                   */
+    FP8BS_ERR_TIMEOUT = -7      /* (fp8bs_last_error only) a device-side wait timed out */
+} fp8bs_status;
+
+enum { FP8BS_OUT_BF16 = 0, FP8BS_OUT_FP32 = 1 };
+enum { FP8BS_B_KMAJOR = 0, FP8BS_B_MNMAJOR = 1 };
+
+/*
+ * 1x128 activation quantisation.
+ *   x_bf16 : [M][K] BF16, row stride ldx (elements).
+ *   q_e4m3 : [M][K] E4M3 codes (1 byte each), row stride ldq (bytes).
+ *   sA     : [K/128][M] FP32, M contiguous: sA[kb*M + m] is the scale of
+ *            row m, columns [128*kb, 128*kb + 128).
+ * M >= 0 arbitrary; K a multiple of 128 (else FP8BS_ERR_SHAPE).
+ * M == 0 or K == 0 is a no-op.
+ */
+int fp8_quant_act_1x128(const void *x_bf16, int64_t M, int64_t K, int64_t ldx,
+                        void *q_e4m3, int64_t ldq, float *sA, cudaStream_t stream);
+
+/*
+ * 128x128 block quantisation of a weight stored as [R][C].
+ *   w_bf16 : [R][C] BF16, row stride ldw (elements).
+ *   q_e4m3 : [R][C] E4M3 codes, row stride ldq (bytes).
+ *   sW     : [ceil(R/128)][C/128] FP32 row-major; sW[rb*(C/128) + cb] is the
+ *            scale of rows [128*rb, 128*rb+128) x columns [128*cb, 128*cb+128).
+ * R >= 0 arbitrary (a last, shorter row block takes its amax over the rows
+ * that exist); C a multiple of 128.
+ * For a K-major GEMM weight W[N][K] call it with (R, C) = (N, K).  For a weight
+ * stored [K][N] (the MN-major B operand) call it with (R, C) = (K, N).
+ */
+int fp8_quant_w_128x128(const void *w_bf16, int64_t R, int64_t C, int64_t ldw,
+                        void *q_e4m3, int64_t ldq, float *sW, cudaStream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM:  C[m][n] = sum_kb  sA[kb][m] * sB(n, kb) *
+ *                                   sum_{k in kb} qA[m][k] * qB(n, k)
+ * with each 128-wide K slice's FP8 product formed on the tensor cores in FP32
+ * and promoted into an FP32 accumulator with its two scales applied.
+ *   qA, sA : as written by fp8_quant_act_1x128 ([M][K], ld = K; [K/128][M]).
+ *   b_major == FP8BS_B_KMAJOR : qB is [N][K] (ld = K), sB [ceil(N/128)][K/128]
+ *                               (fp8_quant_w_128x128 with R = N, C = K).
+ *   b_major == FP8BS_B_MNMAJOR: qB is stored [K][N] (ld = N), sB [K/128][N/128]
+ *                               (fp8_quant_w_128x128 with R = K, C = N);
+ *                               this is the data-gradient form dX = dY . W for
+ *                               a weight kept as [K][N].  N % 128 == 0 required
+ *                               (the weight quantiser's column rule).
+ *   C      : [M][N], row stride ldc >= N (elements), BF16 (round to nearest
+ *            even) or FP32 by c_dtype.  C needs only element alignment; a
+ *            16-byte aligned base and row stride enable vector stores.
+ * M, N >= 0 arbitrary (partial tiles are masked); K a multiple of 128.
+ * K == 0 writes zeros.  M, N < 2^31.
+ */
+int fp8_gemm_blockscaled(const void *qA, const float *sA, const void *qB, const float *sB,
+                         int64_t M, int64_t N, int64_t K, int b_major,
+                         void *C, int c_dtype, int64_t ldc, cudaStream_t stream);
+
+/*
+ * Grouped block-scaled FP8 GEMM for routed experts (one expert per segment of
+ * rows).  Rows [seg_offsets[e], seg_offsets[e+1]) of qA belong to expert e:
+ *   C[m][n] = sum_kb sA[kb][m] * sB[e][n/128][kb] * sum_{k in kb} qA[m][k] * qB[e][n][k]
+ *   qA          : [M_total][K] E4M3, sA [K/128][M_total] (quantise the
+ *                 gathered rows, or gather rows and scale columns of a
+ *                 quantised token matrix: the two are identical).
+ *   qB          : [E][N][K] E4M3 (K contiguous), sB [E][ceil(N/128)][K/128].
+ *   seg_offsets : DEVICE int32[E+1], nondecreasing, [0] == 0, [E] == M_total.
+ *                 Read on the device only: no host synchronisation.  Offsets
+ *                 that break these rules give unspecified output rows (never
+ *                 an out-of-bounds access: rows are clamped to [0, M_total)).
+ *   C           : [M_total][N], row stride ldc, BF16 or FP32.
+ * Segments may be empty.  1 <= E <= 4096.
+ */
+int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA,
+                                 const void *qB, const float *sB,
+                                 const int32_t *seg_offsets, int E, int64_t M_total,
+                                 int64_t N, int64_t K,
+                                 void *C, int c_dtype, int64_t ldc, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reports and clears the current device's error
+ * word: FP8BS_OK, FP8BS_ERR_TIMEOUT (a kernel's pipeline wait exceeded its
+ * time limit; that kernel's outputs are incomplete), or FP8BS_ERR_LAUNCH (the
+ * CUDA runtime reported an error for the stream).
+ */
+int fp8bs_last_error(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

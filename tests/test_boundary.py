@@ -1,0 +1,103 @@
+"""C-ABI boundary checks that need no GPU: the library loads, exports every
+entry point the public header declares, and rejects bad arguments on the host
+before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8bs.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*int\s+(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted([
+        "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
+        "fp8_grouped_gemm_blockscaled", "fp8bs_last_error"])
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    import fp8_fine_grained_26_b300 as fp8
+    assert os.path.exists(fp8.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(fp8.lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", fp8.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert set(declared_functions()) <= exported
+
+
+def test_oracle_is_not_linked_into_the_library():
+    import fp8_fine_grained_26_b300 as fp8
+    out = subprocess.run(["nm", "-D", fp8.LIB_PATH], capture_output=True, text=True).stdout
+    assert "oracle_" not in out
+    out = subprocess.run(["ldd", fp8.LIB_PATH], capture_output=True, text=True).stdout
+    assert "liboracle" not in out
+
+
+def test_package_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "fp8_fine_grained_26_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "liboracle" not in src and "fp8_oracle" not in src, f
+
+
+# Host-side validation: these calls return before any CUDA call.
+def _raw():
+    import fp8_fine_grained_26_b300 as fp8
+    return fp8.lib
+
+
+P = ctypes.c_void_p
+
+
+def test_quant_act_rejects_bad_shapes_and_pointers():
+    lib = _raw()
+    assert lib.fp8_quant_act_1x128(P(0), 4, 100, 100, P(0), 100, P(0), P(0)) == -2   # K % 128
+    assert lib.fp8_quant_act_1x128(P(0), -1, 128, 128, P(0), 128, P(0), P(0)) == -2  # M < 0
+    assert lib.fp8_quant_act_1x128(P(0), 0, 128, 128, P(0), 128, P(0), P(0)) == 0    # empty
+    assert lib.fp8_quant_act_1x128(P(0), 4, 128, 128, P(0), 128, P(0), P(0)) == -1   # NULL
+    assert lib.fp8_quant_act_1x128(P(16), 4, 128, 64, P(16), 128, P(16), P(0)) == -2  # ldx < K
+    assert lib.fp8_quant_act_1x128(P(8), 4, 128, 128, P(16), 128, P(16), P(0)) == -3  # align
+    assert lib.fp8_quant_act_1x128(P(16), 4, 128, 132, P(16), 128, P(16), P(0)) == -3  # ldx*2 % 16
+
+
+def test_quant_w_rejects_bad_shapes():
+    lib = _raw()
+    assert lib.fp8_quant_w_128x128(P(0), 4, 130, 130, P(0), 130, P(0), P(0)) == -2
+    assert lib.fp8_quant_w_128x128(P(0), 0, 128, 128, P(0), 128, P(0), P(0)) == 0
+    assert lib.fp8_quant_w_128x128(P(16), 4, 128, 128, P(16), 136, P(16), P(0)) == -3
+
+
+def test_gemm_rejects_bad_arguments():
+    lib = _raw()
+    g = lib.fp8_gemm_blockscaled
+    assert g(P(16), P(16), P(16), P(16), 4, 4, 128, 2, P(16), 0, 8, P(0)) == -4       # b_major
+    assert g(P(16), P(16), P(16), P(16), 4, 4, 128, 0, P(16), 7, 8, P(0)) == -4       # c_dtype
+    assert g(P(16), P(16), P(16), P(16), 4, 4, 100, 0, P(16), 0, 8, P(0)) == -2       # K % 128
+    assert g(P(16), P(16), P(16), P(16), 0, 4, 128, 0, P(16), 0, 8, P(0)) == 0        # M == 0
+    assert g(P(0), P(16), P(16), P(16), 4, 4, 128, 0, P(16), 0, 8, P(0)) == -1        # NULL qA
+    assert g(P(16), P(16), P(16), P(16), 4, 8, 128, 0, P(16), 0, 4, P(0)) == -2       # ldc < N
+    assert g(P(16), P(16), P(16), P(16), 4, 4, 128, 0, P(17), 0, 4, P(0)) == -3       # C align
+    assert g(P(8), P(16), P(16), P(16), 4, 4, 128, 0, P(16), 0, 8, P(0)) == -3        # qA align
+    gg = lib.fp8_grouped_gemm_blockscaled
+    assert gg(P(16), P(16), P(16), P(16), P(16), 0, 4, 4, 128, P(16), 0, 8, P(0)) == -4   # E < 1
+    assert gg(P(16), P(16), P(16), P(16), P(0), 2, 4, 4, 128, P(16), 0, 8, P(0)) == -1    # offsets
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="checks the no-GPU answer")
+def test_no_gpu_is_reported_as_device_error():
+    lib = _raw()
+    st = lib.fp8_quant_act_1x128(P(16), 4, 128, 128, P(16), 128, P(16), P(0))
+    assert st == -6
