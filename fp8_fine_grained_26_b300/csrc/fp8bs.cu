@@ -113,6 +113,20 @@ bool encode_3d_u8(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, ui
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// BF16 output [M][N] (row stride ldc elements) as a 2-D tensor map for the
+// epilogue's TMA stores: 64 x 32 boxes, 128-byte swizzle.
+bool encode_c_bf16(CUtensorMap *m, void *C, uint64_t N, uint64_t M, uint64_t ldc)
+{
+    const cuuint64_t dims[2] = {N, M};
+    const cuuint64_t strides[1] = {ldc * 2};
+    const cuuint32_t box[2] = {64, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int c_vector_ok(const void *C, int c_dtype, int64_t ldc)
 {
     const int64_t es = c_dtype == FP8BS_OUT_FP32 ? 4 : 2;
@@ -247,7 +261,9 @@ int fp8_gemm_blockscaled(const void *qA, const float *sA, const void *qB, const 
     g.offsets = nullptr;
     g.E = 1;
     g.c_fp32 = c_dtype == FP8BS_OUT_FP32;
-    g.c_vec = c_vector_ok(C, c_dtype, ldc);
+    CUtensorMap tmC = tmA;                        // unused unless the BF16 TMA epilogue runs
+    g.c_tma = !g.c_fp32 && c_vector_ok(C, c_dtype, ldc) &&
+              encode_c_bf16(&tmC, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc);
     g.num_m_blk = (int)((M + BM - 1) / BM);
     g.num_n_blk = (int)((N + BN - 1) / BN);
     g.KB = (int)(K / BK);
@@ -255,9 +271,9 @@ int fp8_gemm_blockscaled(const void *qA, const float *sA, const void *qB, const 
     g.num_tiles = (int64_t)g.num_m_blk * g.num_n_blk;
     const int grid = (int)std::min<int64_t>(g.num_tiles, dev->num_sms);
     if (b_major == FP8BS_B_KMAJOR)
-        fp8_gemm_kernel<false, false><<<grid, GEMM_THREADS, gemm_smem_bytes(false), stream>>>(tmA, tmB, g);
+        fp8_gemm_kernel<false, false><<<grid, GEMM_THREADS, gemm_smem_bytes(false), stream>>>(tmA, tmB, tmC, g);
     else
-        fp8_gemm_kernel<false, true><<<grid, GEMM_THREADS, gemm_smem_bytes(false), stream>>>(tmA, tmB, g);
+        fp8_gemm_kernel<false, true><<<grid, GEMM_THREADS, gemm_smem_bytes(false), stream>>>(tmA, tmB, tmC, g);
     return launch_status();
 }
 
@@ -299,13 +315,15 @@ int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA, const void *qB
     g.offsets = seg_offsets;
     g.E = E;
     g.c_fp32 = c_dtype == FP8BS_OUT_FP32;
-    g.c_vec = c_vector_ok(C, c_dtype, ldc);
+    CUtensorMap tmC = tmA;                        // unused unless the BF16 TMA epilogue runs
+    g.c_tma = !g.c_fp32 && c_vector_ok(C, c_dtype, ldc) &&
+              encode_c_bf16(&tmC, C, (uint64_t)N, (uint64_t)M_total, (uint64_t)ldc);
     g.num_m_blk = 0;
     g.num_n_blk = (int)((N + BN - 1) / BN);
     g.KB = (int)(K / BK);
     g.NB128 = (int)((N + 127) / 128);
     g.num_tiles = 0;
-    fp8_gemm_kernel<true, false><<<dev->num_sms, GEMM_THREADS, gemm_smem_bytes(true), stream>>>(tmA, tmB, g);
+    fp8_gemm_kernel<true, false><<<dev->num_sms, GEMM_THREADS, gemm_smem_bytes(true), stream>>>(tmA, tmB, tmC, g);
     return launch_status();
 }
 

@@ -18,13 +18,18 @@
 //               smem stage and signals the partial.
 //   warps 4-11  promote / epilogue: two warpgroups, each owning 128 of the
 //               256 columns; thread = tile row.  Per slice they load the
-//               partial from TMEM (tcgen05.ld 32x32b) and apply
-//               acc = fma(P, sA*sB, acc) in FP32 registers -- the pages'
-//               promotion, on CUDA cores -- then release the TMEM buffer so
-//               the MMA of slice kb+2 can start while slice kb+1 is promoted.
-//               After the last slice they round acc to BF16 (or keep FP32)
-//               and store the tile, masking rows >= M (or the expert's segment
-//               end) and columns >= N.
+//               partial from TMEM (tcgen05.ld 32x32b, next chunk in flight
+//               while the current one is applied) and apply
+//               acc = fma(P, sA*sB, acc) with packed f32x2 FMAs in FP32
+//               registers -- the pages' promotion, on CUDA cores -- then
+//               release the TMEM buffer so the MMA of slice kb+2 can start
+//               while slice kb+1 is promoted.  Scales are fetched one slice
+//               ahead.  After the last slice each warp rounds its 32 x 128
+//               block to BF16, writes it to its own 128-byte-swizzled staging
+//               buffer and issues asynchronous TMA stores (rows >= M and
+//               columns >= N are clipped by the tensor map); FP32 outputs,
+//               unaligned row strides and the rows of a grouped tile that
+//               reach past the expert's segment are stored directly, masked.
 //   warps 2-3   idle.
 // Every mbarrier wait is bounded (WAIT_LIMIT_NS); on expiry the kernel sets
 // the device error word, stops all roles, drains its own TMA copies and MMAs,
@@ -39,18 +44,20 @@ __device__ unsigned int g_error_word;   // bit 0: a pipeline wait timed out
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 128;
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int A_STAGE_BYTES = BM * BK;                   // 16 KiB
 constexpr int B_STAGE_BYTES = BN * BK;                   // 32 KiB
+constexpr int EPI_WARP_BYTES = 2 * 32 * 128;             // two 32-row x 64-col BF16 boxes
 constexpr int GEMM_THREADS = 384;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;        // 2 s
-constexpr int MAX_EXPERTS = 4096;
+constexpr int MAX_EXPERTS = 2048;
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 constexpr int SMEM_A = 0;
 constexpr int SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
-constexpr int SMEM_BAR = SMEM_B + STAGES * B_STAGE_BYTES;            // 8-byte barriers
+constexpr int SMEM_EPI = SMEM_B + STAGES * B_STAGE_BYTES;            // 8 warps x 8 KiB
+constexpr int SMEM_BAR = SMEM_EPI + 8 * EPI_WARP_BYTES;              // 8-byte barriers
 constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;                     // full, empty, pfull, pempty, drain
 constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;                   // tmem slot, abort flag
 constexpr int SMEM_TILES = SMEM_MISC + 16;                           // grouped: tile prefix [E+1]
@@ -69,7 +76,7 @@ struct GemmArgs {
     const int32_t *offsets;   // grouped: [E+1]
     int E;
     int c_fp32;
-    int c_vec;          // C base and row stride allow 16-byte vector stores
+    int c_tma;          // BF16 output through the C tensor map
     int num_m_blk;      // dense: ceil(M/128)
     int num_n_blk;      // ceil(N/256)
     int KB;             // K/128
@@ -235,10 +242,60 @@ __device__ void build_tile_prefix(const GemmArgs &g, const SharedState &ss)
     __syncthreads();
 }
 
+// acc[j] += P[j] * scale for 32 columns, as 16 packed f32x2 FMAs.
+__device__ __forceinline__ void promote32(float *acc, const uint32_t (&p)[32], float scale)
+{
+#pragma unroll
+    for (int j = 0; j < 32; j += 2)
+        ptx::ffma2(acc[j], acc[j + 1], __uint_as_float(p[j]), __uint_as_float(p[j + 1]), scale);
+}
+
+// Direct, masked stores of one thread's row segment (128 columns from n_first).
+__device__ __forceinline__ void store_row_direct(const GemmArgs &g, const float *acc, int64_t gm,
+                                                 int64_t n_first)
+{
+    const bool full_cols = n_first + 128 <= g.N;
+    if (g.c_fp32) {
+        float *crow = reinterpret_cast<float *>(g.C) + gm * g.ldc + n_first;
+        const bool vec = full_cols && ((reinterpret_cast<uintptr_t>(crow) & 15u) == 0);
+        if (vec) {
+#pragma unroll
+            for (int j = 0; j < 128; j += 4)
+                ptx::st_v4(crow + j, __float_as_uint(acc[j]), __float_as_uint(acc[j + 1]),
+                           __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 128; ++j)
+                if (n_first + j < g.N)
+                    crow[j] = acc[j];
+        }
+    } else {
+        uint16_t *crow = reinterpret_cast<uint16_t *>(g.C) + gm * g.ldc + n_first;
+        const bool vec = full_cols && ((reinterpret_cast<uintptr_t>(crow) & 15u) == 0);
+        if (vec) {
+#pragma unroll
+            for (int j = 0; j < 128; j += 8)
+                ptx::st_v4(crow + j, ptx::cvt_bf16x2(acc[j], acc[j + 1]),
+                           ptx::cvt_bf16x2(acc[j + 2], acc[j + 3]),
+                           ptx::cvt_bf16x2(acc[j + 4], acc[j + 5]),
+                           ptx::cvt_bf16x2(acc[j + 6], acc[j + 7]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 128; j += 2) {
+                const uint32_t pr = ptx::cvt_bf16x2(acc[j], acc[j + 1]);
+                if (n_first + j < g.N)
+                    crow[j] = (uint16_t)(pr & 0xFFFFu);
+                if (n_first + j + 1 < g.N)
+                    crow[j + 1] = (uint16_t)(pr >> 16);
+            }
+        }
+    }
+}
+
 template <bool GROUPED, bool B_MN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmArgs g)
+                const __grid_constant__ CUtensorMap tmC, const GemmArgs g)
 {
     extern __shared__ uint8_t smem_raw[];
     SharedState ss;
@@ -267,6 +324,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
+        if (g.c_tma)
+            ptx::prefetch_tmap(&tmC);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ss.base + SMEM_MISC, TMEM_COLS);
@@ -280,13 +339,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const uint32_t tmem_base = *ss.tmem_slot();
     const int64_t ntiles = total_tiles<GROUPED>(g, ss);
 
-    // Register split, one setmaxnreg per warpgroup (same instruction for its
-    // four warps): 128 x 56 + 256 x 224 = 64512 = the launch's 384 x 168.
+    // Register split, one setmaxnreg per warpgroup (the same instruction for
+    // its four warps): 128 x 56 + 256 x 224 = 64512 = the launch's 384 x 168.
     if (warp < 4) {
-    ptx::setmaxnreg_dec<56>();
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
+        ptx::setmaxnreg_dec<56>();
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------- TMA producer
             uint32_t it = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
@@ -317,11 +375,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 while (!ptx::mbar_try_wait(ss.full(j % STAGES), (j / STAGES) & 1u))
                     if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) { atomicOr(&g_error_word, 1u); break; }
             }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------- MMA issuer
             constexpr uint32_t idesc = make_idesc(BM, BN, B_MN);
             uint32_t it = 0, pit = 0;
             bool ok = true;
@@ -357,9 +412,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             while (!ptx::mbar_try_wait(ss.drain(), 0))
                 if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) { atomicOr(&g_error_word, 1u); break; }
         }
-        __syncwarp();
-    }
-    // warps 2-3: no role
+        __syncwarp();                                // warps 2-3 have no role
     } else {
         ptx::setmaxnreg_inc<224>();
         // ------------------------------------------------ promote + epilogue
@@ -367,6 +420,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const int quarter = warp & 3;                // TMEM lane quarter
         const int row = quarter * 32 + lane;         // tile row owned by this thread
         const int col_half = wg * 128;
+        const uint32_t epi = ss.base + SMEM_EPI + (uint32_t)(warp - 4) * EPI_WARP_BYTES;
         uint32_t pit = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
@@ -387,81 +441,82 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 sBrow = g.sB + (int64_t)nblk * g.KB;
                 sb_stride = 1;
             }
+            const float *sArow = g.sA + gm;
             float acc[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j)
                 acc[j] = 0.0f;
+            float sa_next = row_ok ? __ldg(sArow) : 0.0f;
+            float sb_next = col_ok ? __ldg(sBrow) : 0.0f;
             for (int kb = 0; kb < g.KB; ++kb, ++pit) {
-                const float sa = row_ok ? __ldg(g.sA + (int64_t)kb * g.M + gm) : 0.0f;
-                const float sb = col_ok ? __ldg(sBrow + (int64_t)kb * sb_stride) : 0.0f;
+                const float scale = sa_next * sb_next;
+                if (kb + 1 < g.KB) {                                 // next slice's scales
+                    sa_next = row_ok ? __ldg(sArow + (int64_t)(kb + 1) * g.M) : 0.0f;
+                    sb_next = col_ok ? __ldg(sBrow + (int64_t)(kb + 1) * sb_stride) : 0.0f;
+                }
                 const int p = pit & 1;
                 const uint32_t pph = (pit >> 1) & 1u;
                 if (!wait_bounded(ss, ss.pfull(p), pph)) { ok = false; break; }
                 ptx::tc_fence_after();
-                const float scale = sa * sb;
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                        (uint32_t)(p * BN + col_half);
-                uint32_t r0[32], r1[32];
-                ptx::tmem_ld_32x32b_x32(taddr, r0);
-                ptx::tmem_ld_32x32b_x32(taddr + 32, r1);
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    acc[j] = fmaf(__uint_as_float(r0[j]), scale, acc[j]);
-                    acc[32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[32 + j]);
-                }
-                ptx::tmem_ld_32x32b_x32(taddr + 64, r0);
-                ptx::tmem_ld_32x32b_x32(taddr + 96, r1);
-                ptx::tmem_ld_wait();
+                uint32_t ra[32], rb[32];
+                ptx::tmem_ld_32x32b_x32(taddr, ra);
+                ptx::tmem_ld_wait(ra);
+                ptx::tmem_ld_32x32b_x32(taddr + 32, rb);
+                promote32(acc, ra, scale);
+                ptx::tmem_ld_wait(rb);
+                ptx::tmem_ld_32x32b_x32(taddr + 64, ra);
+                promote32(acc + 32, rb, scale);
+                ptx::tmem_ld_wait(ra);
+                ptx::tmem_ld_32x32b_x32(taddr + 96, rb);
+                promote32(acc + 64, ra, scale);
+                ptx::tmem_ld_wait(rb);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(ss.pempty(p));
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    acc[64 + j] = fmaf(__uint_as_float(r0[j]), scale, acc[64 + j]);
-                    acc[96 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[96 + j]);
-                }
+                promote32(acc + 96, rb, scale);
             }
             if (!ok)
                 break;
-            // ---- epilogue: this thread's row, 128 columns starting at n0 + col_half
-            if (row_ok && col_ok) {
-                const int64_t n_first = tl.n0 + col_half;
-                const bool full_cols = g.c_vec && n_first + 128 <= g.N;
-                if (g.c_fp32) {
-                    float *crow = reinterpret_cast<float *>(g.C) + gm * g.ldc + n_first;
-                    if (full_cols) {
+            // ---- epilogue: rows [m0 + 32*quarter, +32), columns [n0 + col_half, +128)
+            const int64_t n_first = tl.n0 + col_half;
+            if (n_first >= g.N)
+                continue;
+            const int64_t wrow0 = tl.m0 + quarter * 32;
+            if (wrow0 >= tl.m_end)
+                continue;
+            // TMA clips rows at M; a grouped tile may not write past its segment.
+            const bool warp_tma = g.c_tma && (wrow0 + 32 <= tl.m_end || tl.m_end == g.M);
+            if (warp_tma) {
+                if (lane == 0)
+                    ptx::bulk_wait_read_all();        // the previous tile's stores left the buffer
+                __syncwarp();
 #pragma unroll
-                        for (int j = 0; j < 128; j += 4)
-                            ptx::st_v4(crow + j, __float_as_uint(acc[j]), __float_as_uint(acc[j + 1]),
-                                       __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
-                    } else {
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t buf = epi + h * 4096 + lane * 128;
 #pragma unroll
-                        for (int j = 0; j < 128; ++j)
-                            if (n_first + j < g.N)
-                                crow[j] = acc[j];
-                    }
-                } else {
-                    uint16_t *crow = reinterpret_cast<uint16_t *>(g.C) + gm * g.ldc + n_first;
-                    if (full_cols) {
-#pragma unroll
-                        for (int j = 0; j < 128; j += 8)
-                            ptx::st_v4(crow + j, ptx::cvt_bf16x2(acc[j], acc[j + 1]),
-                                       ptx::cvt_bf16x2(acc[j + 2], acc[j + 3]),
-                                       ptx::cvt_bf16x2(acc[j + 4], acc[j + 5]),
-                                       ptx::cvt_bf16x2(acc[j + 6], acc[j + 7]));
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 128; j += 2) {
-                            const uint32_t pr = ptx::cvt_bf16x2(acc[j], acc[j + 1]);
-                            if (n_first + j < g.N)
-                                crow[j] = (uint16_t)(pr & 0xFFFFu);
-                            if (n_first + j + 1 < g.N)
-                                crow[j + 1] = (uint16_t)(pr >> 16);
-                        }
+                    for (int c = 0; c < 8; ++c) {
+                        const float *v = acc + h * 64 + c * 8;
+                        ptx::st_shared_v4(buf + ((c ^ (lane & 7)) << 4),
+                                          ptx::cvt_bf16x2(v[0], v[1]), ptx::cvt_bf16x2(v[2], v[3]),
+                                          ptx::cvt_bf16x2(v[4], v[5]), ptx::cvt_bf16x2(v[6], v[7]));
                     }
                 }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_2d(&tmC, epi, (int32_t)n_first, (int32_t)wrow0);
+                    if (n_first + 64 < g.N)
+                        ptx::tma_store_2d(&tmC, epi + 4096, (int32_t)(n_first + 64), (int32_t)wrow0);
+                    ptx::bulk_commit();
+                }
+            } else if (row_ok) {
+                store_row_direct(g, acc, gm, n_first);
             }
         }
+        if (lane == 0)
+            ptx::bulk_wait_all();
+        __syncwarp();
     }
 
     ptx::tc_fence_before();

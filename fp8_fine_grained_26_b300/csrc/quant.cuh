@@ -7,9 +7,9 @@
 // element plus 4 bytes per scale.  Each 1x128 tile is one 256-byte row segment,
 // read by a half-warp with one 16-byte load per lane; the tile's amax is an
 // integer max over the BF16 magnitude bits (monotone for finite values)
-// reduced with four xor-shuffles.  scale = amax / 448 and q = E4M3(x / scale)
-// use IEEE round-to-nearest division and the hardware RNE-satfinite E4M3
-// conversion; codes are stored 8 bytes per lane.
+// reduced with four xor-shuffles.  scale = amax / 448 is one IEEE division;
+// x / scale is formed exactly (see Divisor below) and encoded with the
+// hardware RNE-satfinite E4M3 conversion; codes are stored 8 bytes per lane.
 #pragma once
 #include "ptx.cuh"
 
@@ -23,23 +23,52 @@ __device__ __forceinline__ uint32_t absmax_bits_bf16x2(uint32_t w)
     return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu);
 }
 
-// q = E4M3(x / s) for two BF16 values packed in `w`; s == 0 means the group is
-// all +-0, and x itself (a signed zero) is encoded.
-__device__ __forceinline__ uint32_t quant_pair(uint32_t w, float s)
+// Per-group divisor.  The quotient fp32(x / s) is formed with Markstein's
+// correction step (P. Markstein, IBM J. Res. Dev. 34(1), 1990): with the
+// correctly rounded reciprocal r = RN(1/s),
+//     q0 = RN(x * r),  rem = fma(-q0, s, x),  q = copysign(fma(rem, r, q0), x),
+// which an exhaustive check over every BF16 amax >= 2^-90 and every BF16
+// |x| <= amax shows to equal IEEE division bit for bit (up to the sign of
+// zero-encoding quotients below 2^-11).  Groups with a smaller amax use
+// IEEE division; an all-zero group (s == 0) encodes x itself (a signed zero).
+struct Divisor {
+    float s, r;
+    int mode;           // 0: s == 0, 1: IEEE division, 2: reciprocal + correction
+};
+
+__device__ __forceinline__ Divisor make_divisor(uint32_t amax_bits)
 {
-    float a = bf16lo(w), b = bf16hi(w);
-    if (s != 0.0f) {
-        a = __fdiv_rn(a, s);
-        b = __fdiv_rn(b, s);
-    }
-    return ptx::cvt_e4m3x2(a, b);
+    Divisor d;
+    const float amax = __uint_as_float(amax_bits << 16);
+    d.s = __fdiv_rn(amax, 448.0f);
+    d.mode = amax_bits == 0 ? 0 : (amax_bits >= 0x1280u ? 2 : 1);   // 0x1280 = 2^-90 in BF16
+    d.r = d.mode == 2 ? __frcp_rn(d.s) : 0.0f;
+    return d;
 }
 
-__device__ __forceinline__ uint2 quant_8(const uint4 &v, float s)
+__device__ __forceinline__ float quotient(float x, const Divisor &d)
+{
+    if (d.mode == 2) {
+        const float q0 = __fmul_rn(x, d.r);
+        const float rem = __fmaf_rn(-q0, d.s, x);
+        // the quotient of x by a positive s carries x's sign; this also keeps
+        // -0 (where rem = +0 and +0 + -0 would round to +0)
+        return copysignf(__fmaf_rn(rem, d.r, q0), x);
+    }
+    return d.mode == 1 ? __fdiv_rn(x, d.s) : x;
+}
+
+// q = E4M3(x / s) for the two BF16 values packed in `w`.
+__device__ __forceinline__ uint32_t quant_pair(uint32_t w, const Divisor &d)
+{
+    return ptx::cvt_e4m3x2(quotient(bf16lo(w), d), quotient(bf16hi(w), d));
+}
+
+__device__ __forceinline__ uint2 quant_8(const uint4 &v, const Divisor &d)
 {
     uint2 r;
-    r.x = quant_pair(v.x, s) | (quant_pair(v.y, s) << 16);
-    r.y = quant_pair(v.z, s) | (quant_pair(v.w, s) << 16);
+    r.x = quant_pair(v.x, d) | (quant_pair(v.y, d) << 16);
+    r.y = quant_pair(v.z, d) | (quant_pair(v.w, d) << 16);
     return r;
 }
 
@@ -68,13 +97,12 @@ __global__ void __launch_bounds__(256) quant_act_1x128_kernel(
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1)
             a = max(a, __shfl_xor_sync(0xffffffffu, a, o, 16));
-        const float amax = __uint_as_float(a << 16);
-        const float s = __fdiv_rn(amax, 448.0f);
+        const Divisor d = make_divisor(a);
         if (valid) {
-            const uint2 r = quant_8(v, s);
+            const uint2 r = quant_8(v, d);
             ptx::st_v2(q + m * ldq + kb * 128 + lane16 * 8, r.x, r.y);
             if (lane16 == 0)
-                sA[kb * M + m] = s;
+                sA[kb * M + m] = d.s;
         }
     }
 }
@@ -115,18 +143,17 @@ __global__ void __launch_bounds__(256) quant_w_128x128_kernel(
 #pragma unroll
     for (int i = 1; i < 8; ++i)
         a = max(a, warp_max[i]);
-    const float amax = __uint_as_float(a << 16);
-    const float s = __fdiv_rn(amax, 448.0f);
+    const Divisor d = make_divisor(a);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int64_t r = row0 + r0 + 16 * i;
         if (r < R) {
-            const uint2 c = quant_8(v[i], s);
+            const uint2 c = quant_8(v[i], d);
             ptx::st_v2(q + r * ldq + col, c.x, c.y);
         }
     }
     if (threadIdx.x == 0)
-        sW[rb * CB + cb] = s;
+        sW[rb * CB + cb] = d.s;
 }
 
 } // namespace fp8bs
