@@ -63,7 +63,11 @@ int current_device(DeviceInfo **info)
                                  gemm_smem_bytes(false)) != cudaSuccess ||
             cudaFuncSetAttribute(fp8_gemm_kernel<true, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 gemm_smem_bytes(true)) != cudaSuccess)
+                                 gemm_smem_bytes(true)) != cudaSuccess ||
+            cudaFuncSetAttribute(quant_act_1x128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 quant_smem_bytes()) != cudaSuccess ||
+            cudaFuncSetAttribute(quant_w_128x128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 quant_smem_bytes()) != cudaSuccess)
             return FP8BS_ERR_LAUNCH;
         d.attrs_set = true;
     }
@@ -127,6 +131,20 @@ bool encode_c_bf16(CUtensorMap *m, void *C, uint64_t N, uint64_t M, uint64_t ldc
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// BF16 matrix [rows][cols] (row stride ld elements) as a 2-D tensor map with
+// 128 x 128 boxes (no swizzle): the quantisers' unit of work.
+bool encode_bf16_units(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld)
+{
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {ld * 2};
+    const cuuint32_t box[2] = {128, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int c_vector_ok(const void *C, int c_dtype, int64_t ldc)
 {
     const int64_t es = c_dtype == FP8BS_OUT_FP32 ? 4 : 2;
@@ -185,13 +203,13 @@ int fp8_quant_act_1x128(const void *x_bf16, int64_t M, int64_t K, int64_t ldx, v
     DeviceInfo *dev = nullptr;
     if (int st = current_device(&dev))
         return st;
-    const int64_t tiles = M * (K / 128);
-    const int64_t warps = (tiles + 1) / 2;
-    const int64_t max_blocks = (int64_t)dev->num_sms * 8;
-    const int blocks = (int)std::min<int64_t>((warps + 7) / 8, max_blocks);
-    quant_act_1x128_kernel<<<blocks, 256, 0, stream>>>(
-        static_cast<const uint16_t *>(x_bf16), M, K / 128, ldx, static_cast<uint8_t *>(q_e4m3),
-        ldq, sA);
+    CUtensorMap tmX;
+    if (!encode_bf16_units(&tmX, x_bf16, (uint64_t)K, (uint64_t)M, (uint64_t)ldx))
+        return FP8BS_ERR_ARG;
+    const int64_t units = ((M + 127) / 128) * (K / 128);
+    const int grid = (int)std::min<int64_t>(units, 2 * (int64_t)dev->num_sms);
+    quant_act_1x128_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
+        tmX, M, K / 128, static_cast<uint8_t *>(q_e4m3), ldq, sA, units);
     return launch_status();
 }
 
@@ -213,11 +231,13 @@ int fp8_quant_w_128x128(const void *w_bf16, int64_t R, int64_t C, int64_t ldw, v
     if (int st = current_device(&dev))
         return st;
     const int64_t RB = (R + 127) / 128, CB = C / 128;
-    if (RB * CB > INT32_MAX)
-        return FP8BS_ERR_SHAPE;
-    quant_w_128x128_kernel<<<(unsigned)(RB * CB), 256, 0, stream>>>(
-        static_cast<const uint16_t *>(w_bf16), R, CB, ldw, static_cast<uint8_t *>(q_e4m3), ldq,
-        sW);
+    CUtensorMap tmW;
+    if (!encode_bf16_units(&tmW, w_bf16, (uint64_t)C, (uint64_t)R, (uint64_t)ldw))
+        return FP8BS_ERR_ARG;
+    const int64_t units = RB * CB;
+    const int grid = (int)std::min<int64_t>(units, 2 * (int64_t)dev->num_sms);
+    quant_w_128x128_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
+        tmW, R, CB, static_cast<uint8_t *>(q_e4m3), ldq, sW, units);
     return launch_status();
 }
 

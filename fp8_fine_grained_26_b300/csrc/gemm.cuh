@@ -35,11 +35,9 @@
 // the device error word, stops all roles, drains its own TMA copies and MMAs,
 // frees TMEM and returns.
 #pragma once
-#include "ptx.cuh"
+#include "common.cuh"
 
 namespace fp8bs {
-
-__device__ unsigned int g_error_word;   // bit 0: a pipeline wait timed out
 
 constexpr int BM = 128;
 constexpr int BN = 256;
@@ -50,7 +48,6 @@ constexpr int B_STAGE_BYTES = BN * BK;                   // 32 KiB
 constexpr int EPI_WARP_BYTES = 2 * 32 * 128;             // two 32-row x 64-col BF16 boxes
 constexpr int GEMM_THREADS = 384;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;        // 2 s
 constexpr int MAX_EXPERTS = 2048;
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
@@ -137,26 +134,9 @@ struct SharedState {
     }
 };
 
-// Bounded wait on phase `parity` of barrier `bar`.  Returns false when the
-// wait gave up (time limit, or another role already aborted).
 __device__ __forceinline__ bool wait_bounded(const SharedState &ss, uint32_t bar, uint32_t parity)
 {
-    if (ptx::mbar_try_wait(bar, parity))
-        return true;
-    const uint64_t t0 = ptx::globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (ptx::mbar_try_wait(bar, parity))
-            return true;
-        if ((it & 15u) == 0) {
-            if (*ss.abort_flag())
-                return false;
-            if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-                *ss.abort_flag() = 1u;
-                atomicOr(&g_error_word, 1u);
-                return false;
-            }
-        }
-    }
+    return wait_bounded(bar, parity, ss.abort_flag());
 }
 
 template <bool GROUPED>
@@ -370,11 +350,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             // Drain: every copy this thread issued must land before exit.
             const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
-            for (uint32_t j = first; j < it; ++j) {
-                const uint64_t t0 = ptx::globaltimer_ns();
-                while (!ptx::mbar_try_wait(ss.full(j % STAGES), (j / STAGES) & 1u))
-                    if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) { atomicOr(&g_error_word, 1u); break; }
-            }
+            for (uint32_t j = first; j < it; ++j)
+                wait_drain(ss.full(j % STAGES), (j / STAGES) & 1u);
         } else if (warp == 1 && lane == 0) {
             // -------------------------------------------- MMA issuer
             constexpr uint32_t idesc = make_idesc(BM, BN, B_MN);
@@ -408,9 +385,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             // Drain: all MMAs this thread issued complete before TMEM is freed.
             ptx::mma_commit(ss.drain());
-            const uint64_t t0 = ptx::globaltimer_ns();
-            while (!ptx::mbar_try_wait(ss.drain(), 0))
-                if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) { atomicOr(&g_error_word, 1u); break; }
+            wait_drain(ss.drain(), 0);
         }
         __syncwarp();                                // warps 2-3 have no role
     } else {

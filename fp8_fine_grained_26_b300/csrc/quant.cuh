@@ -4,14 +4,21 @@
 // tile, weights per 128x128 block.]
 //
 // Both kernels are HBM-bound streams: 2 bytes read + 1 byte written per
-// element plus 4 bytes per scale.  Each 1x128 tile is one 256-byte row segment,
-// read by a half-warp with one 16-byte load per lane; the tile's amax is an
-// integer max over the BF16 magnitude bits (monotone for finite values)
-// reduced with four xor-shuffles.  scale = amax / 448 is one IEEE division;
-// x / scale is formed exactly (see Divisor below) and encoded with the
-// hardware RNE-satfinite E4M3 conversion; codes are stored 8 bytes per lane.
+// element plus 4 bytes per scale.  They are persistent (two 256-thread CTAs
+// per SM) and stream 128 x 128 BF16 units (32 KiB: 128 rows of one 128-column
+// K-block) through a QSTAGES-deep ring of TMA loads in shared memory, so each
+// SM keeps several units in flight while it encodes another.  A unit is one
+// 128x128 weight block, or 128 activation rows x one 1x128 tile column.
+// A 1x128 tile is one 256-byte row segment handled by a half-warp (16 bytes
+// per lane); its amax is an integer max over the BF16 magnitude bits
+// (monotone for finite values) reduced with four xor-shuffles; a weight
+// block's amax adds a warp and a CTA reduction.  scale = amax / 448 is one
+// IEEE division; x / scale is formed exactly (see Divisor below) and encoded
+// with the hardware RNE-satfinite E4M3 conversion; codes are stored 8 bytes
+// per lane (128 contiguous bytes per half-warp), scales of a unit's 128 rows
+// are staged in shared memory and stored as one coalesced 512-byte run.
 #pragma once
-#include "ptx.cuh"
+#include "common.cuh"
 
 namespace fp8bs {
 
@@ -72,88 +79,210 @@ __device__ __forceinline__ uint2 quant_8(const uint4 &v, const Divisor &d)
     return r;
 }
 
-// One half-warp per 1x128 tile.  Tiles are numbered t = kb * M + m so that
-// consecutive half-warps write consecutive scales of sA[kb][*].  The loop is
-// warp-uniform (both half-warps iterate together) because of the shuffles.
-__global__ void __launch_bounds__(256) quant_act_1x128_kernel(
-    const uint16_t *__restrict__ x, int64_t M, int64_t KB, int64_t ldx,
-    uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ sA)
-{
-    const int lane16 = threadIdx.x & 15;
-    const int half = (threadIdx.x >> 4) & 1;
-    const int64_t total = M * KB;
-    const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t wp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-         wp * 2 < total; wp += warps_total) {
-        const int64_t t = wp * 2 + half;
-        const bool valid = t < total;
-        const int64_t kb = valid ? t / M : 0;
-        const int64_t m = valid ? t - kb * M : 0;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (valid)
-            v = ptx::ld_nc_v4(x + m * ldx + kb * 128 + lane16 * 8);
-        uint32_t a = max(max(absmax_bits_bf16x2(v.x), absmax_bits_bf16x2(v.y)),
-                         max(absmax_bits_bf16x2(v.z), absmax_bits_bf16x2(v.w)));
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1)
-            a = max(a, __shfl_xor_sync(0xffffffffu, a, o, 16));
-        const Divisor d = make_divisor(a);
-        if (valid) {
-            const uint2 r = quant_8(v, d);
-            ptx::st_v2(q + m * ldq + kb * 128 + lane16 * 8, r.x, r.y);
-            if (lane16 == 0)
-                sA[kb * M + m] = d.s;
-        }
+
+constexpr int QSTAGES = 3;
+constexpr int QUNIT_BYTES = 128 * 128 * 2;                    // 32 KiB of BF16
+constexpr int QUANT_THREADS = 256;
+constexpr int QSMEM_BAR = QSTAGES * QUNIT_BYTES;                // full barriers
+constexpr int QSMEM_ABORT = QSMEM_BAR + 8 * QSTAGES;
+constexpr int QSMEM_RED = QSMEM_ABORT + 8;                       // 2 x 128 floats / 2 x 8 words
+constexpr int QSMEM_END = QSMEM_RED + 2 * 128 * 4;
+constexpr int quant_smem_bytes() { return 1024 + QSMEM_END; }
+
+struct QRing {
+    uint32_t base;
+    uint8_t *gbase;
+    __device__ uint32_t stage(int s) const { return base + s * QUNIT_BYTES; }
+    __device__ uint32_t full(int s) const { return base + QSMEM_BAR + 8 * s; }
+    __device__ volatile uint32_t *abort() const
+    {
+        return reinterpret_cast<volatile uint32_t *>(gbase + QSMEM_ABORT);
     }
+    __device__ float *red_f(int b) const { return reinterpret_cast<float *>(gbase + QSMEM_RED) + 128 * b; }
+    __device__ uint32_t *red_u(int b) const
+    {
+        return reinterpret_cast<uint32_t *>(gbase + QSMEM_RED) + 128 * b;
+    }
+};
+
+__device__ __forceinline__ QRing qring_setup()
+{
+    extern __shared__ uint8_t smem_raw[];
+    QRing r;
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    r.base = (raw + 1023u) & ~1023u;
+    r.gbase = smem_raw + (r.base - raw);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < QSTAGES; ++s)
+            ptx::mbar_init(r.full(s), 1);
+        *r.abort() = 0u;
+        ptx::fence_mbarrier_init();
+    }
+    __syncthreads();
+    return r;
 }
 
-// One 256-thread CTA per 128x128 block.  Thread t owns the 16-byte column
-// chunk (t & 15) of rows (t >> 4) + 16 i, i = 0..7: 64 elements held in
-// registers between the amax pass and the encode pass (one HBM read).
-__global__ void __launch_bounds__(256) quant_w_128x128_kernel(
-    const uint16_t *__restrict__ w, int64_t R, int64_t CB, int64_t ldw,
-    uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ sW)
+// Unit j of this CTA (j-th in its strided list) -> (row block, column block).
+__device__ __forceinline__ void qunit(int64_t j, int64_t cols_blocks, int64_t &rb, int64_t &cb)
 {
-    __shared__ uint32_t warp_max[8];
-    const int64_t blk = blockIdx.x;
-    const int64_t rb = blk / CB, cb = blk - rb * CB;
-    const int chunk = threadIdx.x & 15;
-    const int r0 = threadIdx.x >> 4;
-    const int64_t row0 = rb * 128;
-    const int64_t col = cb * 128 + chunk * 8;
+    const int64_t u = (int64_t)blockIdx.x + j * gridDim.x;
+    rb = u / cols_blocks;
+    cb = u - rb * cols_blocks;
+}
 
-    uint4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int64_t r = row0 + r0 + 16 * i;
-        v[i] = (r < R) ? ptx::ld_nc_v4(w + r * ldw + col) : make_uint4(0, 0, 0, 0);
-    }
-    uint32_t a = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        a = max(a, max(max(absmax_bits_bf16x2(v[i].x), absmax_bits_bf16x2(v[i].y)),
-                       max(absmax_bits_bf16x2(v[i].z), absmax_bits_bf16x2(v[i].w))));
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1)
-        a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
-    if ((threadIdx.x & 31) == 0)
-        warp_max[threadIdx.x >> 5] = a;
+__device__ __forceinline__ void qissue(const QRing &r, const CUtensorMap *tm, int64_t j,
+                                       int64_t cols_blocks)
+{
+    int64_t rb, cb;
+    qunit(j, cols_blocks, rb, cb);
+    const int s = (int)(j % QSTAGES);
+    ptx::fence_proxy_async_smem();             // earlier generic reads of the stage come first
+    ptx::mbar_arrive_expect_tx(r.full(s), QUNIT_BYTES);
+    ptx::tma_load_2d(r.stage(s), tm, r.full(s), (int32_t)(cb * 128), (int32_t)(rb * 128));
+}
+
+// Waits for unit j's stage; every thread of the CTA agrees on the outcome.
+__device__ __forceinline__ bool qwait(const QRing &r, int64_t j)
+{
+    const int s = (int)(j % QSTAGES);
+    wait_bounded(r.full(s), (uint32_t)((j / QSTAGES) & 1), r.abort());
     __syncthreads();
-    a = warp_max[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i)
-        a = max(a, warp_max[i]);
-    const Divisor d = make_divisor(a);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int64_t r = row0 + r0 + 16 * i;
-        if (r < R) {
-            const uint2 c = quant_8(v[i], d);
-            ptx::st_v2(q + r * ldq + col, c.x, c.y);
-        }
-    }
+    return *r.abort() == 0u;
+}
+
+// After an abort: the copies this CTA issued but never consumed must land
+// before it exits.
+__device__ __forceinline__ void qdrain(const QRing &r, int64_t consumed, int64_t issued)
+{
     if (threadIdx.x == 0)
-        sW[rb * CB + cb] = d.s;
+        for (int64_t j = consumed; j < issued; ++j)
+            wait_drain(r.full((int)(j % QSTAGES)), (uint32_t)((j / QSTAGES) & 1));
+}
+
+// Activation quantiser.  Unit (mb, kb): rows [128 mb, +128) of tile column kb.
+// Half-warp h (0..15) owns rows h + 16 i, i = 0..7: a warp reads two adjacent
+// 256-byte rows of the staged unit per step.
+__global__ void __launch_bounds__(QUANT_THREADS, 2) quant_act_1x128_kernel(
+    const __grid_constant__ CUtensorMap tmX, int64_t M, int64_t KB, uint8_t *__restrict__ q,
+    int64_t ldq, float *__restrict__ sA, int64_t units)
+{
+    const QRing r = qring_setup();
+    const int tid = threadIdx.x;
+    const int lane16 = tid & 15;
+    const int hw = tid >> 4;
+    const int64_t mine = (int64_t)blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    int64_t issued = 0;
+    if (tid == 0)
+        for (; issued < mine && issued < QSTAGES; ++issued)
+            qissue(r, &tmX, issued, KB);
+    int64_t j = 0;
+    for (; j < mine; ++j) {
+        if (!qwait(r, j))
+            break;
+        const uint32_t st = r.stage((int)(j % QSTAGES));
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t a = st + (uint32_t)((hw + 16 * i) * 256 + lane16 * 16);
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w) : "r"(a));
+        }
+        __syncthreads();                                   // the stage is free again
+        if (tid == 0 && issued < mine && issued < j + 1 + QSTAGES) {
+            qissue(r, &tmX, issued, KB);
+            ++issued;
+        }
+        int64_t mb, kb;
+        qunit(j, KB, mb, kb);
+        float *scales = r.red_f((int)(j & 1));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t a = max(max(absmax_bits_bf16x2(v[i].x), absmax_bits_bf16x2(v[i].y)),
+                             max(absmax_bits_bf16x2(v[i].z), absmax_bits_bf16x2(v[i].w)));
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1)
+                a = max(a, __shfl_xor_sync(0xffffffffu, a, o, 16));
+            const Divisor d = make_divisor(a);
+            const int row = hw + 16 * i;
+            const int64_t gm = mb * 128 + row;
+            if (gm < M) {
+                const uint2 c = quant_8(v[i], d);
+                ptx::st_v2(q + gm * ldq + kb * 128 + lane16 * 8, c.x, c.y);
+            }
+            if (lane16 == 0)
+                scales[row] = d.s;
+        }
+        __syncthreads();
+        if (tid < 128 && mb * 128 + tid < M)
+            sA[kb * M + mb * 128 + tid] = scales[tid];
+    }
+    qdrain(r, j, issued);
+}
+
+// Weight quantiser.  Unit (rb, cb): one 128x128 block.  Thread t owns the
+// 16-byte column chunk (t & 15) of rows (t >> 4) + 16 i, i = 0..7: 64 values
+// held in registers between the amax and the encode passes.
+__global__ void __launch_bounds__(QUANT_THREADS, 2) quant_w_128x128_kernel(
+    const __grid_constant__ CUtensorMap tmW, int64_t R, int64_t CB, uint8_t *__restrict__ q,
+    int64_t ldq, float *__restrict__ sW, int64_t units)
+{
+    const QRing r = qring_setup();
+    const int tid = threadIdx.x;
+    const int chunk = tid & 15;
+    const int r0 = tid >> 4;
+    const int64_t mine = (int64_t)blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    int64_t issued = 0;
+    if (tid == 0)
+        for (; issued < mine && issued < QSTAGES; ++issued)
+            qissue(r, &tmW, issued, CB);
+    int64_t j = 0;
+    for (; j < mine; ++j) {
+        if (!qwait(r, j))
+            break;
+        const uint32_t st = r.stage((int)(j % QSTAGES));
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t a = st + (uint32_t)((r0 + 16 * i) * 256 + chunk * 16);
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w) : "r"(a));
+        }
+        uint32_t a = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            a = max(a, max(max(absmax_bits_bf16x2(v[i].x), absmax_bits_bf16x2(v[i].y)),
+                           max(absmax_bits_bf16x2(v[i].z), absmax_bits_bf16x2(v[i].w))));
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+        uint32_t *wmax = r.red_u((int)(j & 1));
+        if ((tid & 31) == 0)
+            wmax[tid >> 5] = a;
+        __syncthreads();                                   // stage read, warp maxima written
+        if (tid == 0 && issued < mine && issued < j + 1 + QSTAGES) {
+            qissue(r, &tmW, issued, CB);
+            ++issued;
+        }
+        a = wmax[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i)
+            a = max(a, wmax[i]);
+        const Divisor d = make_divisor(a);
+        int64_t rb, cb;
+        qunit(j, CB, rb, cb);
+        const int64_t col = cb * 128 + chunk * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int64_t row = rb * 128 + r0 + 16 * i;
+            if (row < R) {
+                const uint2 c = quant_8(v[i], d);
+                ptx::st_v2(q + row * ldq + col, c.x, c.y);
+            }
+        }
+        if (tid == 0)
+            sW[rb * CB + cb] = d.s;
+    }
+    qdrain(r, j, issued);
 }
 
 } // namespace fp8bs
