@@ -25,9 +25,13 @@ namespace fp8bs {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ uint32_t absmax_bits_bf16x2(uint32_t w)
+// BF16 magnitude bits of 8 values (16 bytes): max over the masked 16-bit
+// lanes, then over the two halves.
+__device__ __forceinline__ uint32_t absmax_bits8(const uint4 &v)
 {
-    return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu);
+    const uint32_t m = 0x7FFF7FFFu;
+    const uint32_t a = ptx::max_u16x2(ptx::max_u16x2(v.x & m, v.y & m), ptx::max_u16x2(v.z & m, v.w & m));
+    return max(a & 0xFFFFu, a >> 16);
 }
 
 // Per-group divisor.  The quotient fp32(x / s) is formed with Markstein's
@@ -38,47 +42,59 @@ __device__ __forceinline__ uint32_t absmax_bits_bf16x2(uint32_t w)
 // |x| <= amax shows to equal IEEE division bit for bit (up to the sign of
 // zero-encoding quotients below 2^-11).  Groups with a smaller amax use
 // IEEE division; an all-zero group (s == 0) encodes x itself (a signed zero).
+// Two elements are processed at once with packed f32x2 arithmetic (each lane
+// rounds exactly as the scalar operation).
 struct Divisor {
     float s, r;
     int mode;           // 0: s == 0, 1: IEEE division, 2: reciprocal + correction
 };
+
+__device__ __forceinline__ int divisor_mode(uint32_t amax_bits)
+{
+    return amax_bits == 0 ? 0 : (amax_bits >= 0x1280u ? 2 : 1);   // 0x1280 = 2^-90 in BF16
+}
 
 __device__ __forceinline__ Divisor make_divisor(uint32_t amax_bits)
 {
     Divisor d;
     const float amax = __uint_as_float(amax_bits << 16);
     d.s = __fdiv_rn(amax, 448.0f);
-    d.mode = amax_bits == 0 ? 0 : (amax_bits >= 0x1280u ? 2 : 1);   // 0x1280 = 2^-90 in BF16
+    d.mode = divisor_mode(amax_bits);
     d.r = d.mode == 2 ? __frcp_rn(d.s) : 0.0f;
     return d;
 }
 
-__device__ __forceinline__ float quotient(float x, const Divisor &d)
+__device__ __forceinline__ float quotient_slow(float x, const Divisor &d)
 {
-    if (d.mode == 2) {
-        const float q0 = __fmul_rn(x, d.r);
-        const float rem = __fmaf_rn(-q0, d.s, x);
-        // the quotient of x by a positive s carries x's sign; this also keeps
-        // -0 (where rem = +0 and +0 + -0 would round to +0)
-        return copysignf(__fmaf_rn(rem, d.r, q0), x);
-    }
     return d.mode == 1 ? __fdiv_rn(x, d.s) : x;
 }
 
-// q = E4M3(x / s) for the two BF16 values packed in `w`.
-__device__ __forceinline__ uint32_t quant_pair(uint32_t w, const Divisor &d)
-{
-    return ptx::cvt_e4m3x2(quotient(bf16lo(w), d), quotient(bf16hi(w), d));
-}
-
+// E4M3 codes of the 8 BF16 values in v, as 8 bytes (element 0 lowest).
 __device__ __forceinline__ uint2 quant_8(const uint4 &v, const Divisor &d)
 {
-    uint2 r;
-    r.x = quant_pair(v.x, d) | (quant_pair(v.y, d) << 16);
-    r.y = quant_pair(v.z, d) | (quant_pair(v.w, d) << 16);
-    return r;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t c[4];
+    if (d.mode == 2) {
+        const uint64_t r2 = ptx::pack_f32x2(d.r, d.r);
+        const uint64_t ns2 = ptx::pack_f32x2(-d.s, -d.s);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float xl = bf16lo(w[k]), xh = bf16hi(w[k]);
+            const uint64_t x2 = ptx::pack_f32x2(xl, xh);
+            const uint64_t q0 = ptx::mul_f32x2(x2, r2);
+            const uint64_t rem = ptx::fma_f32x2(q0, ns2, x2);      // x - q0 * s, exact
+            float ql, qh;
+            ptx::unpack_f32x2(ptx::fma_f32x2(rem, r2, q0), ql, qh);
+            // the quotient carries x's sign (keeps -0, where +0 + -0 rounds to +0)
+            c[k] = ptx::cvt_e4m3x2(copysignf(ql, xl), copysignf(qh, xh));
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            c[k] = ptx::cvt_e4m3x2(quotient_slow(bf16lo(w[k]), d), quotient_slow(bf16hi(w[k]), d));
+    }
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
-
 
 constexpr int QSTAGES = 3;
 constexpr int QUNIT_BYTES = 128 * 128 * 2;                    // 32 KiB of BF16
@@ -160,8 +176,10 @@ __device__ __forceinline__ void qdrain(const QRing &r, int64_t consumed, int64_t
 }
 
 // Activation quantiser.  Unit (mb, kb): rows [128 mb, +128) of tile column kb.
-// Half-warp h (0..15) owns rows h + 16 i, i = 0..7: a warp reads two adjacent
-// 256-byte rows of the staged unit per step.
+// Warp w owns rows [16 w, 16 w + 16); at step i its two half-warps take rows
+// 16 w + 2 i and 16 w + 2 i + 1 (512 contiguous bytes of the staged unit).
+// The eight row divisors of a half-warp are formed by eight different lanes
+// and broadcast with shuffles.
 __global__ void __launch_bounds__(QUANT_THREADS, 2) quant_act_1x128_kernel(
     const __grid_constant__ CUtensorMap tmX, int64_t M, int64_t KB, uint8_t *__restrict__ q,
     int64_t ldq, float *__restrict__ sA, int64_t units)
@@ -183,7 +201,8 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2) quant_act_1x128_kernel(
         uint4 v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t a = st + (uint32_t)((hw + 16 * i) * 256 + lane16 * 16);
+            const int row = 2 * i + (hw & 1) + 16 * (hw >> 1);
+            const uint32_t a = st + (uint32_t)(row * 256 + lane16 * 16);
             asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w) : "r"(a));
         }
@@ -195,15 +214,30 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2) quant_act_1x128_kernel(
         int64_t mb, kb;
         qunit(j, KB, mb, kb);
         float *scales = r.red_f((int)(j & 1));
+        // amax of each of this half-warp's 8 rows, known to all its 16 lanes
+        uint32_t am[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            uint32_t a = max(max(absmax_bits_bf16x2(v[i].x), absmax_bits_bf16x2(v[i].y)),
-                             max(absmax_bits_bf16x2(v[i].z), absmax_bits_bf16x2(v[i].w)));
+            uint32_t a = absmax_bits8(v[i]);
 #pragma unroll
             for (int o = 8; o >= 1; o >>= 1)
                 a = max(a, __shfl_xor_sync(0xffffffffu, a, o, 16));
-            const Divisor d = make_divisor(a);
-            const int row = hw + 16 * i;
+            am[i] = a;
+        }
+        // lane i of the half-warp forms row i's divisor once; the others fetch it
+        uint32_t mine_a = am[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i)
+            mine_a = (lane16 & 7) == i ? am[i] : mine_a;
+        const Divisor dm = make_divisor(mine_a);
+        const int half_base = (tid & 16);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            Divisor d;
+            d.s = __shfl_sync(0xffffffffu, dm.s, half_base + i);
+            d.r = __shfl_sync(0xffffffffu, dm.r, half_base + i);
+            d.mode = divisor_mode(am[i]);
+            const int row = 2 * i + (hw & 1) + 16 * (hw >> 1);
             const int64_t gm = mb * 128 + row;
             if (gm < M) {
                 const uint2 c = quant_8(v[i], d);
@@ -250,8 +284,7 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2) quant_w_128x128_kernel(
         uint32_t a = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            a = max(a, max(max(absmax_bits_bf16x2(v[i].x), absmax_bits_bf16x2(v[i].y)),
-                           max(absmax_bits_bf16x2(v[i].z), absmax_bits_bf16x2(v[i].w))));
+            a = max(a, absmax_bits8(v[i]));
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1)
             a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
