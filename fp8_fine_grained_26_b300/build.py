@@ -8,7 +8,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libfp8bs.so")
 SOURCES = [os.path.join(CSRC, "fp8bs.cu")]
-HEADERS = [os.path.join(CSRC, f) for f in ("ptx.cuh", "quant.cuh", "gemm.cuh")] + \
+HEADERS = [os.path.join(CSRC, f) for f in ("ptx.cuh", "common.cuh", "quant.cuh", "gemm.cuh")] + \
     [os.path.join(ROOT, "include", "fp8bs.h")]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -18,13 +18,12 @@
 //               smem stage and signals the partial.
 //   warps 4-11  promote / epilogue: two warpgroups, each owning 128 of the
 //               256 columns; thread = tile row.  Per slice they load the
-//               partial from TMEM (tcgen05.ld 32x32b, next chunk in flight
-//               while the current one is applied) and apply
+//               partial from TMEM (two 64-column tcgen05.ld 32x32b) and apply
 //               acc = fma(P, sA*sB, acc) with packed f32x2 FMAs in FP32
 //               registers -- the pages' promotion, on CUDA cores -- then
 //               release the TMEM buffer so the MMA of slice kb+2 can start
-//               while slice kb+1 is promoted.  Scales are fetched one slice
-//               ahead.  After the last slice each warp rounds its 32 x 128
+//               while slice kb+1 is promoted.  Scales are fetched two
+//               slices ahead.  After the last slice each warp rounds its 32 x 128
 //               block to BF16, writes it to its own 128-byte-swizzled staging
 //               buffer and issues asynchronous TMA stores (rows >= M and
 //               columns >= N are clipped by the tensor map); FP32 outputs,
@@ -42,25 +41,33 @@ namespace fp8bs {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 128;
-constexpr int STAGES = 3;
 constexpr int A_STAGE_BYTES = BM * BK;                   // 16 KiB
 constexpr int B_STAGE_BYTES = BN * BK;                   // 32 KiB
-constexpr int EPI_WARP_BYTES = 2 * 32 * 128;             // two 32-row x 64-col BF16 boxes
+constexpr int EPI_WARP_BYTES = 32 * 128;                 // one 32-row x 64-col BF16 box
 constexpr int GEMM_THREADS = 384;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_EXPERTS = 2048;
 
-// Shared-memory layout (offsets from a 1024-byte aligned base).
-constexpr int SMEM_A = 0;
-constexpr int SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
-constexpr int SMEM_EPI = SMEM_B + STAGES * B_STAGE_BYTES;            // 8 warps x 8 KiB
-constexpr int SMEM_BAR = SMEM_EPI + 8 * EPI_WARP_BYTES;              // 8-byte barriers
-constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;                     // full, empty, pfull, pempty, drain
-constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;                   // tmem slot, abort flag
-constexpr int SMEM_TILES = SMEM_MISC + 16;                           // grouped: tile prefix [E+1]
-constexpr int gemm_smem_bytes(bool grouped)
+// Shared-memory layout for S pipeline stages and E epilogue boxes per promote
+// warp (offsets from a 1024-byte aligned base).  Long-K GEMMs take S = 4,
+// E = 1 (deeper operand pipeline; the epilogue is rare); short-K GEMMs and the
+// grouped GEMM take S = 3, E = 2 (both output halves of a warp are staged at
+// once, so a tile's stores never wait on each other).
+template <int S, int E>
+struct Layout {
+    static constexpr int A = 0;
+    static constexpr int B = A + S * A_STAGE_BYTES;
+    static constexpr int EPI = B + S * B_STAGE_BYTES;                // 8 warps x E x 4 KiB
+    static constexpr int BAR = EPI + 8 * E * EPI_WARP_BYTES;        // 8-byte barriers
+    static constexpr int NUM_BARS = 2 * S + 2 + 2 + 1;              // full, empty, pfull, pempty, drain
+    static constexpr int MISC = BAR + NUM_BARS * 8;                 // tmem slot, abort flag
+    static constexpr int TILES = MISC + 16;                         // grouped: tile prefix [E+1]
+};
+
+template <bool GROUPED, int S, int E>
+constexpr int gemm_smem_bytes()
 {
-    return 1024 + SMEM_TILES + (grouped ? (MAX_EXPERTS + 1) * 4 : 0);
+    return 1024 + Layout<S, E>::TILES + (GROUPED ? (MAX_EXPERTS + 1) * 4 : 0);
 }
 
 struct GemmArgs {
@@ -111,36 +118,41 @@ struct Tile {
     int32_t expert;
 };
 
+template <int S, int E>
 struct SharedState {
+    using L = Layout<S, E>;
     uint32_t base;      // shared address of the aligned base
     uint8_t *gbase;     // generic pointer to the same
-    __device__ uint32_t bar(int i) const { return base + SMEM_BAR + 8 * i; }
+    __device__ uint32_t bar(int i) const { return base + L::BAR + 8 * i; }
     __device__ uint32_t full(int s) const { return bar(s); }
-    __device__ uint32_t empty(int s) const { return bar(STAGES + s); }
-    __device__ uint32_t pfull(int p) const { return bar(2 * STAGES + p); }
-    __device__ uint32_t pempty(int p) const { return bar(2 * STAGES + 2 + p); }
-    __device__ uint32_t drain() const { return bar(2 * STAGES + 4); }
+    __device__ uint32_t empty(int s) const { return bar(S + s); }
+    __device__ uint32_t pfull(int p) const { return bar(2 * S + p); }
+    __device__ uint32_t pempty(int p) const { return bar(2 * S + 2 + p); }
+    __device__ uint32_t drain() const { return bar(2 * S + 4); }
+    __device__ uint32_t a_stage(int s) const { return base + L::A + s * A_STAGE_BYTES; }
+    __device__ uint32_t b_stage(int s) const { return base + L::B + s * B_STAGE_BYTES; }
     __device__ volatile uint32_t *tmem_slot() const
     {
-        return reinterpret_cast<volatile uint32_t *>(gbase + SMEM_MISC);
+        return reinterpret_cast<volatile uint32_t *>(gbase + L::MISC);
     }
     __device__ volatile uint32_t *abort_flag() const
     {
-        return reinterpret_cast<volatile uint32_t *>(gbase + SMEM_MISC + 4);
+        return reinterpret_cast<volatile uint32_t *>(gbase + L::MISC + 4);
     }
     __device__ int32_t *tile_prefix() const
     {
-        return reinterpret_cast<int32_t *>(gbase + SMEM_TILES);
+        return reinterpret_cast<int32_t *>(gbase + L::TILES);
     }
 };
 
-__device__ __forceinline__ bool wait_bounded(const SharedState &ss, uint32_t bar, uint32_t parity)
+template <int S, int E>
+__device__ __forceinline__ bool wait_bounded(const SharedState<S, E> &ss, uint32_t bar, uint32_t parity)
 {
     return wait_bounded(bar, parity, ss.abort_flag());
 }
 
-template <bool GROUPED>
-__device__ __forceinline__ int64_t total_tiles(const GemmArgs &g, const SharedState &ss)
+template <bool GROUPED, int S, int E>
+__device__ __forceinline__ int64_t total_tiles(const GemmArgs &g, const SharedState<S, E> &ss)
 {
     if constexpr (GROUPED)
         return ss.tile_prefix()[g.E];
@@ -148,8 +160,8 @@ __device__ __forceinline__ int64_t total_tiles(const GemmArgs &g, const SharedSt
         return g.num_tiles;
 }
 
-template <bool GROUPED>
-__device__ __forceinline__ Tile tile_at(const GemmArgs &g, const SharedState &ss, int64_t t)
+template <bool GROUPED, int S, int E>
+__device__ __forceinline__ Tile tile_at(const GemmArgs &g, const SharedState<S, E> &ss, int64_t t)
 {
     Tile tl;
     if constexpr (GROUPED) {
@@ -186,7 +198,8 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &g, const SharedState &ss
 // prefix over experts into shared memory.  Offsets are clamped into
 // [0, M_total] and made nondecreasing, so malformed offsets cannot move any
 // access out of bounds.
-__device__ void build_tile_prefix(const GemmArgs &g, const SharedState &ss)
+template <int S, int E>
+__device__ void build_tile_prefix(const GemmArgs &g, const SharedState<S, E> &ss)
 {
     __shared__ int32_t chunk_sum[GEMM_THREADS];
     int32_t *pre = ss.tile_prefix();
@@ -222,16 +235,19 @@ __device__ void build_tile_prefix(const GemmArgs &g, const SharedState &ss)
     __syncthreads();
 }
 
-// acc[j] += P[j] * scale for 32 columns, as 16 packed f32x2 FMAs.
-__device__ __forceinline__ void promote32(float *acc, const uint32_t (&p)[32], float scale)
+// acc[j] += P[j] * scale for 64 columns (32 column pairs), as packed f32x2
+// FMAs: each lane is one correctly rounded fused multiply-add.
+__device__ __forceinline__ void promote64(float2 *acc, const uint32_t (&p)[64], float scale)
 {
+    const float2 s2 = make_float2(scale, scale);
 #pragma unroll
-    for (int j = 0; j < 32; j += 2)
-        ptx::ffma2(acc[j], acc[j + 1], __uint_as_float(p[j]), __uint_as_float(p[j + 1]), scale);
+    for (int j = 0; j < 32; ++j)
+        acc[j] = __ffma2_rn(make_float2(__uint_as_float(p[2 * j]), __uint_as_float(p[2 * j + 1])), s2,
+                            acc[j]);
 }
 
 // Direct, masked stores of one thread's row segment (128 columns from n_first).
-__device__ __forceinline__ void store_row_direct(const GemmArgs &g, const float *acc, int64_t gm,
+__device__ __forceinline__ void store_row_direct(const GemmArgs &g, const float2 *acc2, int64_t gm,
                                                  int64_t n_first)
 {
     const bool full_cols = n_first + 128 <= g.N;
@@ -240,45 +256,49 @@ __device__ __forceinline__ void store_row_direct(const GemmArgs &g, const float 
         const bool vec = full_cols && ((reinterpret_cast<uintptr_t>(crow) & 15u) == 0);
         if (vec) {
 #pragma unroll
-            for (int j = 0; j < 128; j += 4)
-                ptx::st_v4(crow + j, __float_as_uint(acc[j]), __float_as_uint(acc[j + 1]),
-                           __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
+            for (int j = 0; j < 64; j += 2)
+                ptx::st_v4(crow + 2 * j, __float_as_uint(acc2[j].x), __float_as_uint(acc2[j].y),
+                           __float_as_uint(acc2[j + 1].x), __float_as_uint(acc2[j + 1].y));
         } else {
 #pragma unroll
-            for (int j = 0; j < 128; ++j)
-                if (n_first + j < g.N)
-                    crow[j] = acc[j];
+            for (int j = 0; j < 64; ++j) {
+                if (n_first + 2 * j < g.N)
+                    crow[2 * j] = acc2[j].x;
+                if (n_first + 2 * j + 1 < g.N)
+                    crow[2 * j + 1] = acc2[j].y;
+            }
         }
     } else {
         uint16_t *crow = reinterpret_cast<uint16_t *>(g.C) + gm * g.ldc + n_first;
         const bool vec = full_cols && ((reinterpret_cast<uintptr_t>(crow) & 15u) == 0);
         if (vec) {
 #pragma unroll
-            for (int j = 0; j < 128; j += 8)
-                ptx::st_v4(crow + j, ptx::cvt_bf16x2(acc[j], acc[j + 1]),
-                           ptx::cvt_bf16x2(acc[j + 2], acc[j + 3]),
-                           ptx::cvt_bf16x2(acc[j + 4], acc[j + 5]),
-                           ptx::cvt_bf16x2(acc[j + 6], acc[j + 7]));
+            for (int j = 0; j < 64; j += 4)
+                ptx::st_v4(crow + 2 * j, ptx::cvt_bf16x2(acc2[j].x, acc2[j].y),
+                           ptx::cvt_bf16x2(acc2[j + 1].x, acc2[j + 1].y),
+                           ptx::cvt_bf16x2(acc2[j + 2].x, acc2[j + 2].y),
+                           ptx::cvt_bf16x2(acc2[j + 3].x, acc2[j + 3].y));
         } else {
 #pragma unroll
-            for (int j = 0; j < 128; j += 2) {
-                const uint32_t pr = ptx::cvt_bf16x2(acc[j], acc[j + 1]);
-                if (n_first + j < g.N)
-                    crow[j] = (uint16_t)(pr & 0xFFFFu);
-                if (n_first + j + 1 < g.N)
-                    crow[j + 1] = (uint16_t)(pr >> 16);
+            for (int j = 0; j < 64; ++j) {
+                const uint32_t pr = ptx::cvt_bf16x2(acc2[j].x, acc2[j].y);
+                if (n_first + 2 * j < g.N)
+                    crow[2 * j] = (uint16_t)(pr & 0xFFFFu);
+                if (n_first + 2 * j + 1 < g.N)
+                    crow[2 * j + 1] = (uint16_t)(pr >> 16);
             }
         }
     }
 }
 
-template <bool GROUPED, bool B_MN>
+template <bool GROUPED, bool B_MN, int STAGES, int EPI_BOXES>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs g)
 {
+    using L = Layout<STAGES, EPI_BOXES>;
     extern __shared__ uint8_t smem_raw[];
-    SharedState ss;
+    SharedState<STAGES, EPI_BOXES> ss;
     {
         const uint32_t raw = ptx::smem_u32(smem_raw);
         const uint32_t aligned = (raw + 1023u) & ~1023u;
@@ -308,7 +328,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             ptx::prefetch_tmap(&tmC);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ss.base + SMEM_MISC, TMEM_COLS);
+        ptx::tmem_alloc(ss.base + L::MISC, TMEM_COLS);
         ptx::tmem_relinquish();
     }
     if constexpr (GROUPED)
@@ -317,7 +337,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *ss.tmem_slot();
-    const int64_t ntiles = total_tiles<GROUPED>(g, ss);
+    const int64_t ntiles = total_tiles<GROUPED, STAGES, EPI_BOXES>(g, ss);
 
     // Register split, one setmaxnreg per warpgroup (the same instruction for
     // its four warps): 128 x 56 + 256 x 224 = 64512 = the launch's 384 x 168.
@@ -325,21 +345,27 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         ptx::setmaxnreg_dec<56>();
         if (warp == 0 && lane == 0) {
             // -------------------------------------------- TMA producer
+            // L2 policy: A row blocks are re-read by the tiles of later
+            // N-blocks (keep them); dense B column blocks are shared by the
+            // concurrently running M-tiles (default policy); an expert's
+            // weights are not needed again once its tiles are done.
+            const uint64_t keep = ptx::policy_evict_last();
+            const uint64_t stream = ptx::policy_evict_first();
             uint32_t it = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-                const Tile tl = tile_at<GROUPED>(g, ss, t);
+                const Tile tl = tile_at<GROUPED, STAGES, EPI_BOXES>(g, ss, t);
                 for (int kb = 0; kb < g.KB; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!wait_bounded(ss, ss.empty(s), ph ^ 1u)) { ok = false; break; }
                     const uint32_t fb = ss.full(s);
                     ptx::mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
-                    const uint32_t sa = ss.base + SMEM_A + s * A_STAGE_BYTES;
-                    const uint32_t sb = ss.base + SMEM_B + s * B_STAGE_BYTES;
-                    ptx::tma_load_2d(sa, &tmA, fb, kb * BK, (int32_t)tl.m0);
+                    const uint32_t sa = ss.a_stage(s);
+                    const uint32_t sb = ss.b_stage(s);
+                    ptx::tma_load_2d_hint(sa, &tmA, fb, kb * BK, (int32_t)tl.m0, keep);
                     if constexpr (GROUPED) {
-                        ptx::tma_load_3d(sb, &tmB, fb, kb * BK, tl.n0, tl.expert);
+                        ptx::tma_load_3d_hint(sb, &tmB, fb, kb * BK, tl.n0, tl.expert, stream);
                     } else if constexpr (B_MN) {
                         ptx::tma_load_2d(sb, &tmB, fb, tl.n0, kb * BK);
                         ptx::tma_load_2d(sb + B_STAGE_BYTES / 2, &tmB, fb, tl.n0 + 128, kb * BK);
@@ -367,8 +393,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     if (!wait_bounded(ss, ss.pempty(p), pph ^ 1u)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t d = tmem_base + (uint32_t)(p * BN);
-                    const uint32_t sa = ss.base + SMEM_A + s * A_STAGE_BYTES;
-                    const uint32_t sb = ss.base + SMEM_B + s * B_STAGE_BYTES;
+                    const uint32_t sa = ss.a_stage(s);
+                    const uint32_t sb = ss.b_stage(s);
 #pragma unroll
                     for (int kk = 0; kk < BK / 32; ++kk) {
                         const uint64_t ad = make_sdesc_sw128(sa + kk * 32, 16, 1024);
@@ -395,11 +421,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const int quarter = warp & 3;                // TMEM lane quarter
         const int row = quarter * 32 + lane;         // tile row owned by this thread
         const int col_half = wg * 128;
-        const uint32_t epi = ss.base + SMEM_EPI + (uint32_t)(warp - 4) * EPI_WARP_BYTES;
+        const uint32_t epi = ss.base + L::EPI + (uint32_t)(warp - 4) * EPI_BOXES * EPI_WARP_BYTES;
+        const uint64_t c_policy = ptx::policy_evict_first();   // C is written once, never re-read
         uint32_t pit = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-            const Tile tl = tile_at<GROUPED>(g, ss, t);
+            const Tile tl = tile_at<GROUPED, STAGES, EPI_BOXES>(g, ss, t);
             const int64_t gm = tl.m0 + row;
             const bool row_ok = gm < tl.m_end;
             const int nblk = (tl.n0 + col_half) >> 7;              // 128-column scale block
@@ -417,39 +444,42 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 sb_stride = 1;
             }
             const float *sArow = g.sA + gm;
-            float acc[128];
+            float2 acc2[64];
 #pragma unroll
-            for (int j = 0; j < 128; ++j)
-                acc[j] = 0.0f;
-            float sa_next = row_ok ? __ldg(sArow) : 0.0f;
-            float sb_next = col_ok ? __ldg(sBrow) : 0.0f;
+            for (int j = 0; j < 64; ++j)
+                acc2[j] = make_float2(0.0f, 0.0f);
+            // Scales travel through a 2-deep register queue: the loads for
+            // slice kb+2 are issued while slice kb is promoted, so their L2
+            // latency is covered by two slices of work.
+            auto load_sa = [&](int k) {
+                return ptx::ld_f32_early(sArow + (int64_t)min(k, g.KB - 1) * g.M, row_ok && k < g.KB);
+            };
+            auto load_sb = [&](int k) {
+                return ptx::ld_f32_early(sBrow + (int64_t)min(k, g.KB - 1) * sb_stride, col_ok && k < g.KB);
+            };
+            float sa0 = load_sa(0), sa1 = load_sa(1);
+            float sb0 = load_sb(0), sb1 = load_sb(1);
             for (int kb = 0; kb < g.KB; ++kb, ++pit) {
-                const float scale = sa_next * sb_next;
-                if (kb + 1 < g.KB) {                                 // next slice's scales
-                    sa_next = row_ok ? __ldg(sArow + (int64_t)(kb + 1) * g.M) : 0.0f;
-                    sb_next = col_ok ? __ldg(sBrow + (int64_t)(kb + 1) * sb_stride) : 0.0f;
-                }
+                const float scale = sa0 * sb0;
+                sa0 = sa1; sa1 = load_sa(kb + 2);
+                sb0 = sb1; sb1 = load_sb(kb + 2);
                 const int p = pit & 1;
                 const uint32_t pph = (pit >> 1) & 1u;
                 if (!wait_bounded(ss, ss.pfull(p), pph)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                        (uint32_t)(p * BN + col_half);
-                uint32_t ra[32], rb[32];
-                ptx::tmem_ld_32x32b_x32(taddr, ra);
-                ptx::tmem_ld_wait(ra);
-                ptx::tmem_ld_32x32b_x32(taddr + 32, rb);
-                promote32(acc, ra, scale);
-                ptx::tmem_ld_wait(rb);
-                ptx::tmem_ld_32x32b_x32(taddr + 64, ra);
-                promote32(acc + 32, rb, scale);
-                ptx::tmem_ld_wait(ra);
-                ptx::tmem_ld_32x32b_x32(taddr + 96, rb);
-                promote32(acc + 64, ra, scale);
-                ptx::tmem_ld_wait(rb);
+                // two 64-column TMEM round trips; the buffer is released as
+                // soon as the second one has landed in registers
+                uint32_t r[64];
+                ptx::tmem_ld_32x32b_x64(taddr, r);
+                ptx::tmem_ld_wait(r);
+                promote64(acc2, r, scale);
+                ptx::tmem_ld_32x32b_x64(taddr + 64, r);
+                ptx::tmem_ld_wait(r);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(ss.pempty(p));
-                promote32(acc + 96, rb, scale);
+                promote64(acc2 + 32, r, scale);
             }
             if (!ok)
                 break;
@@ -463,30 +493,60 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             // TMA clips rows at M; a grouped tile may not write past its segment.
             const bool warp_tma = g.c_tma && (wrow0 + 32 <= tl.m_end || tl.m_end == g.M);
             if (warp_tma) {
-                if (lane == 0)
-                    ptx::bulk_wait_read_all();        // the previous tile's stores left the buffer
-                __syncwarp();
+                const bool two = n_first + 64 < g.N;            // second 64-column box exists
+                if constexpr (EPI_BOXES == 2) {
+                    // both halves staged at once: one proxy fence, one commit
+                    if (lane == 0)
+                        ptx::bulk_wait_read_all();              // the previous tile's stores read them
+                    __syncwarp();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t buf = epi + h * 4096 + lane * 128;
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t buf = epi + h * EPI_WARP_BYTES + lane * 128;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float *v = acc + h * 64 + c * 8;
-                        ptx::st_shared_v4(buf + ((c ^ (lane & 7)) << 4),
-                                          ptx::cvt_bf16x2(v[0], v[1]), ptx::cvt_bf16x2(v[2], v[3]),
-                                          ptx::cvt_bf16x2(v[4], v[5]), ptx::cvt_bf16x2(v[6], v[7]));
+                        for (int c = 0; c < 8; ++c) {
+                            const float2 *v = acc2 + h * 32 + c * 4;
+                            ptx::st_shared_v4(buf + ((c ^ (lane & 7)) << 4),
+                                              ptx::cvt_bf16x2(v[0].x, v[0].y), ptx::cvt_bf16x2(v[1].x, v[1].y),
+                                              ptx::cvt_bf16x2(v[2].x, v[2].y), ptx::cvt_bf16x2(v[3].x, v[3].y));
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d_hint(&tmC, epi, (int32_t)n_first, (int32_t)wrow0, c_policy);
+                        if (two)
+                            ptx::tma_store_2d_hint(&tmC, epi + EPI_WARP_BYTES, (int32_t)(n_first + 64),
+                                                   (int32_t)wrow0, c_policy);
+                        ptx::bulk_commit();
+                    }
+                } else {
+                    // one staging box, reused for the second half
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (h == 1 && !two)
+                            break;
+                        if (lane == 0)
+                            ptx::bulk_wait_read_all();
+                        __syncwarp();
+                        const uint32_t buf = epi + lane * 128;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const float2 *v = acc2 + h * 32 + c * 4;
+                            ptx::st_shared_v4(buf + ((c ^ (lane & 7)) << 4),
+                                              ptx::cvt_bf16x2(v[0].x, v[0].y), ptx::cvt_bf16x2(v[1].x, v[1].y),
+                                              ptx::cvt_bf16x2(v[2].x, v[2].y), ptx::cvt_bf16x2(v[3].x, v[3].y));
+                        }
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d_hint(&tmC, epi, (int32_t)(n_first + h * 64), (int32_t)wrow0,
+                                                   c_policy);
+                            ptx::bulk_commit();
+                        }
                     }
                 }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::tma_store_2d(&tmC, epi, (int32_t)n_first, (int32_t)wrow0);
-                    if (n_first + 64 < g.N)
-                        ptx::tma_store_2d(&tmC, epi + 4096, (int32_t)(n_first + 64), (int32_t)wrow0);
-                    ptx::bulk_commit();
-                }
             } else if (row_ok) {
-                store_row_direct(g, acc, gm, n_first);
+                store_row_direct(g, acc2, gm, n_first);
             }
         }
         if (lane == 0)

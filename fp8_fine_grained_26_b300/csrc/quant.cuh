@@ -75,18 +75,16 @@ __device__ __forceinline__ uint2 quant_8(const uint4 &v, const Divisor &d)
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t c[4];
     if (d.mode == 2) {
-        const uint64_t r2 = ptx::pack_f32x2(d.r, d.r);
-        const uint64_t ns2 = ptx::pack_f32x2(-d.s, -d.s);
+        const float2 r2 = make_float2(d.r, d.r);
+        const float2 ns2 = make_float2(-d.s, -d.s);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const float xl = bf16lo(w[k]), xh = bf16hi(w[k]);
-            const uint64_t x2 = ptx::pack_f32x2(xl, xh);
-            const uint64_t q0 = ptx::mul_f32x2(x2, r2);
-            const uint64_t rem = ptx::fma_f32x2(q0, ns2, x2);      // x - q0 * s, exact
-            float ql, qh;
-            ptx::unpack_f32x2(ptx::fma_f32x2(rem, r2, q0), ql, qh);
+            const float2 x2 = make_float2(bf16lo(w[k]), bf16hi(w[k]));
+            const float2 q0 = __fmul2_rn(x2, r2);
+            const float2 rem = __ffma2_rn(q0, ns2, x2);             // x - q0 * s, exact
+            const float2 q = __ffma2_rn(rem, r2, q0);
             // the quotient carries x's sign (keeps -0, where +0 + -0 rounds to +0)
-            c[k] = ptx::cvt_e4m3x2(copysignf(ql, xl), copysignf(qh, xh));
+            c[k] = ptx::cvt_e4m3x2(copysignf(q.x, x2.x), copysignf(q.y, x2.y));
         }
     } else {
 #pragma unroll
