@@ -280,6 +280,28 @@ def dense_host_inputs(case):
     return synthetic.bf16_bits(case.a), synthetic.bf16_bits(case.w), case.b_major
 
 
+def kernel_src_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm.cuh", "ptx.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "fp8_fine_grained_26_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def gemm_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu record, or None when there
+    is none for this workload or the kernel source changed since it was taken."""
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(prof):
+        return None
+    with open(prof) as f:
+        rec = json.load(f).get(f"{kernel}:{workload}")
+    if rec is None or rec.get("src_sha") != kernel_src_sha():
+        return None
+    return rec["bytes"]
+
+
 # ---------------------------------------------------------------- main arms
 def run_ours(args):
     import torch
@@ -377,13 +399,7 @@ def run_ours(args):
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     fp8_peak_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP8_OVER_BF16
     achieved = step.flops / (gemm_ms * 1e-3) / 1e12
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        with open(prof) as f:
-            tr = json.load(f).get(f"{gemm_name}:{args.workload}")
-        if tr is not None:
-            traffic = tr
+    traffic = gemm_traffic(gemm_name, args.workload)
     roofline = {"kernel": gemm_name, "bound": "tensor", "achieved": round(achieved, 1),
                 "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
                 "traffic": traffic,
