@@ -213,7 +213,7 @@ int fp8_quant_act_1x128(const void *x_bf16, int64_t M, int64_t K, int64_t ldx, v
     if (!encode_bf16_units(&tmX, x_bf16, (uint64_t)K, (uint64_t)M, (uint64_t)ldx))
         return FP8BS_ERR_ARG;
     const int64_t units = ((M + 127) / 128) * (K / 128);
-    const int grid = (int)std::min<int64_t>(units, 2 * (int64_t)dev->num_sms);
+    const int grid = (int)std::min<int64_t>(units, 3 * (int64_t)dev->num_sms);
     quant_act_1x128_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
         tmX, M, K / 128, static_cast<uint8_t *>(q_e4m3), ldq, sA, units);
     return launch_status();
@@ -241,7 +241,7 @@ int fp8_quant_w_128x128(const void *w_bf16, int64_t R, int64_t C, int64_t ldw, v
     if (!encode_bf16_units(&tmW, w_bf16, (uint64_t)C, (uint64_t)R, (uint64_t)ldw))
         return FP8BS_ERR_ARG;
     const int64_t units = RB * CB;
-    const int grid = (int)std::min<int64_t>(units, 2 * (int64_t)dev->num_sms);
+    const int grid = (int)std::min<int64_t>(units, 3 * (int64_t)dev->num_sms);
     quant_w_128x128_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
         tmW, R, CB, static_cast<uint8_t *>(q_e4m3), ldq, sW, units);
     return launch_status();

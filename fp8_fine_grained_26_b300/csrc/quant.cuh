@@ -94,7 +94,7 @@ __device__ __forceinline__ uint2 quant_8(const uint4 &v, const Divisor &d)
     return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
-constexpr int QSTAGES = 3;
+constexpr int QSTAGES = 2;
 constexpr int QUNIT_BYTES = 128 * 128 * 2;                    // 32 KiB of BF16
 constexpr int QUANT_THREADS = 256;
 constexpr int QSMEM_BAR = QSTAGES * QUNIT_BYTES;                // full barriers
@@ -178,7 +178,7 @@ __device__ __forceinline__ void qdrain(const QRing &r, int64_t consumed, int64_t
 // 16 w + 2 i and 16 w + 2 i + 1 (512 contiguous bytes of the staged unit).
 // The eight row divisors of a half-warp are formed by eight different lanes
 // and broadcast with shuffles.
-__global__ void __launch_bounds__(QUANT_THREADS, 2) quant_act_1x128_kernel(
+__global__ void __launch_bounds__(QUANT_THREADS, 3) quant_act_1x128_kernel(
     const __grid_constant__ CUtensorMap tmX, int64_t M, int64_t KB, uint8_t *__restrict__ q,
     int64_t ldq, float *__restrict__ sA, int64_t units)
 {
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2) quant_act_1x128_kernel(
 // Weight quantiser.  Unit (rb, cb): one 128x128 block.  Thread t owns the
 // 16-byte column chunk (t & 15) of rows (t >> 4) + 16 i, i = 0..7: 64 values
 // held in registers between the amax and the encode passes.
-__global__ void __launch_bounds__(QUANT_THREADS, 2) quant_w_128x128_kernel(
+__global__ void __launch_bounds__(QUANT_THREADS, 3) quant_w_128x128_kernel(
     const __grid_constant__ CUtensorMap tmW, int64_t R, int64_t CB, uint8_t *__restrict__ q,
     int64_t ldq, float *__restrict__ sW, int64_t units)
 {
