@@ -55,13 +55,7 @@ int current_device(DeviceInfo **info)
     if (!d.is_sm103)
         return FP8BS_ERR_DEVICE;
     if (!d.attrs_set) {
-        if (cudaFuncSetAttribute(fp8_gemm_kernel<false, false, 4, 1>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 gemm_smem_bytes<false, 4, 1>()) != cudaSuccess ||
-            cudaFuncSetAttribute(fp8_gemm_kernel<false, true, 4, 1>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 gemm_smem_bytes<false, 4, 1>()) != cudaSuccess ||
-            cudaFuncSetAttribute(fp8_gemm_kernel<false, false, 3, 2>,
+        if (cudaFuncSetAttribute(fp8_gemm_kernel<false, false, 3, 2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  gemm_smem_bytes<false, 3, 2>()) != cudaSuccess ||
             cudaFuncSetAttribute(fp8_gemm_kernel<false, true, 3, 2>,
@@ -296,20 +290,10 @@ int fp8_gemm_blockscaled(const void *qA, const float *sA, const void *qB, const 
     g.NB128 = (int)((N + 127) / 128);
     g.num_tiles = (int64_t)g.num_m_blk * g.num_n_blk;
     const int grid = (int)std::min<int64_t>(g.num_tiles, dev->num_sms);
-    // Short K (<= 16 slices per tile): the epilogue is frequent, stage both
-    // output halves at once; long K: one more operand stage instead.
-    const bool short_k = g.KB <= 16;
-    if (b_major == FP8BS_B_KMAJOR) {
-        if (short_k)
-            fp8_gemm_kernel<false, false, 3, 2><<<grid, GEMM_THREADS, gemm_smem_bytes<false, 3, 2>(), stream>>>(tmA, tmB, tmC, g);
-        else
-            fp8_gemm_kernel<false, false, 4, 1><<<grid, GEMM_THREADS, gemm_smem_bytes<false, 4, 1>(), stream>>>(tmA, tmB, tmC, g);
-    } else {
-        if (short_k)
-            fp8_gemm_kernel<false, true, 3, 2><<<grid, GEMM_THREADS, gemm_smem_bytes<false, 3, 2>(), stream>>>(tmA, tmB, tmC, g);
-        else
-            fp8_gemm_kernel<false, true, 4, 1><<<grid, GEMM_THREADS, gemm_smem_bytes<false, 4, 1>(), stream>>>(tmA, tmB, tmC, g);
-    }
+    if (b_major == FP8BS_B_KMAJOR)
+        fp8_gemm_kernel<false, false, 3, 2><<<grid, GEMM_THREADS, gemm_smem_bytes<false, 3, 2>(), stream>>>(tmA, tmB, tmC, g);
+    else
+        fp8_gemm_kernel<false, true, 3, 2><<<grid, GEMM_THREADS, gemm_smem_bytes<false, 3, 2>(), stream>>>(tmA, tmB, tmC, g);
     return launch_status();
 }
 

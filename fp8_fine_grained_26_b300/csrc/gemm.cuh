@@ -22,14 +22,16 @@
 //               acc = fma(P, sA*sB, acc) with packed f32x2 FMAs in FP32
 //               registers -- the pages' promotion, on CUDA cores -- then
 //               release the TMEM buffer so the MMA of slice kb+2 can start
-//               while slice kb+1 is promoted.  Scales are fetched two
-//               slices ahead.  After the last slice each warp rounds its 32 x 128
+//               while slice kb+1 is promoted.  The scales come from a
+//               shared ring that warp 2 fills ahead of time.  After the last slice each warp rounds its 32 x 128
 //               block to BF16, writes it to its own 128-byte-swizzled staging
 //               buffer and issues asynchronous TMA stores (rows >= M and
 //               columns >= N are clipped by the tensor map); FP32 outputs,
 //               unaligned row strides and the rows of a grouped tile that
 //               reach past the expert's segment are stored directly, masked.
-//   warps 2-3   idle.
+//   warp 2      scale loader: copies each slice's row and column-block
+//               scales into a shared ring ahead of the promote warps.
+//   warp 3      idle.
 // Every mbarrier wait is bounded (WAIT_LIMIT_NS); on expiry the kernel sets
 // the device error word, stops all roles, drains its own TMA copies and MMAs,
 // frees TMEM and returns.
@@ -47,21 +49,25 @@ constexpr int EPI_WARP_BYTES = 32 * 128;                 // one 32-row x 64-col 
 constexpr int GEMM_THREADS = 384;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_EXPERTS = 2048;
+constexpr int SCALE_SLOTS = 8;                           // slices of scales staged ahead
+constexpr int SCALE_SLOT_FLOATS = 132;                   // 128 row scales + 2 column-block scales (+pad)
+constexpr int SCALE_LOOKAHEAD = 2;                       // loader copy groups in flight
 
 // Shared-memory layout for S pipeline stages and E epilogue boxes per promote
-// warp (offsets from a 1024-byte aligned base).  Long-K GEMMs take S = 4,
-// E = 1 (deeper operand pipeline; the epilogue is rare); short-K GEMMs and the
-// grouped GEMM take S = 3, E = 2 (both output halves of a warp are staged at
-// once, so a tile's stores never wait on each other).
+// warp (offsets from a 1024-byte aligned base).  Both GEMMs use S = 3, E = 2:
+// both output halves of a warp are staged at once, so a tile's stores never
+// wait on each other; the scale ring and (grouped) the expert tile table
+// take the rest of the 227 KiB.
 template <int S, int E>
 struct Layout {
     static constexpr int A = 0;
     static constexpr int B = A + S * A_STAGE_BYTES;
     static constexpr int EPI = B + S * B_STAGE_BYTES;                // 8 warps x E x 4 KiB
     static constexpr int BAR = EPI + 8 * E * EPI_WARP_BYTES;        // 8-byte barriers
-    static constexpr int NUM_BARS = 2 * S + 2 + 2 + 1;              // full, empty, pfull, pempty, drain
+    static constexpr int NUM_BARS = 2 * S + 2 + 2 + 1 + 2 * SCALE_SLOTS;  // + sready, sfree
     static constexpr int MISC = BAR + NUM_BARS * 8;                 // tmem slot, abort flag
-    static constexpr int TILES = MISC + 16;                         // grouped: tile prefix [E+1]
+    static constexpr int SCALES = MISC + 16;                        // scale ring
+    static constexpr int TILES = SCALES + SCALE_SLOTS * SCALE_SLOT_FLOATS * 4;  // grouped: tile prefix [E+1]
 };
 
 template <bool GROUPED, int S, int E>
@@ -129,6 +135,9 @@ struct SharedState {
     __device__ uint32_t pfull(int p) const { return bar(2 * S + p); }
     __device__ uint32_t pempty(int p) const { return bar(2 * S + 2 + p); }
     __device__ uint32_t drain() const { return bar(2 * S + 4); }
+    __device__ uint32_t sready(int j) const { return bar(2 * S + 5 + j); }
+    __device__ uint32_t sfree(int j) const { return bar(2 * S + 5 + SCALE_SLOTS + j); }
+    __device__ uint32_t scale_slot(int j) const { return base + L::SCALES + j * SCALE_SLOT_FLOATS * 4; }
     __device__ uint32_t a_stage(int s) const { return base + L::A + s * A_STAGE_BYTES; }
     __device__ uint32_t b_stage(int s) const { return base + L::B + s * B_STAGE_BYTES; }
     __device__ volatile uint32_t *tmem_slot() const
@@ -318,6 +327,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             ptx::mbar_init(ss.pempty(p), 256);
         }
         ptx::mbar_init(ss.drain(), 1);
+        for (int j = 0; j < SCALE_SLOTS; ++j) {
+            ptx::mbar_init(ss.sready(j), 32);          // every lane of the loader warp
+            ptx::mbar_init(ss.sfree(j), 256);          // every promote thread
+        }
         *ss.abort_flag() = 0u;
         ptx::fence_mbarrier_init();
     }
@@ -413,7 +426,55 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             ptx::mma_commit(ss.drain());
             wait_drain(ss.drain(), 0);
         }
-        __syncwarp();                                // warps 2-3 have no role
+        if (warp == 2) {
+            // -------------------------------------------- scale loader
+            // Stages each slice's 128 row scales sA[kb][m0 .. m0+127] and the
+            // two column-block scales of the tile into a SCALE_SLOTS-deep
+            // shared ring (cp.async, SCALE_LOOKAHEAD slices of copies in
+            // flight), so that the promote warps never wait on global memory.
+            uint32_t sit = 0, done = 0;
+            bool ok = true;
+            auto publish = [&](uint32_t j) {             // slice j's copies have landed
+                ptx::mbar_arrive(ss.sready((int)(j % SCALE_SLOTS)));
+            };
+            for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+                const Tile tl = tile_at<GROUPED, STAGES, EPI_BOXES>(g, ss, t);
+                for (int kb = 0; kb < g.KB; ++kb, ++sit) {
+                    const int slot = (int)(sit % SCALE_SLOTS);
+                    if (!wait_bounded(ss, ss.sfree(slot), ((sit / SCALE_SLOTS) & 1u) ^ 1u)) { ok = false; break; }
+                    const uint32_t dst = ss.scale_slot(slot);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = lane + 32 * i;
+                        const int64_t gm = tl.m0 + r;
+                        const bool in = gm < tl.m_end;
+                        ptx::cp_async_4(dst + 4 * r, in ? (const void *)(g.sA + (int64_t)kb * g.M + gm) : (const void *)g.sA,
+                                        in ? 4u : 0u);
+                    }
+                    if (lane < 2) {
+                        const int nblk = (tl.n0 >> 7) + lane;
+                        const bool in = nblk < g.NB128;
+                        const float *src;
+                        if constexpr (GROUPED)
+                            src = g.sB + ((int64_t)tl.expert * g.NB128 + nblk) * g.KB + kb;
+                        else if constexpr (B_MN)
+                            src = g.sB + (int64_t)kb * g.NB128 + nblk;
+                        else
+                            src = g.sB + (int64_t)nblk * g.KB + kb;
+                        ptx::cp_async_4(dst + 4 * (128 + lane), in ? (const void *)src : (const void *)g.sB, in ? 4u : 0u);
+                    }
+                    ptx::cp_async_commit();
+                    if (sit >= (uint32_t)SCALE_LOOKAHEAD) {
+                        ptx::cp_async_wait<SCALE_LOOKAHEAD>();
+                        publish(done++);
+                    }
+                }
+            }
+            ptx::cp_async_wait<0>();
+            while (done < sit)
+                publish(done++);
+        }
+        __syncwarp();                                // warp 3 has no role
     } else {
         ptx::setmaxnreg_inc<224>();
         // ------------------------------------------------ promote + epilogue
@@ -429,40 +490,19 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const Tile tl = tile_at<GROUPED, STAGES, EPI_BOXES>(g, ss, t);
             const int64_t gm = tl.m0 + row;
             const bool row_ok = gm < tl.m_end;
-            const int nblk = (tl.n0 + col_half) >> 7;              // 128-column scale block
-            const bool col_ok = nblk < g.NB128;
-            const float *sBrow;
-            int64_t sb_stride;
-            if constexpr (GROUPED) {
-                sBrow = g.sB + ((int64_t)tl.expert * g.NB128 + nblk) * g.KB;
-                sb_stride = 1;
-            } else if constexpr (B_MN) {
-                sBrow = g.sB + nblk;
-                sb_stride = g.NB128;
-            } else {
-                sBrow = g.sB + (int64_t)nblk * g.KB;
-                sb_stride = 1;
-            }
-            const float *sArow = g.sA + gm;
             float2 acc2[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j)
                 acc2[j] = make_float2(0.0f, 0.0f);
-            // Scales travel through a 2-deep register queue: the loads for
-            // slice kb+2 are issued while slice kb is promoted, so their L2
-            // latency is covered by two slices of work.
-            auto load_sa = [&](int k) {
-                return ptx::ld_f32_early(sArow + (int64_t)min(k, g.KB - 1) * g.M, row_ok && k < g.KB);
-            };
-            auto load_sb = [&](int k) {
-                return ptx::ld_f32_early(sBrow + (int64_t)min(k, g.KB - 1) * sb_stride, col_ok && k < g.KB);
-            };
-            float sa0 = load_sa(0), sa1 = load_sa(1);
-            float sb0 = load_sb(0), sb1 = load_sb(1);
             for (int kb = 0; kb < g.KB; ++kb, ++pit) {
-                const float scale = sa0 * sb0;
-                sa0 = sa1; sa1 = load_sa(kb + 2);
-                sb0 = sb1; sb1 = load_sb(kb + 2);
+                // this slice's scales from the shared ring (staged by warp 2)
+                const int slot = (int)(pit % SCALE_SLOTS);
+                if (!wait_bounded(ss, ss.sready(slot), (pit / SCALE_SLOTS) & 1u)) { ok = false; break; }
+                float sa, sb;
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sa) : "r"(ss.scale_slot(slot) + 4 * row));
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sb) : "r"(ss.scale_slot(slot) + 4 * (128 + wg)));
+                ptx::mbar_arrive(ss.sfree(slot));
+                const float scale = sa * sb;
                 const int p = pit & 1;
                 const uint32_t pph = (pit >> 1) & 1u;
                 if (!wait_bounded(ss, ss.pfull(p), pph)) { ok = false; break; }
