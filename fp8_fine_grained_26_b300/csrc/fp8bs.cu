@@ -25,7 +25,10 @@ struct DeviceInfo {
     bool is_sm103 = false;
     int num_sms = 0;
     bool attrs_set = false;
+    int max_pairs = 0;      // co-resident CTA pairs of the dense GEMM
 };
+
+constexpr int PAIR_STAGES = 4;      // 4 x 32 KiB operand stages per CTA of a pair
 
 std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
@@ -55,20 +58,42 @@ int current_device(DeviceInfo **info)
     if (!d.is_sm103)
         return FP8BS_ERR_DEVICE;
     if (!d.attrs_set) {
-        if (cudaFuncSetAttribute(fp8_gemm_kernel<false, false, 3, 2>,
+        const int pair_smem = gemm_smem_bytes<false, PAIR_STAGES, B_STAGE_BYTES / 2>();
+        if (cudaFuncSetAttribute(fp8_gemm_kernel<false, false, false, 3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 gemm_smem_bytes<false, 3, 2>()) != cudaSuccess ||
-            cudaFuncSetAttribute(fp8_gemm_kernel<false, true, 3, 2>,
+                                 gemm_smem_bytes<false, 3>()) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, true, false, 3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 gemm_smem_bytes<false, 3, 2>()) != cudaSuccess ||
-            cudaFuncSetAttribute(fp8_gemm_kernel<true, false, 3, 2>,
+                                 gemm_smem_bytes<false, 3>()) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, false, true, PAIR_STAGES>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, true, true, PAIR_STAGES>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<true, false, false, 3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 gemm_smem_bytes<true, 3, 2>()) != cudaSuccess ||
+                                 gemm_smem_bytes<true, 3>()) != cudaSuccess ||
             cudaFuncSetAttribute(quant_act_1x128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  quant_smem_bytes()) != cudaSuccess ||
             cudaFuncSetAttribute(quant_w_128x128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  quant_smem_bytes()) != cudaSuccess)
             return FP8BS_ERR_LAUNCH;
+        // how many CTA pairs (2-CTA clusters) fit at once
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(d.num_sms & ~1));
+        cfg.blockDim = dim3(GEMM_THREADS);
+        cfg.dynamicSmemBytes = pair_smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, fp8_gemm_kernel<false, false, true, PAIR_STAGES>, &cfg) != cudaSuccess)
+            clusters = 0;
+        cudaGetLastError();
+        d.max_pairs = std::min(clusters, d.num_sms / 2);
         d.attrs_set = true;
     }
     if (!g_encode) {
@@ -123,7 +148,7 @@ bool encode_c_bf16(CUtensorMap *m, void *C, uint64_t N, uint64_t M, uint64_t ldc
 {
     const cuuint64_t dims[2] = {N, M};
     const cuuint64_t strides[1] = {ldc * 2};
-    const cuuint32_t box[2] = {64, 32};
+    const cuuint32_t box[2] = {64, BM};            // one promote warpgroup's 64-column half
     const cuuint32_t estr[2] = {1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -263,8 +288,15 @@ int fp8_gemm_blockscaled(const void *qA, const float *sA, const void *qB, const 
     if (!encode_2d_u8(&tmA, qA, (uint64_t)K, (uint64_t)M, (uint64_t)K, BK, BM))
         return FP8BS_ERR_ARG;
     bool ok;
+    // Dense GEMMs of two or more M-blocks run on CTA pairs (256 x 256 tiles,
+    // each CTA holding its 128 rows of A and half of the B block).
+#ifndef FP8BS_NO_PAIR
+    const bool pair = dev->max_pairs > 0 && M > BM;
+#else
+    const bool pair = false;
+#endif
     if (b_major == FP8BS_B_KMAJOR)
-        ok = encode_2d_u8(&tmB, qB, (uint64_t)K, (uint64_t)N, (uint64_t)K, BK, BN);
+        ok = encode_2d_u8(&tmB, qB, (uint64_t)K, (uint64_t)N, (uint64_t)K, BK, pair ? 128 : BN);
     else
         ok = encode_2d_u8(&tmB, qB, (uint64_t)N, (uint64_t)K, (uint64_t)N, 128, BK);
     if (!ok)
@@ -288,12 +320,34 @@ int fp8_gemm_blockscaled(const void *qA, const float *sA, const void *qB, const 
     g.num_n_blk = (int)((N + BN - 1) / BN);
     g.KB = (int)(K / BK);
     g.NB128 = (int)((N + 127) / 128);
+    g.num_m_pair = (g.num_m_blk + 1) / 2;
+    if (pair) {
+        g.num_tiles = (int64_t)g.num_m_pair * g.num_n_blk;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(g.num_tiles, dev->max_pairs)));
+        cfg.blockDim = dim3(GEMM_THREADS);
+        cfg.dynamicSmemBytes = gemm_smem_bytes<false, PAIR_STAGES, B_STAGE_BYTES / 2>();
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e;
+        if (b_major == FP8BS_B_KMAJOR)
+            e = cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES>, tmA, tmB, tmC, g);
+        else
+            e = cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, true, true, PAIR_STAGES>, tmA, tmB, tmC, g);
+        return e == cudaSuccess ? launch_status() : (cudaGetLastError(), FP8BS_ERR_LAUNCH);
+    }
     g.num_tiles = (int64_t)g.num_m_blk * g.num_n_blk;
     const int grid = (int)std::min<int64_t>(g.num_tiles, dev->num_sms);
     if (b_major == FP8BS_B_KMAJOR)
-        fp8_gemm_kernel<false, false, 3, 2><<<grid, GEMM_THREADS, gemm_smem_bytes<false, 3, 2>(), stream>>>(tmA, tmB, tmC, g);
+        fp8_gemm_kernel<false, false, false, 3><<<grid, GEMM_THREADS, gemm_smem_bytes<false, 3>(), stream>>>(tmA, tmB, tmC, g);
     else
-        fp8_gemm_kernel<false, true, 3, 2><<<grid, GEMM_THREADS, gemm_smem_bytes<false, 3, 2>(), stream>>>(tmA, tmB, tmC, g);
+        fp8_gemm_kernel<false, true, false, 3><<<grid, GEMM_THREADS, gemm_smem_bytes<false, 3>(), stream>>>(tmA, tmB, tmC, g);
     return launch_status();
 }
 
@@ -343,7 +397,7 @@ int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA, const void *qB
     g.KB = (int)(K / BK);
     g.NB128 = (int)((N + 127) / 128);
     g.num_tiles = 0;
-    fp8_gemm_kernel<true, false, 3, 2><<<dev->num_sms, GEMM_THREADS, gemm_smem_bytes<true, 3, 2>(), stream>>>(tmA, tmB, tmC, g);
+    fp8_gemm_kernel<true, false, false, 3><<<dev->num_sms, GEMM_THREADS, gemm_smem_bytes<true, 3>(), stream>>>(tmA, tmB, tmC, g);
     return launch_status();
 }
 

@@ -9,29 +9,38 @@
 //     C[m][n] = sum_kb sA[kb][m] * sB(n, kb) * P_kb[m][n],
 //     P_kb[m][n] = sum_{k in 128-wide slice kb} qA[m][k] * qB(n, k)   (exact FP8 products)
 //
-// Design (one persistent CTA per SM, 384 threads, 128 x 256 output tile):
-//   warp 0      TMA producer: one 128-K slice of A (128x128 B) and B (256x128 B)
-//               per pipeline stage, 128-byte swizzle, STAGES-deep ring.
+// Design (one persistent 384-thread CTA per SM; each CTA owns a 128 x 256
+// FP32 output tile at a time):
+//   warp 0      TMA producer: one 128-K slice of A (128x128 B) and B per
+//               pipeline stage, 128-byte swizzle, STAGES-deep ring.
 //   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) write a
-//               FRESH 128x256 FP32 partial P_kb into one of two TMEM buffers
-//               (2 x 256 columns = all 512), then tcgen05.commit frees the
-//               smem stage and signals the partial.
+//               FRESH FP32 partial P_kb into one of two 256-column TMEM
+//               buffers (2 x 256 columns = all 512), then tcgen05.commit
+//               frees the smem stage and signals the partial.
 //   warps 4-11  promote / epilogue: two warpgroups, each owning 128 of the
 //               256 columns; thread = tile row.  Per slice they load the
 //               partial from TMEM (two 64-column tcgen05.ld 32x32b) and apply
 //               acc = fma(P, sA*sB, acc) with packed f32x2 FMAs in FP32
 //               registers -- the pages' promotion, on CUDA cores -- then
 //               release the TMEM buffer so the MMA of slice kb+2 can start
-//               while slice kb+1 is promoted.  The scales come from a
-//               shared ring that warp 2 fills ahead of time.  After the last slice each warp rounds its 32 x 128
-//               block to BF16, writes it to its own 128-byte-swizzled staging
-//               buffer and issues asynchronous TMA stores (rows >= M and
-//               columns >= N are clipped by the tensor map); FP32 outputs,
-//               unaligned row strides and the rows of a grouped tile that
-//               reach past the expert's segment are stored directly, masked.
+//               while slice kb+1 is promoted.  After the last slice each
+//               warpgroup rounds its 128 x 128 block to BF16 into two
+//               128-row, 128-byte-swizzled staging boxes and one thread issues
+//               the two TMA stores (rows >= M and columns >= N are clipped by
+//               the tensor map); FP32 outputs, unaligned row strides and the
+//               rows of a grouped tile that reach past the expert's segment
+//               are stored directly, masked.
 //   warp 2      scale loader: copies each slice's row and column-block
 //               scales into a shared ring ahead of the promote warps.
 //   warp 3      idle.
+// CTA pairs (PAIR, dense GEMMs of two or more M-blocks): a 2-CTA cluster
+// computes a 256 x 256 tile with tcgen05 cta_group::2 MMAs (M = 256).  Each
+// CTA stages only its own 128 rows of A and half (128 rows) of the B block,
+// 32 KiB per stage instead of 48, and both CTAs' copies complete on the
+// leader CTA's `full` barrier; the leader issues the MMAs and multicasts its
+// commits to both CTAs; every promote warp of either CTA releases a TMEM
+// buffer with one arrive on the leader's barrier.  Each CTA still promotes
+// and stores its own 128 x 256 half.
 // Every mbarrier wait is bounded (WAIT_LIMIT_NS); on expiry the kernel sets
 // the device error word, stops all roles, drains its own TMA copies and MMAs,
 // frees TMEM and returns.
@@ -45,7 +54,7 @@ constexpr int BN = 256;
 constexpr int BK = 128;
 constexpr int A_STAGE_BYTES = BM * BK;                   // 16 KiB
 constexpr int B_STAGE_BYTES = BN * BK;                   // 32 KiB
-constexpr int EPI_WARP_BYTES = 32 * 128;                 // one 32-row x 64-col BF16 box
+constexpr int EPI_BOX_BYTES = BM * 128;                 // one 128-row x 64-col BF16 output box
 constexpr int GEMM_THREADS = 384;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_EXPERTS = 2048;
@@ -53,27 +62,28 @@ constexpr int SCALE_SLOTS = 8;                           // slices of scales sta
 constexpr int SCALE_SLOT_FLOATS = 132;                   // 128 row scales + 2 column-block scales (+pad)
 constexpr int SCALE_LOOKAHEAD = 2;                       // loader copy groups in flight
 
-// Shared-memory layout for S pipeline stages and E epilogue boxes per promote
-// warp (offsets from a 1024-byte aligned base).  Both GEMMs use S = 3, E = 2:
-// both output halves of a warp are staged at once, so a tile's stores never
-// wait on each other; the scale ring and (grouped) the expert tile table
-// take the rest of the 227 KiB.
-template <int S, int E>
+// Shared-memory layout for S pipeline stages of BSB bytes of B each
+// (offsets from a 1024-byte aligned base): operand stages, the output staging
+// boxes (two 64-column halves per promote warpgroup, so a tile's stores never
+// wait on each other), barriers, the scale ring and (grouped) the expert tile
+// table.
+template <int S, int BSB = B_STAGE_BYTES>
 struct Layout {
     static constexpr int A = 0;
     static constexpr int B = A + S * A_STAGE_BYTES;
-    static constexpr int EPI = B + S * B_STAGE_BYTES;                // 8 warps x E x 4 KiB
-    static constexpr int BAR = EPI + 8 * E * EPI_WARP_BYTES;        // 8-byte barriers
-    static constexpr int NUM_BARS = 2 * S + 2 + 2 + 1 + 2 * SCALE_SLOTS;  // + sready, sfree
+    static constexpr int EPI = B + S * BSB;                          // [warpgroup][half] boxes
+    static constexpr int BAR = EPI + 2 * 2 * EPI_BOX_BYTES;         // 8-byte barriers
+    // full, empty, pfull, pempty, drain, sready, sfree, per-warpgroup epilogue pair
+    static constexpr int NUM_BARS = 2 * S + 2 + 2 + 1 + 2 * SCALE_SLOTS + 4;
     static constexpr int MISC = BAR + NUM_BARS * 8;                 // tmem slot, abort flag
     static constexpr int SCALES = MISC + 16;                        // scale ring
     static constexpr int TILES = SCALES + SCALE_SLOTS * SCALE_SLOT_FLOATS * 4;  // grouped: tile prefix [E+1]
 };
 
-template <bool GROUPED, int S, int E>
+template <bool GROUPED, int S, int BSB = B_STAGE_BYTES>
 constexpr int gemm_smem_bytes()
 {
-    return 1024 + Layout<S, E>::TILES + (GROUPED ? (MAX_EXPERTS + 1) * 4 : 0);
+    return 1024 + Layout<S, BSB>::TILES + (GROUPED ? (MAX_EXPERTS + 1) * 4 : 0);
 }
 
 struct GemmArgs {
@@ -88,10 +98,11 @@ struct GemmArgs {
     int c_fp32;
     int c_tma;          // BF16 output through the C tensor map
     int num_m_blk;      // dense: ceil(M/128)
+    int num_m_pair;     // dense, cluster pairs: ceil(num_m_blk / 2)
     int num_n_blk;      // ceil(N/256)
     int KB;             // K/128
     int NB128;          // ceil(N/128)
-    int64_t num_tiles;  // dense: num_m_blk * num_n_blk
+    int64_t num_tiles;  // dense: num_m_blk * num_n_blk (cluster pairs: num_m_pair * num_n_blk)
 };
 
 // tcgen05 instruction descriptor, kind::f8f6f4: D = F32 (bits 4-5 = 1),
@@ -124,9 +135,9 @@ struct Tile {
     int32_t expert;
 };
 
-template <int S, int E>
+template <int S, int BSB = B_STAGE_BYTES>
 struct SharedState {
-    using L = Layout<S, E>;
+    using L = Layout<S, BSB>;
     uint32_t base;      // shared address of the aligned base
     uint8_t *gbase;     // generic pointer to the same
     __device__ uint32_t bar(int i) const { return base + L::BAR + 8 * i; }
@@ -137,9 +148,14 @@ struct SharedState {
     __device__ uint32_t drain() const { return bar(2 * S + 4); }
     __device__ uint32_t sready(int j) const { return bar(2 * S + 5 + j); }
     __device__ uint32_t sfree(int j) const { return bar(2 * S + 5 + SCALE_SLOTS + j); }
+    // warpgroup wg's staging boxes are free (its issuing thread saw the last
+    // stores read them) / filled (all four warps wrote and fenced)
+    __device__ uint32_t epi_free(int wg) const { return bar(2 * S + 5 + 2 * SCALE_SLOTS + wg); }
+    __device__ uint32_t epi_full(int wg) const { return bar(2 * S + 7 + 2 * SCALE_SLOTS + wg); }
+    __device__ uint32_t epi_box(int wg, int h) const { return base + L::EPI + (2 * wg + h) * EPI_BOX_BYTES; }
     __device__ uint32_t scale_slot(int j) const { return base + L::SCALES + j * SCALE_SLOT_FLOATS * 4; }
     __device__ uint32_t a_stage(int s) const { return base + L::A + s * A_STAGE_BYTES; }
-    __device__ uint32_t b_stage(int s) const { return base + L::B + s * B_STAGE_BYTES; }
+    __device__ uint32_t b_stage(int s) const { return base + L::B + s * BSB; }
     __device__ volatile uint32_t *tmem_slot() const
     {
         return reinterpret_cast<volatile uint32_t *>(gbase + L::MISC);
@@ -154,14 +170,14 @@ struct SharedState {
     }
 };
 
-template <int S, int E>
-__device__ __forceinline__ bool wait_bounded(const SharedState<S, E> &ss, uint32_t bar, uint32_t parity)
+template <int S, int BSB>
+__device__ __forceinline__ bool wait_bounded(const SharedState<S, BSB> &ss, uint32_t bar, uint32_t parity)
 {
     return wait_bounded(bar, parity, ss.abort_flag());
 }
 
-template <bool GROUPED, int S, int E>
-__device__ __forceinline__ int64_t total_tiles(const GemmArgs &g, const SharedState<S, E> &ss)
+template <bool GROUPED, int S, int BSB>
+__device__ __forceinline__ int64_t total_tiles(const GemmArgs &g, const SharedState<S, BSB> &ss)
 {
     if constexpr (GROUPED)
         return ss.tile_prefix()[g.E];
@@ -169,8 +185,8 @@ __device__ __forceinline__ int64_t total_tiles(const GemmArgs &g, const SharedSt
         return g.num_tiles;
 }
 
-template <bool GROUPED, int S, int E>
-__device__ __forceinline__ Tile tile_at(const GemmArgs &g, const SharedState<S, E> &ss, int64_t t)
+template <bool GROUPED, bool PAIR, int S, int BSB>
+__device__ __forceinline__ Tile tile_at(const GemmArgs &g, const SharedState<S, BSB> &ss, int64_t t, uint32_t rank)
 {
     Tile tl;
     if constexpr (GROUPED) {
@@ -193,6 +209,16 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &g, const SharedState<S, 
         tl.m_end = seg1;
         tl.n0 = (int32_t)(nb * BN);
         tl.expert = e;
+    } else if constexpr (PAIR) {
+        // work unit = one 256 x 256 tile of a CTA pair; CTA `rank` owns its
+        // M-block 2 * pair + rank (a block past the last one computes on zero
+        // rows and stores nothing)
+        const int64_t nb = t / g.num_m_pair;
+        tl.m0 = (2 * (t - nb * g.num_m_pair) + rank) * BM;
+        tl.m_end = g.M;
+        tl.n0 = (int32_t)(nb * BN);
+        tl.expert = 0;
+        (void)ss;
     } else {
         const int64_t nb = t / g.num_m_blk;
         tl.m0 = (t - nb * g.num_m_blk) * BM;
@@ -207,8 +233,8 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &g, const SharedState<S, 
 // prefix over experts into shared memory.  Offsets are clamped into
 // [0, M_total] and made nondecreasing, so malformed offsets cannot move any
 // access out of bounds.
-template <int S, int E>
-__device__ void build_tile_prefix(const GemmArgs &g, const SharedState<S, E> &ss)
+template <int S, int BSB>
+__device__ void build_tile_prefix(const GemmArgs &g, const SharedState<S, BSB> &ss)
 {
     __shared__ int32_t chunk_sum[GEMM_THREADS];
     int32_t *pre = ss.tile_prefix();
@@ -300,14 +326,15 @@ __device__ __forceinline__ void store_row_direct(const GemmArgs &g, const float2
     }
 }
 
-template <bool GROUPED, bool B_MN, int STAGES, int EPI_BOXES>
+template <bool GROUPED, bool B_MN, bool PAIR, int STAGES>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs g)
 {
-    using L = Layout<STAGES, EPI_BOXES>;
+    constexpr int BSB = PAIR ? B_STAGE_BYTES / 2 : B_STAGE_BYTES;   // pair: this CTA's half of B
+    using L = Layout<STAGES, BSB>;
     extern __shared__ uint8_t smem_raw[];
-    SharedState<STAGES, EPI_BOXES> ss;
+    SharedState<STAGES, BSB> ss;
     {
         const uint32_t raw = ptx::smem_u32(smem_raw);
         const uint32_t aligned = (raw + 1023u) & ~1023u;
@@ -324,12 +351,16 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
         for (int p = 0; p < 2; ++p) {
             ptx::mbar_init(ss.pfull(p), 1);
-            ptx::mbar_init(ss.pempty(p), 256);
+            ptx::mbar_init(ss.pempty(p), PAIR ? 16 : 8);   // one arrive per promote warp (pair: of both CTAs)
         }
         ptx::mbar_init(ss.drain(), 1);
         for (int j = 0; j < SCALE_SLOTS; ++j) {
             ptx::mbar_init(ss.sready(j), 32);          // every lane of the loader warp
             ptx::mbar_init(ss.sfree(j), 256);          // every promote thread
+        }
+        for (int wg = 0; wg < 2; ++wg) {
+            ptx::mbar_init(ss.epi_free(wg), 1);        // the warpgroup's store issuer
+            ptx::mbar_init(ss.epi_full(wg), 4);        // one arrive per warp
         }
         *ss.abort_flag() = 0u;
         ptx::fence_mbarrier_init();
@@ -341,16 +372,28 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             ptx::prefetch_tmap(&tmC);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ss.base + L::MISC, TMEM_COLS);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(ss.base + L::MISC, TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ss.base + L::MISC, TMEM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
     if constexpr (GROUPED)
         build_tile_prefix(g, ss);                    // ends with __syncthreads
     ptx::tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        ptx::cluster_sync();                         // the peer's barriers exist before it is signalled
+    else
+        __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *ss.tmem_slot();
-    const int64_t ntiles = total_tiles<GROUPED, STAGES, EPI_BOXES>(g, ss);
+    // persistent schedule: CTA (pair: cluster) i takes work units i, i + count, ...
+    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+    const int64_t t_first = PAIR ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
+    const int64_t t_stride = PAIR ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
+    const int64_t ntiles = total_tiles<GROUPED>(g, ss);
 
     // Register split, one setmaxnreg per warpgroup (the same instruction for
     // its four warps): 128 x 56 + 256 x 224 = 64512 = the launch's 384 x 168.
@@ -366,16 +409,29 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const uint64_t stream = ptx::policy_evict_first();
             uint32_t it = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-                const Tile tl = tile_at<GROUPED, STAGES, EPI_BOXES>(g, ss, t);
+            for (int64_t t = t_first; ok && t < ntiles; t += t_stride) {
+                const Tile tl = tile_at<GROUPED, PAIR>(g, ss, t, rank);
                 for (int kb = 0; kb < g.KB; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!wait_bounded(ss, ss.empty(s), ph ^ 1u)) { ok = false; break; }
                     const uint32_t fb = ss.full(s);
-                    ptx::mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
                     const uint32_t sa = ss.a_stage(s);
                     const uint32_t sb = ss.b_stage(s);
+                    if constexpr (PAIR) {
+                        // this CTA's A rows and its half of the B block; both
+                        // CTAs' bytes complete on the leader's `full` barrier
+                        const uint32_t fb0 = ptx::mapa_shared(fb, 0);
+                        if (rank == 0)
+                            ptx::mbar_arrive_expect_tx(fb, 2 * (A_STAGE_BYTES + BSB));
+                        ptx::tma_load_2d_pair_hint(sa, &tmA, fb0, kb * BK, (int32_t)tl.m0, keep);
+                        if constexpr (B_MN)
+                            ptx::tma_load_2d_pair(sb, &tmB, fb0, tl.n0 + 128 * (int32_t)rank, kb * BK);
+                        else
+                            ptx::tma_load_2d_pair(sb, &tmB, fb0, kb * BK, tl.n0 + 128 * (int32_t)rank);
+                        continue;
+                    }
+                    ptx::mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
                     ptx::tma_load_2d_hint(sa, &tmA, fb, kb * BK, (int32_t)tl.m0, keep);
                     if constexpr (GROUPED) {
                         ptx::tma_load_3d_hint(sb, &tmB, fb, kb * BK, tl.n0, tl.expert, stream);
@@ -387,16 +443,19 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     }
                 }
             }
-            // Drain: every copy this thread issued must land before exit.
+            // Drain: every copy this thread issued must land before exit.  (A
+            // pair's second CTA completes its bytes on the leader's barriers,
+            // which the leader's MMA waits on before the final cluster sync.)
             const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
-            for (uint32_t j = first; j < it; ++j)
-                wait_drain(ss.full(j % STAGES), (j / STAGES) & 1u);
-        } else if (warp == 1 && lane == 0) {
-            // -------------------------------------------- MMA issuer
-            constexpr uint32_t idesc = make_idesc(BM, BN, B_MN);
+            if (rank == 0)
+                for (uint32_t j = first; j < it; ++j)
+                    wait_drain(ss.full(j % STAGES), (j / STAGES) & 1u);
+        } else if (warp == 1 && lane == 0 && rank == 0) {
+            // -------------------------------------------- MMA issuer (pair: leader CTA, M = 256)
+            constexpr uint32_t idesc = make_idesc(PAIR ? 2 * BM : BM, BN, B_MN);
             uint32_t it = 0, pit = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+            for (int64_t t = t_first; ok && t < ntiles; t += t_stride) {
                 for (int kb = 0; kb < g.KB; ++kb, ++it, ++pit) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -416,14 +475,26 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             bd = make_sdesc_sw128(sb + kk * 32 * 128, B_STAGE_BYTES / 2, 1024);
                         else
                             bd = make_sdesc_sw128(sb + kk * 32, 16, 1024);
-                        ptx::mma_f8f6f4(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                        if constexpr (PAIR)
+                            ptx::mma_f8f6f4_pair(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                        else
+                            ptx::mma_f8f6f4(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
                     }
-                    ptx::mma_commit(ss.empty(s));
-                    ptx::mma_commit(ss.pfull(p));
+                    if constexpr (PAIR) {
+                        // stage free and partial ready, in both CTAs
+                        ptx::mma_commit_pair_mc(ss.empty(s), 0x3);
+                        ptx::mma_commit_pair_mc(ss.pfull(p), 0x3);
+                    } else {
+                        ptx::mma_commit(ss.empty(s));
+                        ptx::mma_commit(ss.pfull(p));
+                    }
                 }
             }
             // Drain: all MMAs this thread issued complete before TMEM is freed.
-            ptx::mma_commit(ss.drain());
+            if constexpr (PAIR)
+                ptx::mma_commit_pair(ss.drain());
+            else
+                ptx::mma_commit(ss.drain());
             wait_drain(ss.drain(), 0);
         }
         if (warp == 2) {
@@ -437,8 +508,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             auto publish = [&](uint32_t j) {             // slice j's copies have landed
                 ptx::mbar_arrive(ss.sready((int)(j % SCALE_SLOTS)));
             };
-            for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-                const Tile tl = tile_at<GROUPED, STAGES, EPI_BOXES>(g, ss, t);
+            for (int64_t t = t_first; ok && t < ntiles; t += t_stride) {
+                const Tile tl = tile_at<GROUPED, PAIR>(g, ss, t, rank);
                 for (int kb = 0; kb < g.KB; ++kb, ++sit) {
                     const int slot = (int)(sit % SCALE_SLOTS);
                     if (!wait_bounded(ss, ss.sfree(slot), ((sit / SCALE_SLOTS) & 1u) ^ 1u)) { ok = false; break; }
@@ -482,12 +553,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const int quarter = warp & 3;                // TMEM lane quarter
         const int row = quarter * 32 + lane;         // tile row owned by this thread
         const int col_half = wg * 128;
-        const uint32_t epi = ss.base + L::EPI + (uint32_t)(warp - 4) * EPI_BOXES * EPI_WARP_BYTES;
         const uint64_t c_policy = ptx::policy_evict_first();   // C is written once, never re-read
-        uint32_t pit = 0;
+        const bool issuer = quarter == 0 && lane == 0;     // the warpgroup's store issuer
+        uint32_t pit = 0, eit = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-            const Tile tl = tile_at<GROUPED, STAGES, EPI_BOXES>(g, ss, t);
+        for (int64_t t = t_first; ok && t < ntiles; t += t_stride) {
+            const Tile tl = tile_at<GROUPED, PAIR>(g, ss, t, rank);
             const int64_t gm = tl.m0 + row;
             const bool row_ok = gm < tl.m_end;
             float2 acc2[64];
@@ -518,72 +589,54 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 ptx::tmem_ld_32x32b_x64(taddr + 64, r);
                 ptx::tmem_ld_wait(r);
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(ss.pempty(p));
+                __syncwarp();                            // the warp's partial is in registers
+                if constexpr (PAIR)
+                    ptx::mbar_arrive_cluster_if(ptx::mapa_shared(ss.pempty(p), 0), lane == 0);   // the leader's MMA
+                else
+                    ptx::mbar_arrive_cluster_if(ss.pempty(p), lane == 0);
                 promote64(acc2 + 32, r, scale);
             }
             if (!ok)
                 break;
-            // ---- epilogue: rows [m0 + 32*quarter, +32), columns [n0 + col_half, +128)
+            // ---- epilogue: the warpgroup's rows [m0, m0 + 128), columns [n0 + col_half, +128)
             const int64_t n_first = tl.n0 + col_half;
-            if (n_first >= g.N)
-                continue;
-            const int64_t wrow0 = tl.m0 + quarter * 32;
-            if (wrow0 >= tl.m_end)
-                continue;
+            if (n_first >= g.N || tl.m0 >= tl.m_end)
+                continue;                                // uniform over the warpgroup
             // TMA clips rows at M; a grouped tile may not write past its segment.
-            const bool warp_tma = g.c_tma && (wrow0 + 32 <= tl.m_end || tl.m_end == g.M);
-            if (warp_tma) {
-                const bool two = n_first + 64 < g.N;            // second 64-column box exists
-                if constexpr (EPI_BOXES == 2) {
-                    // both halves staged at once: one proxy fence, one commit
-                    if (lane == 0)
-                        ptx::bulk_wait_read_all();              // the previous tile's stores read them
-                    __syncwarp();
+            const bool wg_tma = g.c_tma && (tl.m0 + BM <= tl.m_end || tl.m_end == g.M);
+            if (wg_tma) {
+                // Stage both 64-column halves as 128-row, 128-byte-swizzled
+                // boxes shared by the warpgroup's four warps, then one thread
+                // issues the two TMA stores.  The hand-offs are mbarriers with
+                // bounded waits, so an aborting warp cannot strand the others.
+                const uint32_t ph = eit & 1u;
+                ++eit;
+                if (issuer) {
+                    ptx::bulk_wait_read_all();              // the previous tile's stores read the boxes
+                    ptx::mbar_arrive(ss.epi_free(wg));
+                }
+                if (!wait_bounded(ss, ss.epi_free(wg), ph)) { ok = false; break; }
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t buf = epi + h * EPI_WARP_BYTES + lane * 128;
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t buf = ss.epi_box(wg, h) + (uint32_t)row * 128;
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const float2 *v = acc2 + h * 32 + c * 4;
-                            ptx::st_shared_v4(buf + ((c ^ (lane & 7)) << 4),
-                                              ptx::cvt_bf16x2(v[0].x, v[0].y), ptx::cvt_bf16x2(v[1].x, v[1].y),
-                                              ptx::cvt_bf16x2(v[2].x, v[2].y), ptx::cvt_bf16x2(v[3].x, v[3].y));
-                        }
+                    for (int c = 0; c < 8; ++c) {
+                        const float2 *v = acc2 + h * 32 + c * 4;
+                        ptx::st_shared_v4(buf + ((c ^ (lane & 7)) << 4),
+                                          ptx::cvt_bf16x2(v[0].x, v[0].y), ptx::cvt_bf16x2(v[1].x, v[1].y),
+                                          ptx::cvt_bf16x2(v[2].x, v[2].y), ptx::cvt_bf16x2(v[3].x, v[3].y));
                     }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_2d_hint(&tmC, epi, (int32_t)n_first, (int32_t)wrow0, c_policy);
-                        if (two)
-                            ptx::tma_store_2d_hint(&tmC, epi + EPI_WARP_BYTES, (int32_t)(n_first + 64),
-                                                   (int32_t)wrow0, c_policy);
-                        ptx::bulk_commit();
-                    }
-                } else {
-                    // one staging box, reused for the second half
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (h == 1 && !two)
-                            break;
-                        if (lane == 0)
-                            ptx::bulk_wait_read_all();
-                        __syncwarp();
-                        const uint32_t buf = epi + lane * 128;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const float2 *v = acc2 + h * 32 + c * 4;
-                            ptx::st_shared_v4(buf + ((c ^ (lane & 7)) << 4),
-                                              ptx::cvt_bf16x2(v[0].x, v[0].y), ptx::cvt_bf16x2(v[1].x, v[1].y),
-                                              ptx::cvt_bf16x2(v[2].x, v[2].y), ptx::cvt_bf16x2(v[3].x, v[3].y));
-                        }
-                        ptx::fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            ptx::tma_store_2d_hint(&tmC, epi, (int32_t)(n_first + h * 64), (int32_t)wrow0,
-                                                   c_policy);
-                            ptx::bulk_commit();
-                        }
-                    }
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                ptx::mbar_arrive_cluster_if(ss.epi_full(wg), lane == 0);
+                if (issuer) {
+                    if (!wait_bounded(ss, ss.epi_full(wg), ph)) { ok = false; break; }
+                    ptx::tma_store_2d_hint(&tmC, ss.epi_box(wg, 0), (int32_t)n_first, (int32_t)tl.m0, c_policy);
+                    if (n_first + 64 < g.N)                // second 64-column box exists
+                        ptx::tma_store_2d_hint(&tmC, ss.epi_box(wg, 1), (int32_t)(n_first + 64), (int32_t)tl.m0,
+                                               c_policy);
+                    ptx::bulk_commit();
                 }
             } else if (row_ok) {
                 store_row_direct(g, acc2, gm, n_first);
@@ -595,10 +648,16 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
 
     ptx::tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        ptx::cluster_sync();                         // the pair's MMAs, copies and signals are done
+    else
+        __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR)
+            ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            ptx::tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 

@@ -150,6 +150,44 @@ def test_gemm_output_row_stride():
     assert torch.all(big[:, 200:] == 5.0)
 
 
+@pytest.mark.parametrize("b_major", [0, 1])
+def test_gemm_pair_tail_rows_untouched(b_major):
+    # 3 M-blocks: the CTA-pair kernel runs a second pair whose second CTA has
+    # no rows; nothing may be written below row M or right of column N.
+    g = generator(8 + b_major, DEV)
+    M, N, K = 300, 512 if b_major else 520, 384
+    a = normal_bf16((M, K), 1.0, g, DEV)
+    w = normal_bf16((N, K) if b_major == 0 else (K, N), 0.02, g, DEV)
+    qa, sa = fp8.fp8_quant_act_1x128(a)
+    qb, sb = fp8.fp8_quant_w_128x128(w)
+    big = torch.full((M + 12, N + 24), 3.0, dtype=torch.bfloat16, device=DEV)
+    fp8.fp8_gemm_blockscaled(qa, sa, qb, sb, b_major=b_major, C=big[:M, :N])
+    ref = fp8.fp8_gemm_blockscaled(qa, sa, qb, sb, b_major=b_major)
+    torch.cuda.synchronize()
+    assert torch.equal(big[:M, :N], ref)
+    assert torch.all(big[M:] == 3.0) and torch.all(big[:, N:] == 3.0)
+
+
+@pytest.mark.parametrize("b_major", [0, 1])
+def test_gemm_pair_matches_single_cta(b_major):
+    # M > 128 runs on CTA pairs, M <= 128 on single CTAs: the same rows must
+    # come out bit-identical (same slices, same promotion order).
+    g = generator(12 + b_major, DEV)
+    M, N, K = 384, 768, 1024
+    a = normal_bf16((M, K), 1.0, g, DEV, outlier_p=0.01, outlier_scale=30.0)
+    w = normal_bf16((N, K) if b_major == 0 else (K, N), 0.02, g, DEV)
+    qa, sa = fp8.fp8_quant_act_1x128(a)
+    qb, sb = fp8.fp8_quant_w_128x128(w)
+    for dt in (torch.bfloat16, torch.float32):
+        c_pair = fp8.fp8_gemm_blockscaled(qa, sa, qb, sb, b_major=b_major, out_dtype=dt)
+        for r0 in (0, 128, 256):
+            c_one = fp8.fp8_gemm_blockscaled(qa[r0:r0 + 128], sa[:, r0:r0 + 128].contiguous(), qb, sb,
+                                             b_major=b_major, out_dtype=dt)
+            torch.cuda.synchronize()
+            assert torch.equal(c_pair[r0:r0 + 128].view(torch.int16 if dt == torch.bfloat16 else torch.int32),
+                               c_one.view(torch.int16 if dt == torch.bfloat16 else torch.int32)), (dt, r0)
+
+
 def test_gemm_tiny_workload_full():
     c = synthetic.tiny(device=DEV)
     full_check(c.a, c.w, 0, torch.float32, "tiny 128x256x512 fp32")
