@@ -34,7 +34,7 @@ _STATUS_NAMES = {
 }
 
 EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
-            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error")
+            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout")
 
 
 class Fp8bsError(RuntimeError):
@@ -55,6 +55,7 @@ def _load():
         "fp8_gemm_blockscaled": [p, p, p, p, i64, i64, i64, i32, p, i32, i64, p],
         "fp8_grouped_gemm_blockscaled": [p, p, p, p, p, i32, i64, i64, i64, p, i32, i64, p],
         "fp8bs_last_error": [p],
+        "fp8bs_selftest_wait_timeout": [i64, p],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -201,6 +202,14 @@ def fp8bs_last_error(stream=None):
     return lib.fp8bs_last_error(_stream(stream))
 
 
+def fp8bs_selftest_wait_timeout(limit_us=20000, stream=None):
+    """Enqueue the failure-detection self-test: a device wait that nothing
+    ends runs out after ``limit_us`` and is recorded in the error word (read
+    it with fp8bs_last_error)."""
+    _check(lib.fp8bs_selftest_wait_timeout(int(limit_us), _stream(stream)), "fp8bs_selftest_wait_timeout")
+
+
 __all__ = ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
-           "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "Fp8bsError", "lib",
+           "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout",
+           "Fp8bsError", "lib",
            "LIB_PATH", "EXPORTED", "B_KMAJOR", "B_MNMAJOR", "OUT_BF16", "OUT_FP32"]

@@ -12,10 +12,11 @@ __device__ unsigned int g_error_word;
 
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;        // 2 s
 
-// Wait for phase `parity` of barrier `bar`, giving up after WAIT_LIMIT_NS or
+// Wait for phase `parity` of barrier `bar`, giving up after `limit_ns` or
 // as soon as *abort is set.  On time-out it sets *abort and the error word.
 // Returns true when the phase completed.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t *abort)
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t *abort,
+                                             uint64_t limit_ns = WAIT_LIMIT_NS)
 {
     if (ptx::mbar_try_wait(bar, parity))
         return true;
@@ -26,7 +27,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
         if ((it & 15u) == 0) {
             if (*abort)
                 return false;
-            if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+            if (ptx::globaltimer_ns() - t0 > limit_ns) {
                 *abort = 1u;
                 atomicOr(&g_error_word, 1u);
                 return false;

@@ -209,6 +209,28 @@ int check_gemm_common(const void *qA, const float *sA, const void *qB, const flo
 
 } // namespace
 
+namespace fp8bs {
+
+// One warp; lane 0 waits on a fresh mbarrier that nothing arrives at, with the
+// pipelines' bounded wait and the given limit.
+__global__ void selftest_wait_kernel(uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    const uint32_t b = ptx::smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(b, 1);
+        abort_flag = 0u;
+        ptx::fence_mbarrier_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0)
+        wait_bounded(b, 0u, &abort_flag, limit_ns);
+    __syncwarp();
+}
+
+} // namespace fp8bs
+
 extern "C" {
 
 int fp8_quant_act_1x128(const void *x_bf16, int64_t M, int64_t K, int64_t ldx, void *q_e4m3,
@@ -398,6 +420,17 @@ int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA, const void *qB
     g.NB128 = (int)((N + 127) / 128);
     g.num_tiles = 0;
     fp8_gemm_kernel<true, false, false, 3><<<dev->num_sms, GEMM_THREADS, gemm_smem_bytes<true, 3>(), stream>>>(tmA, tmB, tmC, g);
+    return launch_status();
+}
+
+int fp8bs_selftest_wait_timeout(int64_t limit_us, cudaStream_t stream)
+{
+    if (limit_us < 1 || limit_us > 1000000)
+        return FP8BS_ERR_ARG;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    selftest_wait_kernel<<<1, 32, 0, stream>>>((uint64_t)limit_us * 1000u);
     return launch_status();
 }
 

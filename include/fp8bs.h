@@ -143,6 +143,21 @@ int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA,
  */
 int fp8bs_last_error(cudaStream_t stream);
 
+/*
+ * Self-test of the failure detection (no counterpart in the pages: it checks
+ * the library's own device-side time-out machinery).  Enqueues on `stream`
+ * one single-CTA kernel that waits, through the same bounded mbarrier wait
+ * that every pipeline of the library uses, on a barrier that nothing ever
+ * signals, with a limit of `limit_us` microseconds.  The wait runs out, the
+ * kernel records the time-out in the device error word and returns; the
+ * next fp8bs_last_error(stream) reports FP8BS_ERR_TIMEOUT and clears it, and
+ * the CUDA context stays usable.  No memory is read or written besides the
+ * error word.
+ * Returns FP8BS_OK (enqueued), FP8BS_ERR_ARG (limit_us outside
+ * [1, 1000000]), FP8BS_ERR_DEVICE or FP8BS_ERR_LAUNCH.
+ */
+int fp8bs_selftest_wait_timeout(int64_t limit_us, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
-        "fp8_grouped_gemm_blockscaled", "fp8bs_last_error"])
+        "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout"])
 
 
 def test_library_loads_and_exports_every_declared_symbol():
@@ -94,6 +94,13 @@ def test_gemm_rejects_bad_arguments():
     gg = lib.fp8_grouped_gemm_blockscaled
     assert gg(P(16), P(16), P(16), P(16), P(16), 0, 4, 4, 128, P(16), 0, 8, P(0)) == -4   # E < 1
     assert gg(P(16), P(16), P(16), P(16), P(0), 2, 4, 4, 128, P(16), 0, 8, P(0)) == -1    # offsets
+
+
+def test_selftest_rejects_out_of_range_limits():
+    lib = _raw()
+    assert lib.fp8bs_selftest_wait_timeout(0, P(0)) == -4
+    assert lib.fp8bs_selftest_wait_timeout(-5, P(0)) == -4
+    assert lib.fp8bs_selftest_wait_timeout(1000001, P(0)) == -4
 
 
 @pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="checks the no-GPU answer")
