@@ -61,6 +61,7 @@ constexpr int MAX_EXPERTS = 2048;
 constexpr int SCALE_SLOTS = 8;                           // slices of scales staged ahead
 constexpr int SCALE_SLOT_FLOATS = 132;                   // 128 row scales + 2 column-block scales (+pad)
 constexpr int SCALE_LOOKAHEAD = 2;                       // loader copy groups in flight
+constexpr int B_PREFETCH_SLICES = 2;                     // grouped: L2 prefetch distance of expert weights
 
 // Shared-memory layout for S pipeline stages of BSB bytes of B each
 // (offsets from a 1024-byte aligned base): operand stages, the output staging
@@ -407,6 +408,24 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             // weights are not needed again once its tiles are done.
             const uint64_t keep = ptx::policy_evict_last();
             const uint64_t stream = ptx::policy_evict_first();
+            // Grouped: the expert weights stream from HBM once, so the shared-
+            // memory ring alone keeps too few bytes in flight.  A cursor runs
+            // B_PREFETCH_SLICES slices ahead of the loads and prefetches each
+            // slice's weight box into L2, where the ring's TMA load finds it.
+            int64_t pf_t = t_first;
+            int pf_kb = 0;
+            Tile pf_tl{};
+            if constexpr (GROUPED) {
+                if (pf_t < ntiles)
+                    pf_tl = tile_at<GROUPED, PAIR>(g, ss, pf_t, rank);
+                for (int i = 0; i < B_PREFETCH_SLICES && pf_t < ntiles; ++i)
+                    if (++pf_kb == g.KB) {
+                        pf_kb = 0;
+                        pf_t += t_stride;
+                        if (pf_t < ntiles)
+                            pf_tl = tile_at<GROUPED, PAIR>(g, ss, pf_t, rank);
+                    }
+            }
             uint32_t it = 0;
             bool ok = true;
             for (int64_t t = t_first; ok && t < ntiles; t += t_stride) {
@@ -435,6 +454,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     ptx::tma_load_2d_hint(sa, &tmA, fb, kb * BK, (int32_t)tl.m0, keep);
                     if constexpr (GROUPED) {
                         ptx::tma_load_3d_hint(sb, &tmB, fb, kb * BK, tl.n0, tl.expert, stream);
+                        if (pf_t < ntiles) {
+                            ptx::tma_prefetch_3d(&tmB, pf_kb * BK, pf_tl.n0, pf_tl.expert);
+                            if (++pf_kb == g.KB) {
+                                pf_kb = 0;
+                                pf_t += t_stride;
+                                if (pf_t < ntiles)
+                                    pf_tl = tile_at<GROUPED, PAIR>(g, ss, pf_t, rank);
+                            }
+                        }
                     } else if constexpr (B_MN) {
                         ptx::tma_load_2d(sb, &tmB, fb, tl.n0, kb * BK);
                         ptx::tma_load_2d(sb + B_STAGE_BYTES / 2, &tmB, fb, tl.n0 + 128, kb * BK);
