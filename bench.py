@@ -417,17 +417,31 @@ def run_ours(args):
                "h2d_bytes_per_step": int(step.h2d_bytes), "d2h_bytes_per_step": int(step.d2h_bytes)}
 
     # ---- roofline of the dominant kernel (the GEMM) and the quantisers
+    # The GEMM is timed inside a long run of steps (power-capped clocks), so
+    # its tensor peak is the sustained one; the burst fraction is reported
+    # beside it.  The bound is whichever of the tensor and HBM times of the
+    # kernel's algorithmic work is longer (the expert GEMM streams weights).
     gemm_name = step.kernels[-1]
     gemm_ms = per_kernel[gemm_name]
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     fp8_peak_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP8_OVER_BF16
     achieved = step.flops / (gemm_ms * 1e-3) / 1e12
+    gemm_bytes = step.kernel_bytes[gemm_name]
+    achieved_gbs = gemm_bytes / (gemm_ms * 1e-3) / 1e9
     traffic = gemm_traffic(gemm_name, args.workload)
-    roofline = {"kernel": gemm_name, "bound": "tensor", "achieved": round(achieved, 1),
-                "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
-                "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 burst x {FP8_OVER_BF16} (nominal FP8:BF16)",
-                "frac_of_sustained": round(achieved / fp8_peak_sust, 4)}
+    hbm_bound = gemm_bytes / (peaks["hbm_gbs"] * 1e9) > step.flops / (fp8_peak_sust * 1e12)
+    if hbm_bound:
+        roofline = {"kernel": gemm_name, "bound": "hbm", "achieved": round(achieved_gbs, 1),
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
+                    "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs",
+                    "tensor_tflops": round(achieved, 1),
+                    "tensor_frac_of_sustained": round(achieved / fp8_peak_sust, 4)}
+    else:
+        roofline = {"kernel": gemm_name, "bound": "tensor", "achieved": round(achieved, 1),
+                    "peak": round(fp8_peak_sust, 1), "unit": "TFLOP/s",
+                    "frac": round(achieved / fp8_peak_sust, 4), "traffic": traffic,
+                    "peak_source": f"{peak_src} bf16 sustained x {FP8_OVER_BF16} (nominal FP8:BF16)",
+                    "frac_of_burst": round(achieved / fp8_peak, 4)}
     hbm = peaks["hbm_gbs"]
     kernels = {}
     for name in step.kernels:
@@ -436,7 +450,8 @@ def run_ours(args):
         entry = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
         if name in ("gemm", "grouped_gemm"):
             entry["TFLOP/s"] = round(achieved, 1)
-            entry["frac_fp8_peak"] = round(achieved / fp8_peak, 4)
+            entry["frac_fp8_sustained"] = round(achieved / fp8_peak_sust, 4)
+            entry["frac_fp8_burst"] = round(achieved / fp8_peak, 4)
         kernels[name] = entry
 
     # ---- CPU baseline (oracle) on a bounded sample, rank 0 at N=1 only
