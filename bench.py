@@ -159,11 +159,15 @@ class DenseStep:
     stream forked from the step's stream, concurrently with the weight's, and
     the GEMM waits for both."""
 
-    def __init__(self, case, fp8, torch):
+    def __init__(self, case, fp8, torch, e4m3_out=None):
         self.fp8, self.torch, self.case = fp8, torch, case
         M, K, N = case.M, case.K, case.N
         self.M, self.N, self.K, self.b_major = M, N, K, case.b_major
         self.out_dtype = torch.float32 if case.out_fp32 else torch.bfloat16
+        # e4m3_out "fused": the GEMM writes C quantised per 1x128 row tile
+        # (codes + scales) instead of BF16; "unfused": the same result from the
+        # BF16 GEMM followed by the activation quantiser on C
+        self.e4m3_out = e4m3_out
         in_bytes = (case.a.numel() + case.w.numel()) * 2
         self.nsets = max(1, min(8, -(-2 * L2_BYTES // in_bytes) + 1))
         self.sets = [(case.a, case.w)] + [(case.a.clone(), case.w.clone())
@@ -174,20 +178,32 @@ class DenseStep:
         self.qb = torch.empty(tuple(case.w.shape), dtype=torch.uint8, device=dev)
         R, C = case.w.shape
         self.sb = torch.empty(((R + 127) // 128, C // 128), dtype=torch.float32, device=dev)
-        self.c = torch.empty((M, N), dtype=self.out_dtype, device=dev)
+        if e4m3_out:
+            self.c = torch.empty((M, N), dtype=torch.uint8, device=dev)
+            self.sc = torch.empty((N // 128, M), dtype=torch.float32, device=dev)
+            out_bytes = M * N + self.sc.numel() * 4
+            if e4m3_out == "unfused":
+                self.c16 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        else:
+            self.c = torch.empty((M, N), dtype=self.out_dtype, device=dev)
+            self.sc = None
+            out_bytes = M * N * self.c.element_size()
         self.flops = 2.0 * M * N * K
         self.kernels = ["quant_act", "quant_w", "gemm"]
         self.kernel_bytes = {
             "quant_act": M * K * 3 + (K // 128) * M * 4,
             "quant_w": R * C * 3 + self.sb.numel() * 4,
-            "gemm": M * K + R * C + (self.sa.numel() + self.sb.numel()) * 4 +
-                    M * N * self.c.element_size(),
+            "gemm": M * K + R * C + (self.sa.numel() + self.sb.numel()) * 4 + out_bytes,
         }
+        if e4m3_out == "unfused":
+            self.kernels.append("quant_out")
+            self.kernel_bytes["gemm"] += M * N * 2 - out_bytes
+            self.kernel_bytes["quant_out"] = M * N * 3 + self.sc.numel() * 4
         self.h2d_bytes = in_bytes
-        self.d2h_bytes = M * N * self.c.element_size()
-        self.launches_per_step = 3
+        self.d2h_bytes = out_bytes
+        self.launches_per_step = len(self.kernels)
         self.side = torch.cuda.Stream(device=dev)
-        self.schedule = "quant_act || quant_w -> gemm"
+        self.schedule = "quant_act || quant_w -> gemm" + (" -> quant_out" if e4m3_out == "unfused" else "")
 
     def run(self, i, events=None):
         """events: (start, end) per kernel in `kernels` order, or None."""
@@ -204,9 +220,23 @@ class DenseStep:
         if events: events[3].record(main)
         main.wait_stream(self.side)
         if events: events[4].record(main)
-        f.fp8_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major,
-                               C=self.c)
+        self._gemm()
         if events: events[5].record(main)
+        if self.e4m3_out == "unfused":
+            if events: events[6].record(main)
+            f.fp8_quant_act_1x128(self.c16, self.c, self.sc)
+            if events: events[7].record(main)
+
+    def _gemm(self):
+        if self.e4m3_out == "unfused":
+            self.fp8.fp8_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major,
+                                          C=self.c16)
+        elif self.e4m3_out:
+            self.fp8.fp8_gemm_blockscaled_e4m3_out(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major,
+                                                   qC=self.c, sC=self.sc)
+        else:
+            self.fp8.fp8_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major,
+                                          C=self.c)
 
     def run_host(self, host_a, host_w, host_c, dev_a, dev_w):
         """End-to-end step from pinned host buffers through the C-ABI calls:
@@ -221,9 +251,12 @@ class DenseStep:
         dev_w.copy_(host_w, non_blocking=True)
         f.fp8_quant_w_128x128(dev_w, self.qb, self.sb)
         main.wait_stream(self.side)
-        f.fp8_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major,
-                               C=self.c)
+        self._gemm()
+        if self.e4m3_out == "unfused":
+            f.fp8_quant_act_1x128(self.c16, self.c, self.sc)
         host_c.copy_(self.c, non_blocking=True)
+        if self.sc is not None:
+            self.host_sc.copy_(self.sc, non_blocking=True)
 
 
 class ExpertsStep:
@@ -335,7 +368,10 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
 
     case = make_workload(args.workload, device)
-    step = ExpertsStep(case, fp8, torch) if args.workload == "experts" else DenseStep(case, fp8, torch)
+    if args.e4m3_out and args.workload == "experts":
+        raise SystemExit("--e4m3-out applies to the dense workloads")
+    step = ExpertsStep(case, fp8, torch) if args.workload == "experts" else \
+        DenseStep(case, fp8, torch, e4m3_out=args.e4m3_out)
     stream = torch.cuda.current_stream()
 
     for i in range(args.warmup):
@@ -399,6 +435,8 @@ def run_ours(args):
             host_w = case.w.cpu().pin_memory()
             dev_a, dev_w = torch.empty_like(case.a), torch.empty_like(case.w)
         host_c = torch.empty(tuple(step.c.shape), dtype=step.c.dtype).pin_memory()
+        if getattr(step, "sc", None) is not None:
+            step.host_sc = torch.empty(tuple(step.sc.shape), dtype=step.sc.dtype).pin_memory()
         for _ in range(2):
             step.run_host(host_a, host_w, host_c, dev_a, dev_w)
         torch.cuda.synchronize()
@@ -421,14 +459,15 @@ def run_ours(args):
     # its tensor peak is the sustained one; the burst fraction is reported
     # beside it.  The bound is whichever of the tensor and HBM times of the
     # kernel's algorithmic work is longer (the expert GEMM streams weights).
-    gemm_name = step.kernels[-1]
+    gemm_name = "grouped_gemm" if "grouped_gemm" in step.kernels else "gemm"
     gemm_ms = per_kernel[gemm_name]
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     fp8_peak_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP8_OVER_BF16
     achieved = step.flops / (gemm_ms * 1e-3) / 1e12
     gemm_bytes = step.kernel_bytes[gemm_name]
     achieved_gbs = gemm_bytes / (gemm_ms * 1e-3) / 1e9
-    traffic = gemm_traffic(gemm_name, args.workload)
+    traffic = gemm_traffic(gemm_name + ("_e4m3" if getattr(step, "e4m3_out", None) == "fused" else ""),
+                           args.workload)
     hbm_bound = gemm_bytes / (peaks["hbm_gbs"] * 1e9) > step.flops / (fp8_peak_sust * 1e12)
     if hbm_bound:
         roofline = {"kernel": gemm_name, "bound": "hbm", "achieved": round(achieved_gbs, 1),
@@ -470,7 +509,9 @@ def run_ours(args):
             "config": {"workload": case.name if hasattr(case, "name") else args.workload,
                        "M": step.M, "N": step.N, "K": step.K,
                        "step": step.schedule,
-                       "out": "bf16" if step.c.dtype == torch.bfloat16 else "fp32",
+                       "out": (f"e4m3 + fp32 scale per 1x128 row tile ({step.e4m3_out})"
+                               if getattr(step, "e4m3_out", None)
+                               else "bf16" if step.c.dtype == torch.bfloat16 else "fp32"),
                        "l2": (f"inputs rotate over {step.nsets} sets (> 2x the 126 MB L2)"
                               if step.nsets > 1 else "inputs larger than L2"),
                        "parallelism": f"replicas x{world}",
@@ -546,6 +587,10 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end run")
+    ap.add_argument("--e4m3-out", choices=["fused", "unfused"], default=None,
+                    help="dense workloads: the step's output is C quantised per 1x128 row tile (E4M3 codes "
+                         "+ scales), by the GEMM's epilogue (fused) or by the activation quantiser on the "
+                         "BF16 C (unfused)")
     ap.add_argument("--eager", action="store_true",
                     help="launch the timed steps one by one instead of replaying a CUDA graph")
     args = ap.parse_args(argv)

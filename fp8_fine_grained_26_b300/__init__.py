@@ -34,7 +34,8 @@ _STATUS_NAMES = {
 }
 
 EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
-            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout")
+            "fp8_gemm_blockscaled_e4m3_out", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
+            "fp8bs_selftest_wait_timeout")
 
 
 class Fp8bsError(RuntimeError):
@@ -53,6 +54,7 @@ def _load():
         "fp8_quant_act_1x128": [p, i64, i64, i64, p, i64, p, p],
         "fp8_quant_w_128x128": [p, i64, i64, i64, p, i64, p, p],
         "fp8_gemm_blockscaled": [p, p, p, p, i64, i64, i64, i32, p, i32, i64, p],
+        "fp8_gemm_blockscaled_e4m3_out": [p, p, p, p, i64, i64, i64, i32, p, i64, p, p],
         "fp8_grouped_gemm_blockscaled": [p, p, p, p, p, i32, i64, i64, i64, p, i32, i64, p],
         "fp8bs_last_error": [p],
         "fp8bs_selftest_wait_timeout": [i64, p],
@@ -174,6 +176,40 @@ def fp8_gemm_blockscaled(qA, sA, qB, sB, b_major=B_KMAJOR, out_dtype=torch.bfloa
     return C
 
 
+def fp8_gemm_blockscaled_e4m3_out(qA, sA, qB, sB, b_major=B_KMAJOR, qC=None, sC=None, stream=None):
+    """``C = A . B^T`` as :func:`fp8_gemm_blockscaled`, returned quantised per
+    1x128 row tile: ``qC uint8 [M, N]`` (E4M3 codes) and ``sC float32
+    [N/128, M]``.  N must be a multiple of 128."""
+    _need(qA, torch.uint8, "qA", 2)
+    _need(qB, torch.uint8, "qB", 2)
+    _need(sA, torch.float32, "sA", 2)
+    _need(sB, torch.float32, "sB", 2)
+    for t, n in ((qA, "qA"), (qB, "qB"), (sA, "sA"), (sB, "sB")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    M, K = qA.shape
+    if b_major == B_KMAJOR:
+        N, Kb = qB.shape
+    else:
+        Kb, N = qB.shape
+    if Kb != K:
+        raise ValueError("qA and qB disagree on K")
+    if qC is None:
+        qC = torch.empty((M, N), dtype=torch.uint8, device=qA.device)
+    if sC is None:
+        sC = torch.empty((N // 128, M), dtype=torch.float32, device=qA.device)
+    _need(qC, torch.uint8, "qC", 2)
+    _need(sC, torch.float32, "sC", 2)
+    if tuple(qC.shape) != (M, N) or tuple(sC.shape) != (N // 128, M) or not sC.is_contiguous():
+        raise ValueError("qC must be [M, N] and sC a contiguous [N/128, M]")
+    _row_major(qC, "qC")
+    ldq = qC.stride(0) if M > 0 else N
+    _check(lib.fp8_gemm_blockscaled_e4m3_out(_ptr(qA), _ptr(sA), _ptr(qB), _ptr(sB), M, N, K, b_major,
+                                             _ptr(qC), ldq, _ptr(sC), _stream(stream)),
+           "fp8_gemm_blockscaled_e4m3_out")
+    return qC, sC
+
+
 def fp8_grouped_gemm_blockscaled(qA, sA, qB, sB, seg_offsets, out_dtype=torch.bfloat16, C=None,
                                  stream=None):
     """Per-expert ``C[rows of e] = A[rows of e] . B_e^T`` with ``qB [E, N, K]``,
@@ -210,6 +246,7 @@ def fp8bs_selftest_wait_timeout(limit_us=20000, stream=None):
 
 
 __all__ = ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
+           "fp8_gemm_blockscaled_e4m3_out",
            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout",
            "Fp8bsError", "lib",
            "LIB_PATH", "EXPORTED", "B_KMAJOR", "B_MNMAJOR", "OUT_BF16", "OUT_FP32"]

@@ -69,6 +69,16 @@ int current_device(DeviceInfo **info)
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem) != cudaSuccess ||
             cudaFuncSetAttribute(fp8_gemm_kernel<false, true, true, PAIR_STAGES>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, false, false, 3, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 gemm_smem_bytes<false, 3>()) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, true, false, 3, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 gemm_smem_bytes<false, 3>()) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, false, true, PAIR_STAGES, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, true, true, PAIR_STAGES, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem) != cudaSuccess ||
             cudaFuncSetAttribute(fp8_gemm_kernel<true, false, false, 3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  gemm_smem_bytes<true, 3>()) != cudaSuccess ||
@@ -207,6 +217,99 @@ int check_gemm_common(const void *qA, const float *sA, const void *qB, const flo
     return FP8BS_OK;
 }
 
+// Dense GEMM launch after argument checks (K > 0, M > 0, N > 0).  sC != null
+// selects the E4M3-output epilogue (C is then the code matrix, ldc its row
+// stride in bytes).
+int launch_dense(DeviceInfo *dev, const void *qA, const float *sA, const void *qB, const float *sB,
+                 int64_t M, int64_t N, int64_t K, int b_major, void *C, int c_dtype, int64_t ldc,
+                 float *sC, cudaStream_t stream)
+{
+    const bool qout = sC != nullptr;
+    CUtensorMap tmA, tmB;
+    if (!encode_2d_u8(&tmA, qA, (uint64_t)K, (uint64_t)M, (uint64_t)K, BK, BM))
+        return FP8BS_ERR_ARG;
+    bool ok;
+    // Dense GEMMs of two or more M-blocks run on CTA pairs (256 x 256 tiles,
+    // each CTA holding its 128 rows of A and half of the B block).
+#ifndef FP8BS_NO_PAIR
+    const bool pair = dev->max_pairs > 0 && M > BM;
+#else
+    const bool pair = false;
+#endif
+    if (b_major == FP8BS_B_KMAJOR)
+        ok = encode_2d_u8(&tmB, qB, (uint64_t)K, (uint64_t)N, (uint64_t)K, BK, pair ? 128 : BN);
+    else
+        ok = encode_2d_u8(&tmB, qB, (uint64_t)N, (uint64_t)K, (uint64_t)N, 128, BK);
+    if (!ok)
+        return FP8BS_ERR_ARG;
+
+    GemmArgs g{};
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.ldc = ldc;
+    g.sA = sA;
+    g.sB = sB;
+    g.C = C;
+    g.sC = sC;
+    g.offsets = nullptr;
+    g.E = 1;
+    g.c_fp32 = c_dtype == FP8BS_OUT_FP32;
+    CUtensorMap tmC = tmA;                        // unused unless a TMA epilogue runs
+    if (qout) {
+        // [M][N] codes, 128 x 128-byte boxes: one per warpgroup and tile
+        if (!encode_2d_u8(&tmC, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc, 128, BM))
+            return FP8BS_ERR_ARG;
+        g.c_tma = 1;
+    } else {
+        g.c_tma = !g.c_fp32 && c_vector_ok(C, c_dtype, ldc) &&
+                  encode_c_bf16(&tmC, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc);
+    }
+    g.num_m_blk = (int)((M + BM - 1) / BM);
+    g.num_n_blk = (int)((N + BN - 1) / BN);
+    g.KB = (int)(K / BK);
+    g.NB128 = (int)((N + 127) / 128);
+    g.num_m_pair = (g.num_m_blk + 1) / 2;
+    if (pair) {
+        g.num_tiles = (int64_t)g.num_m_pair * g.num_n_blk;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(g.num_tiles, dev->max_pairs)));
+        cfg.blockDim = dim3(GEMM_THREADS);
+        cfg.dynamicSmemBytes = gemm_smem_bytes<false, PAIR_STAGES, B_STAGE_BYTES / 2>();
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e;
+        if (b_major == FP8BS_B_KMAJOR)
+            e = qout ? cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES, true>, tmA, tmB, tmC, g)
+                     : cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES>, tmA, tmB, tmC, g);
+        else
+            e = qout ? cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, true, true, PAIR_STAGES, true>, tmA, tmB, tmC, g)
+                     : cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, true, true, PAIR_STAGES>, tmA, tmB, tmC, g);
+        return e == cudaSuccess ? launch_status() : (cudaGetLastError(), FP8BS_ERR_LAUNCH);
+    }
+    g.num_tiles = (int64_t)g.num_m_blk * g.num_n_blk;
+    const int grid = (int)std::min<int64_t>(g.num_tiles, dev->num_sms);
+    const int smem = gemm_smem_bytes<false, 3>();
+    if (b_major == FP8BS_B_KMAJOR) {
+        if (qout)
+            fp8_gemm_kernel<false, false, false, 3, true><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmC, g);
+        else
+            fp8_gemm_kernel<false, false, false, 3><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmC, g);
+    } else {
+        if (qout)
+            fp8_gemm_kernel<false, true, false, 3, true><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmC, g);
+        else
+            fp8_gemm_kernel<false, true, false, 3><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmC, g);
+    }
+    return launch_status();
+}
+
 } // namespace
 
 namespace fp8bs {
@@ -305,72 +408,39 @@ int fp8_gemm_blockscaled(const void *qA, const float *sA, const void *qB, const 
         return st;
     if (K == 0)
         return zero_output(C, c_dtype, ldc, M, N, stream);
+    return launch_dense(dev, qA, sA, qB, sB, M, N, K, b_major, C, c_dtype, ldc, nullptr, stream);
+}
 
-    CUtensorMap tmA, tmB;
-    if (!encode_2d_u8(&tmA, qA, (uint64_t)K, (uint64_t)M, (uint64_t)K, BK, BM))
+int fp8_gemm_blockscaled_e4m3_out(const void *qA, const float *sA, const void *qB, const float *sB,
+                                  int64_t M, int64_t N, int64_t K, int b_major, void *qC, int64_t ldqc,
+                                  float *sC, cudaStream_t stream)
+{
+    if (b_major != FP8BS_B_KMAJOR && b_major != FP8BS_B_MNMAJOR)
         return FP8BS_ERR_ARG;
-    bool ok;
-    // Dense GEMMs of two or more M-blocks run on CTA pairs (256 x 256 tiles,
-    // each CTA holding its 128 rows of A and half of the B block).
-#ifndef FP8BS_NO_PAIR
-    const bool pair = dev->max_pairs > 0 && M > BM;
-#else
-    const bool pair = false;
-#endif
-    if (b_major == FP8BS_B_KMAJOR)
-        ok = encode_2d_u8(&tmB, qB, (uint64_t)K, (uint64_t)N, (uint64_t)K, BK, pair ? 128 : BN);
-    else
-        ok = encode_2d_u8(&tmB, qB, (uint64_t)N, (uint64_t)K, (uint64_t)N, 128, BK);
-    if (!ok)
-        return FP8BS_ERR_ARG;
-
-    GemmArgs g{};
-    g.M = M;
-    g.N = N;
-    g.K = K;
-    g.ldc = ldc;
-    g.sA = sA;
-    g.sB = sB;
-    g.C = C;
-    g.offsets = nullptr;
-    g.E = 1;
-    g.c_fp32 = c_dtype == FP8BS_OUT_FP32;
-    CUtensorMap tmC = tmA;                        // unused unless the BF16 TMA epilogue runs
-    g.c_tma = !g.c_fp32 && c_vector_ok(C, c_dtype, ldc) &&
-              encode_c_bf16(&tmC, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc);
-    g.num_m_blk = (int)((M + BM - 1) / BM);
-    g.num_n_blk = (int)((N + BN - 1) / BN);
-    g.KB = (int)(K / BK);
-    g.NB128 = (int)((N + 127) / 128);
-    g.num_m_pair = (g.num_m_blk + 1) / 2;
-    if (pair) {
-        g.num_tiles = (int64_t)g.num_m_pair * g.num_n_blk;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(g.num_tiles, dev->max_pairs)));
-        cfg.blockDim = dim3(GEMM_THREADS);
-        cfg.dynamicSmemBytes = gemm_smem_bytes<false, PAIR_STAGES, B_STAGE_BYTES / 2>();
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        cudaError_t e;
-        if (b_major == FP8BS_B_KMAJOR)
-            e = cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES>, tmA, tmB, tmC, g);
-        else
-            e = cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, true, true, PAIR_STAGES>, tmA, tmB, tmC, g);
-        return e == cudaSuccess ? launch_status() : (cudaGetLastError(), FP8BS_ERR_LAUNCH);
+    if (M < 0 || N < 0 || K < 0 || K % 128 != 0 || N % 128 != 0)
+        return FP8BS_ERR_SHAPE;
+    if (M == 0 || N == 0)
+        return FP8BS_OK;
+    if (!qC || !sC || (K > 0 && (!qA || !sA || !qB || !sB)))
+        return FP8BS_ERR_NULL;
+    if (ldqc < N)
+        return FP8BS_ERR_SHAPE;
+    if (!aligned16(qC) || ldqc % 16 != 0 || !aligned4(sC) ||
+        (K > 0 && (!aligned16(qA) || !aligned16(qB) || !aligned4(sA) || !aligned4(sB))))
+        return FP8BS_ERR_ALIGN;
+    if (M > INT32_MAX || N > INT32_MAX - 2 * BN || K > INT32_MAX)
+        return FP8BS_ERR_SHAPE;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    if (K == 0) {
+        // C == 0: every tile is all zero, so its codes are +0 and its scale 0
+        if (cudaMemset2DAsync(qC, (size_t)ldqc, 0, (size_t)N, (size_t)M, stream) != cudaSuccess ||
+            cudaMemsetAsync(sC, 0, (size_t)(N / 128) * (size_t)M * sizeof(float), stream) != cudaSuccess)
+            return FP8BS_ERR_LAUNCH;
+        return FP8BS_OK;
     }
-    g.num_tiles = (int64_t)g.num_m_blk * g.num_n_blk;
-    const int grid = (int)std::min<int64_t>(g.num_tiles, dev->num_sms);
-    if (b_major == FP8BS_B_KMAJOR)
-        fp8_gemm_kernel<false, false, false, 3><<<grid, GEMM_THREADS, gemm_smem_bytes<false, 3>(), stream>>>(tmA, tmB, tmC, g);
-    else
-        fp8_gemm_kernel<false, true, false, 3><<<grid, GEMM_THREADS, gemm_smem_bytes<false, 3>(), stream>>>(tmA, tmB, tmC, g);
-    return launch_status();
+    return launch_dense(dev, qA, sA, qB, sB, M, N, K, b_major, qC, FP8BS_OUT_BF16, ldqc, sC, stream);
 }
 
 int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA, const void *qB,

@@ -46,6 +46,7 @@
 // frees TMEM and returns.
 #pragma once
 #include "common.cuh"
+#include "quant.cuh"            // the E4M3 encoder shared with the E4M3-output epilogue
 
 namespace fp8bs {
 
@@ -98,6 +99,7 @@ struct GemmArgs {
     int E;
     int c_fp32;
     int c_tma;          // BF16 output through the C tensor map
+    float *sC;          // E4M3 output: [N/128][M] scales of the 1x128 output tiles
     int num_m_blk;      // dense: ceil(M/128)
     int num_m_pair;     // dense, cluster pairs: ceil(num_m_blk / 2)
     int num_n_blk;      // ceil(N/256)
@@ -327,7 +329,11 @@ __device__ __forceinline__ void store_row_direct(const GemmArgs &g, const float2
     }
 }
 
-template <bool GROUPED, bool B_MN, bool PAIR, int STAGES>
+// QOUT: the epilogue writes C as E4M3 codes with one FP32 scale per 1x128
+// row tile (the activation quantiser's rule applied to the BF16-rounded
+// output, bit for bit) instead of BF16.  Dense only; N % 128 == 0 and a
+// TMA-able code matrix are guaranteed by the host.
+template <bool GROUPED, bool B_MN, bool PAIR, int STAGES, bool QOUT = false>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs g)
@@ -643,16 +649,41 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     ptx::bulk_wait_read_all();              // the previous tile's stores read the boxes
                     ptx::mbar_arrive(ss.epi_free(wg));
                 }
-                if (!wait_bounded(ss, ss.epi_free(wg), ph)) { ok = false; break; }
+                if constexpr (QOUT) {
+                    // The thread's 128 columns are exactly one 1x128 tile of
+                    // its row: round to BF16, take the amax of the magnitude
+                    // bits, form the divisor and encode, as the quantiser does.
+                    uint32_t w[64];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t buf = ss.epi_box(wg, h) + (uint32_t)row * 128;
+                    for (int j = 0; j < 64; ++j)
+                        w[j] = ptx::cvt_bf16x2(acc2[j].x, acc2[j].y);
+                    uint32_t mx = 0;
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        mx = ptx::max_u16x2(mx, w[j] & 0x7FFF7FFFu);
+                    const Divisor d = make_divisor(max(mx & 0xFFFFu, mx >> 16));
+                    if (row_ok)
+                        g.sC[(n_first >> 7) * g.M + gm] = d.s;
+                    if (!wait_bounded(ss, ss.epi_free(wg), ph)) { ok = false; break; }
+                    const uint32_t buf = ss.epi_box(wg, 0) + (uint32_t)row * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const float2 *v = acc2 + h * 32 + c * 4;
-                        ptx::st_shared_v4(buf + ((c ^ (lane & 7)) << 4),
-                                          ptx::cvt_bf16x2(v[0].x, v[0].y), ptx::cvt_bf16x2(v[1].x, v[1].y),
-                                          ptx::cvt_bf16x2(v[2].x, v[2].y), ptx::cvt_bf16x2(v[3].x, v[3].y));
+                        const uint2 lo = quant_8(make_uint4(w[8 * c], w[8 * c + 1], w[8 * c + 2], w[8 * c + 3]), d);
+                        const uint2 hi = quant_8(make_uint4(w[8 * c + 4], w[8 * c + 5], w[8 * c + 6], w[8 * c + 7]), d);
+                        ptx::st_shared_v4(buf + ((c ^ (lane & 7)) << 4), lo.x, lo.y, hi.x, hi.y);
+                    }
+                } else {
+                    if (!wait_bounded(ss, ss.epi_free(wg), ph)) { ok = false; break; }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t buf = ss.epi_box(wg, h) + (uint32_t)row * 128;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const float2 *v = acc2 + h * 32 + c * 4;
+                            ptx::st_shared_v4(buf + ((c ^ (lane & 7)) << 4),
+                                              ptx::cvt_bf16x2(v[0].x, v[0].y), ptx::cvt_bf16x2(v[1].x, v[1].y),
+                                              ptx::cvt_bf16x2(v[2].x, v[2].y), ptx::cvt_bf16x2(v[3].x, v[3].y));
+                        }
                     }
                 }
                 ptx::fence_proxy_async_smem();
@@ -661,7 +692,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 if (issuer) {
                     if (!wait_bounded(ss, ss.epi_full(wg), ph)) { ok = false; break; }
                     ptx::tma_store_2d_hint(&tmC, ss.epi_box(wg, 0), (int32_t)n_first, (int32_t)tl.m0, c_policy);
-                    if (n_first + 64 < g.N)                // second 64-column box exists
+                    if (!QOUT && n_first + 64 < g.N)       // second 64-column BF16 box exists
                         ptx::tma_store_2d_hint(&tmC, ss.epi_box(wg, 1), (int32_t)(n_first + 64), (int32_t)tl.m0,
                                                c_policy);
                     ptx::bulk_commit();

@@ -115,6 +115,30 @@ int fp8_gemm_blockscaled(const void *qA, const float *sA, const void *qB, const 
                          void *C, int c_dtype, int64_t ldc, cudaStream_t stream);
 
 /*
+ * Block-scaled GEMM with a quantised output: the same C = A . B^T (same
+ * arguments, same arithmetic, same BF16 rounding of each output element), but
+ * the epilogue quantises every 1x128 tile of each output row with the
+ * activation rule of fp8_quant_act_1x128 -- amax over the tile's BF16 values,
+ * scale = fp32(amax / 448), code = E4M3_RNE_sat(fp32(c / scale)) -- and
+ * writes codes and scales instead of BF16.  The pages store activations and
+ * pass them between devices in low-precision formats ("DeepSeek-V3 training
+ * walkthrough", section 二(四), last item; qqstock.cn walkthrough, FP8
+ * section, low-precision storage and communication, report figure 10); this
+ * call produces that FP8 form without a BF16 round trip through HBM.  The
+ * result is bit-identical to
+ * fp8_gemm_blockscaled (BF16 out) followed by fp8_quant_act_1x128.
+ *   qC : [M][N] E4M3 codes, row stride ldqc BYTES (>= N, multiple of 16;
+ *        base 16-byte aligned).
+ *   sC : [N/128][M] FP32: sC[nb*M + m] is the scale of row m, columns
+ *        [128*nb, 128*nb + 128) -- the layout fp8_quant_act_1x128 gives sA.
+ * N must be a multiple of 128 (else FP8BS_ERR_SHAPE).  K == 0 writes zero
+ * codes and zero scales.  Other rules and errors as fp8_gemm_blockscaled.
+ */
+int fp8_gemm_blockscaled_e4m3_out(const void *qA, const float *sA, const void *qB, const float *sB,
+                                  int64_t M, int64_t N, int64_t K, int b_major, void *qC, int64_t ldqc,
+                                  float *sC, cudaStream_t stream);
+
+/*
  * Grouped block-scaled FP8 GEMM for routed experts (one expert per segment of
  * rows).  Rows [seg_offsets[e], seg_offsets[e+1]) of qA belong to expert e:
  *   C[m][n] = sum_kb sA[kb][m] * sB[e][n/128][kb] * sum_{k in kb} qA[m][k] * qB[e][n][k]

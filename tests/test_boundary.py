@@ -21,7 +21,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
-        "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout"])
+        "fp8_gemm_blockscaled_e4m3_out", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
+        "fp8bs_selftest_wait_timeout"])
 
 
 def test_library_loads_and_exports_every_declared_symbol():
@@ -94,6 +95,20 @@ def test_gemm_rejects_bad_arguments():
     gg = lib.fp8_grouped_gemm_blockscaled
     assert gg(P(16), P(16), P(16), P(16), P(16), 0, 4, 4, 128, P(16), 0, 8, P(0)) == -4   # E < 1
     assert gg(P(16), P(16), P(16), P(16), P(0), 2, 4, 4, 128, P(16), 0, 8, P(0)) == -1    # offsets
+
+
+def test_e4m3_out_gemm_rejects_bad_arguments():
+    lib = _raw()
+    g = lib.fp8_gemm_blockscaled_e4m3_out
+    assert g(P(16), P(16), P(16), P(16), 4, 200, 128, 0, P(16), 208, P(16), P(0)) == -2   # N % 128
+    assert g(P(16), P(16), P(16), P(16), 4, 256, 100, 0, P(16), 256, P(16), P(0)) == -2   # K % 128
+    assert g(P(16), P(16), P(16), P(16), 4, 256, 128, 3, P(16), 256, P(16), P(0)) == -4   # b_major
+    assert g(P(16), P(16), P(16), P(16), 0, 256, 128, 0, P(0), 256, P(0), P(0)) == 0      # M == 0
+    assert g(P(16), P(16), P(16), P(16), 4, 256, 128, 0, P(0), 256, P(16), P(0)) == -1   # NULL qC
+    assert g(P(16), P(16), P(16), P(16), 4, 256, 128, 0, P(16), 256, P(0), P(0)) == -1   # NULL sC
+    assert g(P(16), P(16), P(16), P(16), 4, 256, 128, 0, P(16), 128, P(16), P(0)) == -2  # ldqc < N
+    assert g(P(16), P(16), P(16), P(16), 4, 256, 128, 0, P(16), 264, P(16), P(0)) == -3  # ldqc % 16
+    assert g(P(16), P(16), P(16), P(16), 4, 256, 128, 0, P(8), 256, P(16), P(0)) == -3   # qC align
 
 
 def test_selftest_rejects_out_of_range_limits():
