@@ -41,12 +41,13 @@ def _load():
                                            p, p, i64, p]
         lib.oracle_grouped_gemm_f64.argtypes = [p, p, i64, p, p, p, ctypes.c_int, i64, i64, i64,
                                                 p, i64]
+        lib.oracle_gemm_f64_tokens.argtypes = [p, p, i64, p, p, i64, i64, i64, i64, p, i64]
         lib.oracle_act_row_norms.argtypes = [p, p, i64, i64, i64, p]
         lib.oracle_act_row_norms.restype = None
         lib.oracle_b_row_norms.argtypes = [p, p, i64, ctypes.c_int, i64, i64, p]
         lib.oracle_b_row_norms.restype = None
         for f in ("oracle_quant_act_1x128", "oracle_quant_w_128x128", "oracle_gemm_f64",
-                  "oracle_gemm_f64_at", "oracle_grouped_gemm_f64"):
+                  "oracle_gemm_f64_at", "oracle_grouped_gemm_f64", "oracle_gemm_f64_tokens"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -102,6 +103,18 @@ def quant_act_1x128(x_bf16_bits):
     s = np.empty((K // 128, M), np.float32)
     _check(_load().oracle_quant_act_1x128(_ptr(x), M, K, K, _ptr(q), K, _ptr(s)), "quant_act")
     return q, s
+
+
+def quant_tokens_1x128(x_bf16_bits):
+    """1x128 tiles along the token (row) dimension of a bf16 ``[T, F]`` matrix:
+    each feature column is cut into runs of 128 tokens, each with its own scale
+    -- the operands of the weight-gradient GEMM, whose contraction runs over
+    tokens.  By definition this is the 1x128 row quantisation of the
+    transposed matrix.
+
+    Returns ``(q uint8 [F, T], s float32 [T/128, F])``."""
+    x = _as_c(x_bf16_bits, np.uint16)
+    return quant_act_1x128(np.ascontiguousarray(x.T))
 
 
 def quant_w_128x128(w_bf16_bits):
@@ -170,6 +183,22 @@ def grouped_gemm_f64(qA, sA, qB, sB, offsets) -> np.ndarray:
     C = np.zeros((M, N), np.float64)
     _check(_load().oracle_grouped_gemm_f64(_ptr(qA), _ptr(sA), K, _ptr(qB), _ptr(sB), _ptr(off),
                                            E, M, N, K, _ptr(C), N), "grouped_gemm")
+    return C
+
+
+def gemm_f64_tokens(qA, sA, qB, sB) -> np.ndarray:
+    """float64 ``C = A^ . B^T`` where both operands carry 1x128 scales along K:
+    ``qA [M, K]`` with ``sA [K/128, M]`` and ``qB [N, K]`` with ``sB [K/128, N]``
+    (the weight-gradient GEMM dW = dY^T . X over tokens)."""
+    qA, sA = _as_c(qA, np.uint8), _as_c(sA, np.float32)
+    qB, sB = _as_c(qB, np.uint8), _as_c(sB, np.float32)
+    M, K = qA.shape
+    N, Kb = qB.shape
+    if Kb != K or sA.shape != (K // 128, M) or sB.shape != (K // 128, N):
+        raise ValueError("shape mismatch")
+    C = np.empty((M, N), np.float64)
+    _check(_load().oracle_gemm_f64_tokens(_ptr(qA), _ptr(sA), K, _ptr(qB), _ptr(sB), K, M, N, K,
+                                          _ptr(C), N), "gemm_tokens")
     return C
 
 

@@ -280,6 +280,30 @@ int oracle_grouped_gemm_f64(const uint8_t *qA, const float *sA, int64_t lda,
     return 0;
 }
 
+/* Weight-gradient GEMM, both operands quantised per 1x128 tile along the
+ * contraction dimension (the token dimension of dW = dY^T . X): A is [M][K]
+ * with sA [K/128][M] and B is [N][K] with sB [K/128][N] -- each B row carries
+ * its own scale per 128-wide K-slice, exactly like an activation row.
+ *   C[m][n] = sum_k A^[m][k] * B^[n][k]  (float64 over dequantised operands)
+ * ["DeepSeek-V3 Technical Report digest", section 3, "FP8 operations" bullet:
+ *  forward, data-gradient and weight-gradient GEMMs all run in FP8;
+ *  fine-grained 1x128 tiles for activation-like operands.] */
+int oracle_gemm_f64_tokens(const uint8_t *qA, const float *sA, int64_t lda,
+                           const uint8_t *qB, const float *sB, int64_t ldb,
+                           int64_t M, int64_t N, int64_t K, double *C, int64_t ldc)
+{
+    if (K % 128 != 0)
+        return -2;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += deq_a(qA, sA, M, lda, m, k) * deq_a(qB, sB, N, ldb, n, k);
+            C[m * ldc + n] = acc;
+        }
+    return 0;
+}
+
 /* Euclidean norms of the dequantised rows, used to normalise the GEMM error:
  * act: ||A^[m,:]||_2 for each m;  b: ||B^[n,:]||_2 for each n (B^ as above). */
 void oracle_act_row_norms(const uint8_t *qA, const float *sA, int64_t lda,

@@ -434,3 +434,87 @@ def test_row_norms_match_numpy():
 def test_oracle_rejects_k_not_multiple_of_128():
     with pytest.raises(ValueError):
         oracle.quant_act_1x128(np.zeros((2, 100), np.uint16))
+
+
+# ---- weight-gradient GEMM: both operands with 1x128 scales along the tokens
+def _token_operands(T, M, N, seed):
+    g = generator(seed, "cpu")
+    dy = normal_bf16((T, M), 1.0, g, "cpu")
+    x = normal_bf16((T, N), 1.0, g, "cpu", outlier_p=0.01, outlier_scale=20.0)
+    qa, sa = oracle.quant_tokens_1x128(bf16_bits(dy))
+    qb, sb = oracle.quant_tokens_1x128(bf16_bits(x))
+    return dy, x, qa, sa, qb, sb
+
+
+def test_token_quantiser_brute_force():
+    # per feature column, per run of 128 tokens: amax, fp32 IEEE division, the
+    # torch E4M3 encoder -- written as a plain loop over columns of the input
+    g = generator(31, "cpu")
+    x = normal_bf16((256, 5), 1.0, g, "cpu", outlier_p=0.02, outlier_scale=30.0)
+    q, s = oracle.quant_tokens_1x128(bf16_bits(x))
+    assert q.shape == (5, 256) and s.shape == (2, 5)
+    xf = x.float().numpy()
+    for f in range(5):
+        for tb in range(2):
+            col = xf[tb * 128:(tb + 1) * 128, f]
+            amax = np.float32(np.max(np.abs(col)))
+            sc = np.float32(amax / np.float32(448.0))
+            assert s[tb, f] == sc
+            want = torch.from_numpy((col / sc).astype(np.float32)).to(torch.float8_e4m3fn)
+            np.testing.assert_array_equal(q[f, tb * 128:(tb + 1) * 128], want.view(torch.uint8).numpy())
+            assert np.max(q[f, tb * 128:(tb + 1) * 128] & 0x7F) == 0x7E     # amax -> 448
+
+
+@pytest.mark.parametrize("T,M,N", [(128, 3, 5), (256, 8, 6), (384, 2, 130)])
+def test_gemm_tokens_matches_numpy_matmul_of_torch_dequantised(T, M, N):
+    _, _, qa, sa, qb, sb = _token_operands(T, M, N, seed=T + M + N)
+    A = torch_decode(qa) * np.repeat(sa.T, 128, axis=1).astype(np.float64)
+    B = torch_decode(qb) * np.repeat(sb.T, 128, axis=1).astype(np.float64)
+    got = oracle.gemm_f64_tokens(qa, sa, qb, sb)
+    np.testing.assert_allclose(got, A @ B.T, rtol=1e-12, atol=1e-300)
+
+
+def test_gemm_tokens_reduces_to_block_scaled_gemm():
+    # if every 128-row block of B shares one scale per slice, the per-row B
+    # scales are a 128x128 block grid and the two GEMM definitions coincide
+    _, _, qa, sa, qb, _ = _token_operands(256, 4, 256, seed=3)
+    rng = np.random.default_rng(4)
+    s_block = rng.uniform(0.01, 2.0, size=(2, 2)).astype(np.float32)      # [N/128][K/128]
+    s_rows = np.repeat(s_block.T, 128, axis=1)                             # [K/128][N]
+    np.testing.assert_array_equal(oracle.gemm_f64_tokens(qa, sa, qb, s_rows),
+                                  oracle.gemm_f64(qa, sa, qb, s_block))
+
+
+def test_gemm_tokens_constant_closed_form():
+    # constant magnitude per (row, 128-token run): codes +-448, so
+    # C[m][n] = sum_kb 128 * 448^2 * sA[kb][m] * sB[kb][n] * sign
+    T, M, N = 256, 2, 3
+    dy = np.zeros((T, M), np.float32)
+    x = np.zeros((T, N), np.float32)
+    for tb in range(2):
+        for m in range(M):
+            dy[tb * 128:(tb + 1) * 128, m] = (m + 1) * (0.5 if tb else -1.5)
+        for n in range(N):
+            x[tb * 128:(tb + 1) * 128, n] = (n + 2) * (0.25 if tb else 3.0)
+    qa, sa = oracle.quant_tokens_1x128(f32_bits_to_bf16_bits(dy))
+    qb, sb = oracle.quant_tokens_1x128(f32_bits_to_bf16_bits(x))
+    got = oracle.gemm_f64_tokens(qa, sa, qb, sb)
+    for m in range(M):
+        for n in range(N):
+            want = sum(128 * 448.0 * 448.0 * float(sa[tb, m]) * float(sb[tb, n]) *
+                       float(np.sign(dy[tb * 128, m]) * np.sign(x[tb * 128, n])) for tb in range(2))
+            assert got[m, n] == pytest.approx(want, rel=1e-14)
+
+
+def test_weight_gradient_close_to_unquantised_product():
+    # dW = dY^T . X through the quantised operands stays within the E4M3
+    # rounding of the operands of the float64 product of the BF16 inputs
+    dy, x, qa, sa, qb, sb = _token_operands(512, 16, 24, seed=9)
+    got = oracle.gemm_f64_tokens(qa, sa, qb, sb)
+    dyf, xf = dy.double().numpy(), x.double().numpy()
+    ref = dyf.T @ xf
+    # per element: half an E4M3 step, 2^-4 relative (normal) or 2^-10 * scale (subnormal)
+    ea = 2.0 ** -4 * np.abs(dyf) + 2.0 ** -10 * np.repeat(sa.astype(np.float64), 128, axis=0)
+    eb = 2.0 ** -4 * np.abs(xf) + 2.0 ** -10 * np.repeat(sb.astype(np.float64), 128, axis=0)
+    bound = np.abs(dyf).T @ eb + ea.T @ np.abs(xf) + ea.T @ eb
+    assert np.all(np.abs(got - ref) <= bound * (1 + 1e-9))
