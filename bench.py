@@ -149,6 +149,8 @@ def make_workload(name, device):
         return synthetic.tiny(device=device)
     if name == "experts":
         return synthetic.experts(device=device)
+    if name == "wgrad":
+        return synthetic.wgrad(device=device)
     raise ValueError(name)
 
 
@@ -259,6 +261,69 @@ class DenseStep:
             self.host_sc.copy_(self.sc, non_blocking=True)
 
 
+class WgradStep:
+    """quant_tokens(dY) || quant_tokens(X) -> weight-gradient GEMM, over
+    rotating input sets (> 2x L2): dW = dY^T . X with both operands quantised
+    per 1x128 run of tokens."""
+
+    def __init__(self, case, fp8, torch):
+        self.fp8, self.torch, self.case = fp8, torch, case
+        T, M, N = case.T, case.M, case.N
+        self.M, self.N, self.K = M, N, T
+        in_bytes = (case.dy.numel() + case.x.numel()) * 2
+        self.nsets = max(1, min(8, -(-2 * L2_BYTES // in_bytes) + 1))
+        self.sets = [(case.dy, case.x)] + [(case.dy.clone(), case.x.clone()) for _ in range(self.nsets - 1)]
+        dev = case.dy.device
+        self.qa = torch.empty((M, T), dtype=torch.uint8, device=dev)
+        self.sa = torch.empty((T // 128, M), dtype=torch.float32, device=dev)
+        self.qb = torch.empty((N, T), dtype=torch.uint8, device=dev)
+        self.sb = torch.empty((T // 128, N), dtype=torch.float32, device=dev)
+        self.c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.flops = 2.0 * M * N * T
+        self.kernels = ["quant_dy", "quant_x", "gemm"]
+        self.kernel_bytes = {
+            "quant_dy": T * M * 3 + self.sa.numel() * 4,
+            "quant_x": T * N * 3 + self.sb.numel() * 4,
+            "gemm": M * T + N * T + (self.sa.numel() + self.sb.numel()) * 4 + M * N * 2,
+        }
+        self.h2d_bytes = in_bytes
+        self.d2h_bytes = M * N * 2
+        self.launches_per_step = 3
+        self.side = torch.cuda.Stream(device=dev)
+        self.schedule = "quant_tokens(dY) || quant_tokens(X) -> wgrad gemm"
+
+    def run(self, i, events=None):
+        """events: (start, end) per kernel in `kernels` order, or None."""
+        dy, x = self.sets[i % self.nsets]
+        f, torch = self.fp8, self.torch
+        main = torch.cuda.current_stream()
+        self.side.wait_stream(main)
+        with torch.cuda.stream(self.side):
+            if events: events[0].record(self.side)
+            f.fp8_quant_tokens_1x128(dy, self.qa, self.sa, stream=self.side)
+            if events: events[1].record(self.side)
+        if events: events[2].record(main)
+        f.fp8_quant_tokens_1x128(x, self.qb, self.sb)
+        if events: events[3].record(main)
+        main.wait_stream(self.side)
+        if events: events[4].record(main)
+        f.fp8_gemm_wgrad(self.qa, self.sa, self.qb, self.sb, C=self.c)
+        if events: events[5].record(main)
+
+    def run_host(self, host_a, host_w, host_c, dev_a, dev_w):
+        f, torch = self.fp8, self.torch
+        main = torch.cuda.current_stream()
+        self.side.wait_stream(main)
+        with torch.cuda.stream(self.side):
+            dev_a.copy_(host_a, non_blocking=True)
+            f.fp8_quant_tokens_1x128(dev_a, self.qa, self.sa, stream=self.side)
+        dev_w.copy_(host_w, non_blocking=True)
+        f.fp8_quant_tokens_1x128(dev_w, self.qb, self.sb)
+        main.wait_stream(self.side)
+        f.fp8_gemm_wgrad(self.qa, self.sa, self.qb, self.sb, C=self.c)
+        host_c.copy_(self.c, non_blocking=True)
+
+
 class ExpertsStep:
     """quant_act(X_sorted) + grouped GEMM (weights quantised once, untimed)."""
 
@@ -330,6 +395,24 @@ def oracle_sample(workload_name, case_cpu_fn, rows=8):
                                     f"float64 GEMM), single-threaded C")
 
 
+def oracle_sample_wgrad(case, cols=2):
+    """The oracle on a bounded sample of the weight-gradient workload: quantise
+    the whole dY along tokens and `cols` input-feature columns of X, then the
+    float64 GEMM of every dY feature against those columns."""
+    import oracle
+    import synthetic
+    dy_bits = synthetic.bf16_bits(case.dy)
+    x_bits = synthetic.bf16_bits(case.x[:, :cols])
+    t0 = time.perf_counter()
+    qa, sa = oracle.quant_tokens_1x128(dy_bits)
+    qb, sb = oracle.quant_tokens_1x128(x_bits)
+    c = oracle.gemm_f64_tokens(qa, sa, qb, sb)
+    dt = time.perf_counter() - t0
+    return 2.0 * c.shape[0] * c.shape[1] * case.T, dt, (
+        f"all {case.M} dY features x {cols} X features over {case.T} tokens (quantise dY and those "
+        f"columns along tokens, float64 GEMM), single-threaded C")
+
+
 def dense_host_inputs(case):
     import synthetic
     return synthetic.bf16_bits(case.a), synthetic.bf16_bits(case.w), case.b_major
@@ -368,10 +451,14 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
 
     case = make_workload(args.workload, device)
-    if args.e4m3_out and args.workload == "experts":
-        raise SystemExit("--e4m3-out applies to the dense workloads")
-    step = ExpertsStep(case, fp8, torch) if args.workload == "experts" else \
-        DenseStep(case, fp8, torch, e4m3_out=args.e4m3_out)
+    if args.e4m3_out and args.workload in ("experts", "wgrad"):
+        raise SystemExit("--e4m3-out applies to the dense forward workloads")
+    if args.workload == "experts":
+        step = ExpertsStep(case, fp8, torch)
+    elif args.workload == "wgrad":
+        step = WgradStep(case, fp8, torch)
+    else:
+        step = DenseStep(case, fp8, torch, e4m3_out=args.e4m3_out)
     stream = torch.cuda.current_stream()
 
     for i in range(args.warmup):
@@ -430,6 +517,9 @@ def run_ours(args):
             host_a = step.x.cpu().pin_memory()
             host_w = None
             dev_a, dev_w = torch.empty_like(step.x), None
+        elif args.workload == "wgrad":
+            host_a, host_w = case.dy.cpu().pin_memory(), case.x.cpu().pin_memory()
+            dev_a, dev_w = torch.empty_like(case.dy), torch.empty_like(case.x)
         else:
             host_a = case.a.cpu().pin_memory()
             host_w = case.w.cpu().pin_memory()
@@ -495,7 +585,11 @@ def run_ours(args):
 
     # ---- CPU baseline (oracle) on a bounded sample, rank 0 at N=1 only
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and args.workload != "experts":
+    if rank == 0 and world == 1 and not args.no_cpu and args.workload == "wgrad":
+        flops, secs, desc = oracle_sample_wgrad(case)
+        cpu = {"value": round(flops / secs / 1e12, 9), "unit": "TFLOP/s", "cores": 1,
+               "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+    elif rank == 0 and world == 1 and not args.no_cpu and args.workload != "experts":
         flops, secs, desc = oracle_sample(args.workload, lambda: dense_host_inputs(case))
         cpu = {"value": round(flops / secs / 1e12, 9), "unit": "TFLOP/s", "cores": 1,
                "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
@@ -532,9 +626,9 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    if args.workload == "experts":
+    if args.workload in ("experts", "wgrad"):
         print(json.dumps({"impl": "reference", "unavailable":
-                          "the oracle arm samples the dense workloads only"}), flush=True)
+                          "the oracle arm samples the dense forward workloads only"}), flush=True)
         return
     import numpy as np
     import oracle
@@ -583,7 +677,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="mla_q",
-                    choices=["mla_q", "mla_kv", "dgrad", "experts", "tiny"])
+                    choices=["mla_q", "mla_kv", "dgrad", "experts", "tiny", "wgrad"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end run")

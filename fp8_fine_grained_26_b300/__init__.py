@@ -34,8 +34,8 @@ _STATUS_NAMES = {
 }
 
 EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
-            "fp8_gemm_blockscaled_e4m3_out", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
-            "fp8bs_selftest_wait_timeout")
+            "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
+            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout")
 
 
 class Fp8bsError(RuntimeError):
@@ -55,6 +55,8 @@ def _load():
         "fp8_quant_w_128x128": [p, i64, i64, i64, p, i64, p, p],
         "fp8_gemm_blockscaled": [p, p, p, p, i64, i64, i64, i32, p, i32, i64, p],
         "fp8_gemm_blockscaled_e4m3_out": [p, p, p, p, i64, i64, i64, i32, p, i64, p, p],
+        "fp8_quant_tokens_1x128": [p, i64, i64, i64, p, i64, p, p],
+        "fp8_gemm_wgrad": [p, p, p, p, i64, i64, i64, p, i32, i64, p],
         "fp8_grouped_gemm_blockscaled": [p, p, p, p, p, i32, i64, i64, i64, p, i32, i64, p],
         "fp8bs_last_error": [p],
         "fp8bs_selftest_wait_timeout": [i64, p],
@@ -210,6 +212,43 @@ def fp8_gemm_blockscaled_e4m3_out(qA, sA, qB, sB, b_major=B_KMAJOR, qC=None, sC=
     return qC, sC
 
 
+def fp8_quant_tokens_1x128(x, qT=None, s=None, stream=None):
+    """Quantise a BF16 ``[T, F]`` matrix per 1x128 run of tokens in each
+    feature column; returns ``(qT uint8 [F, T], s float32 [T/128, F])``."""
+    _need(x, torch.bfloat16, "x", 2)
+    _row_major(x, "x")
+    T, F = x.shape
+    if qT is None:
+        qT = torch.empty((F, T), dtype=torch.uint8, device=x.device)
+    if s is None:
+        s = torch.empty((T // 128, F), dtype=torch.float32, device=x.device)
+    _row_major(qT, "qT")
+    ldx = x.stride(0) if T > 0 else F
+    ldq = qT.stride(0) if F > 0 else T
+    _check(lib.fp8_quant_tokens_1x128(_ptr(x), T, F, ldx, _ptr(qT), ldq, _ptr(s), _stream(stream)),
+           "fp8_quant_tokens_1x128")
+    return qT, s
+
+
+def fp8_gemm_wgrad(qA, sA, qB, sB, out_dtype=torch.bfloat16, C=None, stream=None):
+    """Weight-gradient GEMM ``C = A . B^T`` with both operands scaled per row
+    and 128-wide K-slice: ``qA [M, K]`` / ``sA [K/128, M]``, ``qB [N, K]`` /
+    ``sB [K/128, N]`` (outputs of :func:`fp8_quant_tokens_1x128`)."""
+    for t, n, d in ((qA, "qA", torch.uint8), (qB, "qB", torch.uint8), (sA, "sA", torch.float32),
+                    (sB, "sB", torch.float32)):
+        _need(t, d, n, 2)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    M, K = qA.shape
+    N, Kb = qB.shape
+    if Kb != K:
+        raise ValueError("qA and qB disagree on K")
+    C, cd, ldc = _out(C, M, N, out_dtype, qA.device)
+    _check(lib.fp8_gemm_wgrad(_ptr(qA), _ptr(sA), _ptr(qB), _ptr(sB), M, N, K, _ptr(C), cd, ldc,
+                              _stream(stream)), "fp8_gemm_wgrad")
+    return C
+
+
 def fp8_grouped_gemm_blockscaled(qA, sA, qB, sB, seg_offsets, out_dtype=torch.bfloat16, C=None,
                                  stream=None):
     """Per-expert ``C[rows of e] = A[rows of e] . B_e^T`` with ``qB [E, N, K]``,
@@ -246,7 +285,7 @@ def fp8bs_selftest_wait_timeout(limit_us=20000, stream=None):
 
 
 __all__ = ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
-           "fp8_gemm_blockscaled_e4m3_out",
+           "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout",
            "Fp8bsError", "lib",
            "LIB_PATH", "EXPORTED", "B_KMAJOR", "B_MNMAJOR", "OUT_BF16", "OUT_FP32"]

@@ -79,6 +79,15 @@ int current_device(DeviceInfo **info)
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem) != cudaSuccess ||
             cudaFuncSetAttribute(fp8_gemm_kernel<false, true, true, PAIR_STAGES, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, false, false, 3, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 gemm_smem_bytes<false, 3, B_STAGE_BYTES, SCALE_SLOT_FLOATS_TOK>()) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, false, true, PAIR_STAGES, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 gemm_smem_bytes<false, PAIR_STAGES, B_STAGE_BYTES / 2, SCALE_SLOT_FLOATS_TOK>()) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(quant_tokens_1x128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 quant_smem_bytes()) != cudaSuccess ||
             cudaFuncSetAttribute(fp8_gemm_kernel<true, false, false, 3>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  gemm_smem_bytes<true, 3>()) != cudaSuccess ||
@@ -222,9 +231,9 @@ int check_gemm_common(const void *qA, const float *sA, const void *qB, const flo
 // stride in bytes).
 int launch_dense(DeviceInfo *dev, const void *qA, const float *sA, const void *qB, const float *sB,
                  int64_t M, int64_t N, int64_t K, int b_major, void *C, int c_dtype, int64_t ldc,
-                 float *sC, cudaStream_t stream)
+                 float *sC, cudaStream_t stream, bool tok = false)
 {
-    const bool qout = sC != nullptr;
+    const bool qout = sC != nullptr;              // (tok implies K-major B and no qout)
     CUtensorMap tmA, tmB;
     if (!encode_2d_u8(&tmA, qA, (uint64_t)K, (uint64_t)M, (uint64_t)K, BK, BM))
         return FP8BS_ERR_ARG;
@@ -275,7 +284,8 @@ int launch_dense(DeviceInfo *dev, const void *qA, const float *sA, const void *q
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(g.num_tiles, dev->max_pairs)));
         cfg.blockDim = dim3(GEMM_THREADS);
-        cfg.dynamicSmemBytes = gemm_smem_bytes<false, PAIR_STAGES, B_STAGE_BYTES / 2>();
+        cfg.dynamicSmemBytes = tok ? gemm_smem_bytes<false, PAIR_STAGES, B_STAGE_BYTES / 2, SCALE_SLOT_FLOATS_TOK>()
+                                   : gemm_smem_bytes<false, PAIR_STAGES, B_STAGE_BYTES / 2>();
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -285,7 +295,9 @@ int launch_dense(DeviceInfo *dev, const void *qA, const float *sA, const void *q
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         cudaError_t e;
-        if (b_major == FP8BS_B_KMAJOR)
+        if (tok)
+            e = cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES, false, true>, tmA, tmB, tmC, g);
+        else if (b_major == FP8BS_B_KMAJOR)
             e = qout ? cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES, true>, tmA, tmB, tmC, g)
                      : cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES>, tmA, tmB, tmC, g);
         else
@@ -296,7 +308,11 @@ int launch_dense(DeviceInfo *dev, const void *qA, const float *sA, const void *q
     g.num_tiles = (int64_t)g.num_m_blk * g.num_n_blk;
     const int grid = (int)std::min<int64_t>(g.num_tiles, dev->num_sms);
     const int smem = gemm_smem_bytes<false, 3>();
-    if (b_major == FP8BS_B_KMAJOR) {
+    if (tok) {
+        fp8_gemm_kernel<false, false, false, 3, false, true>
+            <<<grid, GEMM_THREADS, gemm_smem_bytes<false, 3, B_STAGE_BYTES, SCALE_SLOT_FLOATS_TOK>(), stream>>>(
+                tmA, tmB, tmC, g);
+    } else if (b_major == FP8BS_B_KMAJOR) {
         if (qout)
             fp8_gemm_kernel<false, false, false, 3, true><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmC, g);
         else
@@ -441,6 +457,48 @@ int fp8_gemm_blockscaled_e4m3_out(const void *qA, const float *sA, const void *q
         return FP8BS_OK;
     }
     return launch_dense(dev, qA, sA, qB, sB, M, N, K, b_major, qC, FP8BS_OUT_BF16, ldqc, sC, stream);
+}
+
+int fp8_quant_tokens_1x128(const void *x_bf16, int64_t T, int64_t F, int64_t ldx, void *qT, int64_t ldq,
+                           float *s, cudaStream_t stream)
+{
+    if (T < 0 || F < 0 || T % 128 != 0)
+        return FP8BS_ERR_SHAPE;
+    if (T == 0 || F == 0)
+        return FP8BS_OK;
+    if (!x_bf16 || !qT || !s)
+        return FP8BS_ERR_NULL;
+    if (ldx < F || ldq < T)
+        return FP8BS_ERR_SHAPE;
+    if (!aligned16(x_bf16) || !aligned16(qT) || !aligned4(s) || (ldx * 2) % 16 != 0 || ldq % 16 != 0)
+        return FP8BS_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    CUtensorMap tmX;
+    if (!encode_bf16_units(&tmX, x_bf16, (uint64_t)F, (uint64_t)T, (uint64_t)ldx))
+        return FP8BS_ERR_ARG;
+    const int64_t FB = (F + 127) / 128;
+    const int64_t units = (T / 128) * FB;
+    const int grid = (int)std::min<int64_t>(units, 3 * (int64_t)dev->num_sms);
+    quant_tokens_1x128_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
+        tmX, T, F, FB, static_cast<uint8_t *>(qT), ldq, s, units);
+    return launch_status();
+}
+
+int fp8_gemm_wgrad(const void *qA, const float *sA, const void *qB, const float *sB, int64_t M, int64_t N,
+                   int64_t K, void *C, int c_dtype, int64_t ldc, cudaStream_t stream)
+{
+    if (int st = check_gemm_common(qA, sA, qB, sB, M, N, K, C, c_dtype, ldc))
+        return st;
+    if (M == 0 || N == 0)
+        return FP8BS_OK;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    if (K == 0)
+        return zero_output(C, c_dtype, ldc, M, N, stream);
+    return launch_dense(dev, qA, sA, qB, sB, M, N, K, FP8BS_B_KMAJOR, C, c_dtype, ldc, nullptr, stream, true);
 }
 
 int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA, const void *qB,

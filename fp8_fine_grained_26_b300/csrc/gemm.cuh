@@ -61,6 +61,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_EXPERTS = 2048;
 constexpr int SCALE_SLOTS = 8;                           // slices of scales staged ahead
 constexpr int SCALE_SLOT_FLOATS = 132;                   // 128 row scales + 2 column-block scales (+pad)
+constexpr int SCALE_SLOT_FLOATS_TOK = 384;               // weight gradient: 128 row + 256 column scales
 constexpr int SCALE_LOOKAHEAD = 2;                       // loader copy groups in flight
 constexpr int B_PREFETCH_SLICES = 2;                     // grouped: L2 prefetch distance of expert weights
 
@@ -69,7 +70,7 @@ constexpr int B_PREFETCH_SLICES = 2;                     // grouped: L2 prefetch
 // boxes (two 64-column halves per promote warpgroup, so a tile's stores never
 // wait on each other), barriers, the scale ring and (grouped) the expert tile
 // table.
-template <int S, int BSB = B_STAGE_BYTES>
+template <int S, int BSB = B_STAGE_BYTES, int SSF = SCALE_SLOT_FLOATS>
 struct Layout {
     static constexpr int A = 0;
     static constexpr int B = A + S * A_STAGE_BYTES;
@@ -78,14 +79,16 @@ struct Layout {
     // full, empty, pfull, pempty, drain, sready, sfree, per-warpgroup epilogue pair
     static constexpr int NUM_BARS = 2 * S + 2 + 2 + 1 + 2 * SCALE_SLOTS + 4;
     static constexpr int MISC = BAR + NUM_BARS * 8;                 // tmem slot, abort flag
-    static constexpr int SCALES = MISC + 16;                        // scale ring
-    static constexpr int TILES = SCALES + SCALE_SLOTS * SCALE_SLOT_FLOATS * 4;  // grouped: tile prefix [E+1]
+    static constexpr int SCALES = (MISC + 16 + 127) & ~127;         // scale ring (16-byte vector reads)
+    static constexpr int TILES = SCALES + SCALE_SLOTS * SSF * 4;   // grouped: tile prefix [E+1]
+    static_assert(SCALES % 16 == 0 && (SSF * 4) % 16 == 0, "scale slots must allow 16-byte reads");
+    static_assert(EPI % 1024 == 0 && A % 1024 == 0 && B % 1024 == 0, "swizzled regions need 1024-byte alignment");
 };
 
-template <bool GROUPED, int S, int BSB = B_STAGE_BYTES>
+template <bool GROUPED, int S, int BSB = B_STAGE_BYTES, int SSF = SCALE_SLOT_FLOATS>
 constexpr int gemm_smem_bytes()
 {
-    return 1024 + Layout<S, BSB>::TILES + (GROUPED ? (MAX_EXPERTS + 1) * 4 : 0);
+    return 1024 + Layout<S, BSB, SSF>::TILES + (GROUPED ? (MAX_EXPERTS + 1) * 4 : 0);
 }
 
 struct GemmArgs {
@@ -138,9 +141,9 @@ struct Tile {
     int32_t expert;
 };
 
-template <int S, int BSB = B_STAGE_BYTES>
+template <int S, int BSB = B_STAGE_BYTES, int SSF = SCALE_SLOT_FLOATS>
 struct SharedState {
-    using L = Layout<S, BSB>;
+    using L = Layout<S, BSB, SSF>;
     uint32_t base;      // shared address of the aligned base
     uint8_t *gbase;     // generic pointer to the same
     __device__ uint32_t bar(int i) const { return base + L::BAR + 8 * i; }
@@ -156,7 +159,7 @@ struct SharedState {
     __device__ uint32_t epi_free(int wg) const { return bar(2 * S + 5 + 2 * SCALE_SLOTS + wg); }
     __device__ uint32_t epi_full(int wg) const { return bar(2 * S + 7 + 2 * SCALE_SLOTS + wg); }
     __device__ uint32_t epi_box(int wg, int h) const { return base + L::EPI + (2 * wg + h) * EPI_BOX_BYTES; }
-    __device__ uint32_t scale_slot(int j) const { return base + L::SCALES + j * SCALE_SLOT_FLOATS * 4; }
+    __device__ uint32_t scale_slot(int j) const { return base + L::SCALES + j * SSF * 4; }
     __device__ uint32_t a_stage(int s) const { return base + L::A + s * A_STAGE_BYTES; }
     __device__ uint32_t b_stage(int s) const { return base + L::B + s * BSB; }
     __device__ volatile uint32_t *tmem_slot() const
@@ -173,14 +176,14 @@ struct SharedState {
     }
 };
 
-template <int S, int BSB>
-__device__ __forceinline__ bool wait_bounded(const SharedState<S, BSB> &ss, uint32_t bar, uint32_t parity)
+template <int S, int BSB, int SSF>
+__device__ __forceinline__ bool wait_bounded(const SharedState<S, BSB, SSF> &ss, uint32_t bar, uint32_t parity)
 {
     return wait_bounded(bar, parity, ss.abort_flag());
 }
 
-template <bool GROUPED, int S, int BSB>
-__device__ __forceinline__ int64_t total_tiles(const GemmArgs &g, const SharedState<S, BSB> &ss)
+template <bool GROUPED, int S, int BSB, int SSF>
+__device__ __forceinline__ int64_t total_tiles(const GemmArgs &g, const SharedState<S, BSB, SSF> &ss)
 {
     if constexpr (GROUPED)
         return ss.tile_prefix()[g.E];
@@ -188,8 +191,8 @@ __device__ __forceinline__ int64_t total_tiles(const GemmArgs &g, const SharedSt
         return g.num_tiles;
 }
 
-template <bool GROUPED, bool PAIR, int S, int BSB>
-__device__ __forceinline__ Tile tile_at(const GemmArgs &g, const SharedState<S, BSB> &ss, int64_t t, uint32_t rank)
+template <bool GROUPED, bool PAIR, int S, int BSB, int SSF>
+__device__ __forceinline__ Tile tile_at(const GemmArgs &g, const SharedState<S, BSB, SSF> &ss, int64_t t, uint32_t rank)
 {
     Tile tl;
     if constexpr (GROUPED) {
@@ -236,8 +239,8 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &g, const SharedState<S, 
 // prefix over experts into shared memory.  Offsets are clamped into
 // [0, M_total] and made nondecreasing, so malformed offsets cannot move any
 // access out of bounds.
-template <int S, int BSB>
-__device__ void build_tile_prefix(const GemmArgs &g, const SharedState<S, BSB> &ss)
+template <int S, int BSB, int SSF>
+__device__ void build_tile_prefix(const GemmArgs &g, const SharedState<S, BSB, SSF> &ss)
 {
     __shared__ int32_t chunk_sum[GEMM_THREADS];
     int32_t *pre = ss.tile_prefix();
@@ -282,6 +285,35 @@ __device__ __forceinline__ void promote64(float2 *acc, const uint32_t (&p)[64], 
     for (int j = 0; j < 32; ++j)
         acc[j] = __ffma2_rn(make_float2(__uint_as_float(p[2 * j]), __uint_as_float(p[2 * j + 1])), s2,
                             acc[j]);
+}
+
+// acc[j] += P[j] * (sa * sB[j]) for 64 columns whose scales sB are 64 floats
+// at shared address `sb`: per-column scales of the weight-gradient GEMM.  The
+// scales are read in groups of 8 (two 16-byte loads issued together: the
+// promote threads have no registers to spare), the scale pairs formed with
+// packed multiplies, then packed FMAs.
+__device__ __forceinline__ void promote64_cols(float2 *acc, const uint32_t (&p)[64], float sa, uint32_t sb)
+{
+    const float2 sa2 = make_float2(sa, sa);
+#pragma unroll
+    for (int grp = 0; grp < 8; ++grp) {
+        float4 b[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(b[i].x), "=f"(b[i].y), "=f"(b[i].z), "=f"(b[i].w)
+                         : "r"(sb + 16 * (2 * grp + i)));
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int c = 2 * grp + i;
+            const float2 s0 = __fmul2_rn(sa2, make_float2(b[i].x, b[i].y));
+            const float2 s1 = __fmul2_rn(sa2, make_float2(b[i].z, b[i].w));
+            acc[2 * c] = __ffma2_rn(make_float2(__uint_as_float(p[4 * c]), __uint_as_float(p[4 * c + 1])), s0,
+                                    acc[2 * c]);
+            acc[2 * c + 1] = __ffma2_rn(make_float2(__uint_as_float(p[4 * c + 2]), __uint_as_float(p[4 * c + 3])),
+                                        s1, acc[2 * c + 1]);
+        }
+    }
 }
 
 // Direct, masked stores of one thread's row segment (128 columns from n_first).
@@ -333,15 +365,19 @@ __device__ __forceinline__ void store_row_direct(const GemmArgs &g, const float2
 // row tile (the activation quantiser's rule applied to the BF16-rounded
 // output, bit for bit) instead of BF16.  Dense only; N % 128 == 0 and a
 // TMA-able code matrix are guaranteed by the host.
-template <bool GROUPED, bool B_MN, bool PAIR, int STAGES, bool QOUT = false>
+// TOK: the weight-gradient GEMM -- B carries one scale per row and 128-wide
+// K-slice (sB [K/128][N]), like A, so each output column has its own B
+// scale; dense, K-major B, BF16 or FP32 output.
+template <bool GROUPED, bool B_MN, bool PAIR, int STAGES, bool QOUT = false, bool TOK = false>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs g)
 {
     constexpr int BSB = PAIR ? B_STAGE_BYTES / 2 : B_STAGE_BYTES;   // pair: this CTA's half of B
-    using L = Layout<STAGES, BSB>;
+    constexpr int SSF = TOK ? SCALE_SLOT_FLOATS_TOK : SCALE_SLOT_FLOATS;
+    using L = Layout<STAGES, BSB, SSF>;
     extern __shared__ uint8_t smem_raw[];
-    SharedState<STAGES, BSB> ss;
+    SharedState<STAGES, BSB, SSF> ss;
     {
         const uint32_t raw = ptx::smem_u32(smem_raw);
         const uint32_t aligned = (raw + 1023u) & ~1023u;
@@ -556,7 +592,18 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         ptx::cp_async_4(dst + 4 * r, in ? (const void *)(g.sA + (int64_t)kb * g.M + gm) : (const void *)g.sA,
                                         in ? 4u : 0u);
                     }
-                    if (lane < 2) {
+                    if constexpr (TOK) {
+                        // the tile's 256 column scales sB[kb][n0 .. n0+255]
+                        const float *src0 = g.sB + (int64_t)kb * g.N + tl.n0;
+#pragma unroll 1
+                        for (int i = 0; i < 8; ++i) {
+                            const int c = lane + 32 * i;
+                            const int64_t n = (int64_t)tl.n0 + c;
+                            const bool in = n < g.N;
+                            ptx::cp_async_4(dst + 4 * (128 + c), in ? (const void *)(src0 + c) : (const void *)g.sB,
+                                            in ? 4u : 0u);
+                        }
+                    } else if (lane < 2) {
                         const int nblk = (tl.n0 >> 7) + lane;
                         const bool in = nblk < g.NB128;
                         const float *src;
@@ -603,11 +650,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 // this slice's scales from the shared ring (staged by warp 2)
                 const int slot = (int)(pit % SCALE_SLOTS);
                 if (!wait_bounded(ss, ss.sready(slot), (pit / SCALE_SLOTS) & 1u)) { ok = false; break; }
-                float sa, sb;
+                float sa, sb = 1.0f;
                 asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sa) : "r"(ss.scale_slot(slot) + 4 * row));
-                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sb) : "r"(ss.scale_slot(slot) + 4 * (128 + wg)));
-                ptx::mbar_arrive(ss.sfree(slot));
+                if constexpr (!TOK) {
+                    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sb) : "r"(ss.scale_slot(slot) + 4 * (128 + wg)));
+                    ptx::mbar_arrive(ss.sfree(slot));
+                }
                 const float scale = sa * sb;
+                // TOK: this warpgroup's 128 column scales, read during the promotion
+                const uint32_t col_scales = ss.scale_slot(slot) + 4 * (128 + col_half);
                 const int p = pit & 1;
                 const uint32_t pph = (pit >> 1) & 1u;
                 if (!wait_bounded(ss, ss.pfull(p), pph)) { ok = false; break; }
@@ -619,7 +670,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 uint32_t r[64];
                 ptx::tmem_ld_32x32b_x64(taddr, r);
                 ptx::tmem_ld_wait(r);
-                promote64(acc2, r, scale);
+                if constexpr (TOK)
+                    promote64_cols(acc2, r, sa, col_scales);
+                else
+                    promote64(acc2, r, scale);
                 ptx::tmem_ld_32x32b_x64(taddr + 64, r);
                 ptx::tmem_ld_wait(r);
                 ptx::tc_fence_before();
@@ -628,7 +682,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     ptx::mbar_arrive_cluster_if(ptx::mapa_shared(ss.pempty(p), 0), lane == 0);   // the leader's MMA
                 else
                     ptx::mbar_arrive_cluster_if(ss.pempty(p), lane == 0);
-                promote64(acc2 + 32, r, scale);
+                if constexpr (TOK) {
+                    promote64_cols(acc2 + 32, r, sa, col_scales + 4 * 64);
+                    ptx::mbar_arrive(ss.sfree(slot));    // the column scales have been read
+                } else {
+                    promote64(acc2 + 32, r, scale);
+                }
             }
             if (!ok)
                 break;

@@ -99,8 +99,8 @@ constexpr int QUNIT_BYTES = 128 * 128 * 2;                    // 32 KiB of BF16
 constexpr int QUANT_THREADS = 256;
 constexpr int QSMEM_BAR = QSTAGES * QUNIT_BYTES;                // full barriers
 constexpr int QSMEM_ABORT = QSMEM_BAR + 8 * QSTAGES;
-constexpr int QSMEM_RED = QSMEM_ABORT + 8;                       // 2 x 128 floats / 2 x 8 words
-constexpr int QSMEM_END = QSMEM_RED + 2 * 128 * 4;
+constexpr int QSMEM_RED = QSMEM_ABORT + 8;                       // 2 buffers x 256 words
+constexpr int QSMEM_END = QSMEM_RED + 2 * 256 * 4;
 constexpr int quant_smem_bytes() { return 1024 + QSMEM_END; }
 
 struct QRing {
@@ -112,10 +112,10 @@ struct QRing {
     {
         return reinterpret_cast<volatile uint32_t *>(gbase + QSMEM_ABORT);
     }
-    __device__ float *red_f(int b) const { return reinterpret_cast<float *>(gbase + QSMEM_RED) + 128 * b; }
+    __device__ float *red_f(int b) const { return reinterpret_cast<float *>(gbase + QSMEM_RED) + 256 * b; }
     __device__ uint32_t *red_u(int b) const
     {
-        return reinterpret_cast<uint32_t *>(gbase + QSMEM_RED) + 128 * b;
+        return reinterpret_cast<uint32_t *>(gbase + QSMEM_RED) + 256 * b;
     }
 };
 
@@ -312,6 +312,89 @@ __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_w_128x128_kernel(
         }
         if (tid == 0)
             sW[rb * CB + cb] = d.s;
+    }
+    qdrain(r, j, issued);
+}
+
+// Token-dimension quantiser (the weight-gradient GEMM's operands): X is
+// [T][F] (features contiguous); every feature column is cut into runs of 128
+// tokens, each quantised with the 1x128 rule, and the codes are written
+// transposed, qT[f][t], so that the GEMM reads them K(token)-major.  Unit
+// (tb, fb): tokens [128 tb, +128) x features [128 fb, +128), staged through
+// the same TMA ring.  Thread t holds the feature pair (2 fp, 2 fp + 1),
+// fp = t % 64, for the 32 tokens of quarter t / 64 (32-bit shared loads, one
+// 128-byte row segment per warp and token); the amax of each feature is the
+// max over the four quarters, exchanged through shared memory.
+__global__ void __launch_bounds__(QUANT_THREADS, 3) quant_tokens_1x128_kernel(
+    const __grid_constant__ CUtensorMap tmX, int64_t T, int64_t F, int64_t FB, uint8_t *__restrict__ q,
+    int64_t ldq, float *__restrict__ s, int64_t units)
+{
+    const QRing r = qring_setup();
+    const int tid = threadIdx.x;
+    const int fp = tid & 63;
+    const int qtr = tid >> 6;
+    const int64_t mine = (int64_t)blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    int64_t issued = 0;
+    if (tid == 0)
+        for (; issued < mine && issued < QSTAGES; ++issued)
+            qissue(r, &tmX, issued, FB);
+    int64_t j = 0;
+    for (; j < mine; ++j) {
+        if (!qwait(r, j))
+            break;
+        const uint32_t st = r.stage((int)(j % QSTAGES));
+        uint32_t w[32];                                    // token qtr*32 + i: features (2fp | 2fp+1 << 16)
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[i]) : "r"(st + (uint32_t)((qtr * 32 + i) * 256 + fp * 4)));
+        uint32_t mx = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            mx = ptx::max_u16x2(mx, w[i] & 0x7FFF7FFFu);
+        uint32_t *red = r.red_u((int)(j & 1));             // [4 quarters][64 feature pairs]
+        red[qtr * 64 + fp] = mx;
+        __syncthreads();                                   // stage read, partial maxima written
+        if (tid == 0 && issued < mine && issued < j + 1 + QSTAGES) {
+            qissue(r, &tmX, issued, FB);
+            ++issued;
+        }
+        mx = ptx::max_u16x2(ptx::max_u16x2(red[fp], red[64 + fp]), ptx::max_u16x2(red[128 + fp], red[192 + fp]));
+        const Divisor d0 = make_divisor(mx & 0xFFFFu);
+        const Divisor d1 = make_divisor(mx >> 16);
+        int64_t tb, fb;
+        qunit(j, FB, tb, fb);
+        const int64_t f0 = fb * 128 + 2 * fp;
+        uint32_t c0[8], c1[8];                             // 32 codes of each feature
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const uint32_t *v = w + 8 * g;
+            const uint4 lo = make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410),
+                                        __byte_perm(v[4], v[5], 0x5410), __byte_perm(v[6], v[7], 0x5410));
+            const uint4 hi = make_uint4(__byte_perm(v[0], v[1], 0x7632), __byte_perm(v[2], v[3], 0x7632),
+                                        __byte_perm(v[4], v[5], 0x7632), __byte_perm(v[6], v[7], 0x7632));
+            const uint2 a = quant_8(lo, d0);
+            const uint2 b = quant_8(hi, d1);
+            c0[2 * g] = a.x; c0[2 * g + 1] = a.y;
+            c1[2 * g] = b.x; c1[2 * g + 1] = b.y;
+        }
+        const int64_t t0 = tb * 128 + qtr * 32;
+        if (f0 < F) {
+            uint8_t *dst = q + f0 * ldq + t0;
+            ptx::st_v4(dst, c0[0], c0[1], c0[2], c0[3]);
+            ptx::st_v4(dst + 16, c0[4], c0[5], c0[6], c0[7]);
+        }
+        if (f0 + 1 < F) {
+            uint8_t *dst = q + (f0 + 1) * ldq + t0;
+            ptx::st_v4(dst, c1[0], c1[1], c1[2], c1[3]);
+            ptx::st_v4(dst + 16, c1[4], c1[5], c1[6], c1[7]);
+        }
+        if (qtr == 0) {
+            float *srow = s + tb * F;
+            if (f0 < F)
+                srow[f0] = d0.s;
+            if (f0 + 1 < F)
+                srow[f0 + 1] = d1.s;
+        }
     }
     qdrain(r, j, issued);
 }

@@ -139,6 +139,43 @@ int fp8_gemm_blockscaled_e4m3_out(const void *qA, const float *sA, const void *q
                                   float *sC, cudaStream_t stream);
 
 /*
+ * Token-dimension 1x128 quantisation, for the operands of the weight-gradient
+ * GEMM dW = dY^T . X, whose contraction runs over tokens.  The pages run all
+ * three GEMM kinds (forward, data gradient, weight gradient) in FP8 with
+ * 1x128 tiles for activation-like operands ("DeepSeek-V3 Technical Report
+ * digest", section 3, "FP8 operations" and fine-grained quantisation
+ * bullets); the tiles of the weight-gradient operands lie along the tokens,
+ * so each feature column of the [tokens][features] matrix is cut into runs of
+ * 128 tokens, each with its own scale (same amax/448 rule and encoder as
+ * fp8_quant_act_1x128), and the codes are written transposed so that the GEMM
+ * reads them token-contiguous.
+ *   x_bf16 : [T][F] BF16, row stride ldx (elements).
+ *   qT     : [F][T] E4M3 codes, row stride ldq (bytes, >= T).
+ *   s      : [T/128][F] FP32: s[tb*F + f] is the scale of feature f over
+ *            tokens [128*tb, 128*tb + 128).
+ * T a multiple of 128 (else FP8BS_ERR_SHAPE); F >= 0 arbitrary.  Alignment
+ * rules as fp8_quant_act_1x128.  Equals fp8_quant_act_1x128 of the
+ * transposed matrix, bit for bit.
+ */
+int fp8_quant_tokens_1x128(const void *x_bf16, int64_t T, int64_t F, int64_t ldx, void *qT, int64_t ldq,
+                           float *s, cudaStream_t stream);
+
+/*
+ * Weight-gradient GEMM: C[M][N] = sum_k A^[m][k] * B^[n][k] where BOTH
+ * operands carry one FP32 scale per row and 128-wide K-slice (both produced
+ * by fp8_quant_tokens_1x128, K = tokens): each slice's FP32 partial is
+ * promoted with sA[kb][m] * sB[kb][n].
+ *   qA : [M][K] E4M3 (K contiguous), sA : [K/128][M].
+ *   qB : [N][K] E4M3 (K contiguous), sB : [K/128][N].
+ *   C  : [M][N] BF16 or FP32 (c_dtype), row stride ldc.
+ * For dW = dY^T . X: A = dY quantised along tokens (M = output features),
+ * B = X quantised along tokens (N = input features), K = tokens.  Shape,
+ * alignment and error rules as fp8_gemm_blockscaled.
+ */
+int fp8_gemm_wgrad(const void *qA, const float *sA, const void *qB, const float *sB, int64_t M, int64_t N,
+                   int64_t K, void *C, int c_dtype, int64_t ldc, cudaStream_t stream);
+
+/*
  * Grouped block-scaled FP8 GEMM for routed experts (one expert per segment of
  * rows).  Rows [seg_offsets[e], seg_offsets[e+1]) of qA belong to expert e:
  *   C[m][n] = sum_kb sA[kb][m] * sB[e][n/128][kb] * sum_{k in kb} qA[m][k] * qB[e][n][k]

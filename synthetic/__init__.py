@@ -104,6 +104,33 @@ def dense_case(name, M, N, K, *, seed=0, device="cpu", w_std=0.02, outlier_p=0.0
     return DenseCase(name, a, w, b_major, out_fp32)
 
 
+@dataclass
+class WgradCase:
+    """Weight gradient dW = dY^T . X over T tokens: dy [T, M], x [T, N] (BF16)."""
+    name: str
+    dy: torch.Tensor
+    x: torch.Tensor
+
+    @property
+    def T(self):
+        return self.dy.shape[0]
+
+    @property
+    def M(self):
+        return self.dy.shape[1]
+
+    @property
+    def N(self):
+        return self.x.shape[1]
+
+
+def wgrad_case(name, T, M, N, *, seed=0, device="cpu", heavy_tail=True) -> WgradCase:
+    g = generator(seed, device)
+    dy = student_t3_bf16((T, M), g, device) if heavy_tail else normal_bf16((T, M), 1.0, g, device)
+    x = normal_bf16((T, N), 1.0, g, device)
+    return WgradCase(name, dy, x)
+
+
 def route_topk(logits: torch.Tensor, bias: torch.Tensor, topk: int):
     """Top-k expert choice per token from sigmoid affinities plus a selection
     bias; ties go to the lower expert index (stable descending sort)."""
@@ -180,6 +207,12 @@ def experts(device="cpu", seed=0, keep_x=False):
 def dgrad(device="cpu", seed=0):
     return dense_case("dgrad 8192x18432x7168 student-t", 8192, 18432, 7168, seed=seed,
                       device=device, heavy_tail=True, b_major=1)
+
+
+def wgrad(device="cpu", seed=0):
+    """Weight gradient of the data-gradient layer: dY 8192x7168 (Student-t),
+    X 8192x18432 ~N(0,1), dW = dY^T . X is 7168x18432 over 8192 tokens."""
+    return wgrad_case("wgrad 7168x18432 over 8192 tokens", 8192, 7168, 18432, seed=seed, device=device)
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:

@@ -21,8 +21,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
-        "fp8_gemm_blockscaled_e4m3_out", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
-        "fp8bs_selftest_wait_timeout"])
+        "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
+        "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout"])
 
 
 def test_library_loads_and_exports_every_declared_symbol():
@@ -109,6 +109,22 @@ def test_e4m3_out_gemm_rejects_bad_arguments():
     assert g(P(16), P(16), P(16), P(16), 4, 256, 128, 0, P(16), 128, P(16), P(0)) == -2  # ldqc < N
     assert g(P(16), P(16), P(16), P(16), 4, 256, 128, 0, P(16), 264, P(16), P(0)) == -3  # ldqc % 16
     assert g(P(16), P(16), P(16), P(16), 4, 256, 128, 0, P(8), 256, P(16), P(0)) == -3   # qC align
+
+
+def test_token_quantiser_and_wgrad_reject_bad_arguments():
+    lib = _raw()
+    q = lib.fp8_quant_tokens_1x128
+    assert q(P(16), 100, 8, 8, P(16), 112, P(16), P(0)) == -2      # T % 128
+    assert q(P(16), 0, 8, 8, P(16), 128, P(16), P(0)) == 0         # empty
+    assert q(P(0), 128, 8, 8, P(16), 128, P(16), P(0)) == -1       # NULL
+    assert q(P(16), 128, 8, 4, P(16), 128, P(16), P(0)) == -2      # ldx < F
+    assert q(P(16), 128, 8, 8, P(16), 120, P(16), P(0)) == -2      # ldq < T
+    assert q(P(16), 128, 8, 12, P(16), 128, P(16), P(0)) == -3     # ldx * 2 % 16
+    w = lib.fp8_gemm_wgrad
+    assert w(P(16), P(16), P(16), P(16), 4, 4, 100, P(16), 0, 8, P(0)) == -2     # K % 128
+    assert w(P(16), P(16), P(16), P(16), 4, 4, 128, P(16), 5, 8, P(0)) == -4     # c_dtype
+    assert w(P(0), P(16), P(16), P(16), 4, 4, 128, P(16), 0, 8, P(0)) == -1      # NULL
+    assert w(P(16), P(16), P(16), P(16), 0, 4, 128, P(16), 0, 8, P(0)) == 0      # M == 0
 
 
 def test_selftest_rejects_out_of_range_limits():
