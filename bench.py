@@ -148,7 +148,7 @@ def make_workload(name, device):
     if name == "tiny":
         return synthetic.tiny(device=device)
     if name == "experts":
-        return synthetic.experts(device=device)
+        return synthetic.experts(device=device, keep_x=True)
     if name == "wgrad":
         return synthetic.wgrad(device=device)
     raise ValueError(name)
@@ -325,7 +325,10 @@ class WgradStep:
 
 
 class ExpertsStep:
-    """quant_act(X_sorted) + grouped GEMM (weights quantised once, untimed)."""
+    """Dispatch + grouped GEMM: the routed copies of the token rows are
+    gathered and quantised in one pass (fp8_quant_act_1x128_gather, bit-equal
+    to quantising the gathered BF16 rows), then the grouped GEMM.  The expert
+    weights are quantised once, untimed, as they are once per weight update."""
 
     def __init__(self, case, fp8, torch):
         self.fp8, self.torch, self.case = fp8, torch, case
@@ -337,27 +340,31 @@ class ExpertsStep:
         self.qb, self.sb = qb.view(E, N, K), sb.view(E, -1, K // 128)
         case.w = None                       # the BF16 weights are not needed any more
         torch.cuda.empty_cache()
-        self.x = case.x_sorted
+        self.x = case.x                      # [tokens, K] BF16, before the dispatch
+        self.rows = case.token_of_row.to(torch.int32)
+        T = self.x.shape[0]
+        case.x_sorted = None
         self.qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
         self.sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
         self.c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         self.nsets = 1                      # 3.76 GB of expert weights stream per step (> L2)
         self.flops = 2.0 * M * N * K
-        self.kernels = ["quant_act", "grouped_gemm"]
+        self.kernels = ["quant_gather", "grouped_gemm"]
         self.kernel_bytes = {
-            "quant_act": M * K * 3 + (K // 128) * M * 4,
+            # each token row read once, every routed copy written once
+            "quant_gather": T * K * 2 + M * 4 + M * K + (K // 128) * M * 4,
             "grouped_gemm": M * K + E * N * K + (self.sa.numel() + self.sb.numel()) * 4 + M * N * 2,
         }
-        self.h2d_bytes = M * K * 2
+        self.h2d_bytes = T * K * 2 + M * 4
         self.d2h_bytes = M * N * 2
         self.launches_per_step = 2
-        self.schedule = "quant_act -> grouped_gemm"
+        self.schedule = "quant_gather(X, routed rows) -> grouped_gemm"
 
     def run(self, i, events=None):
         """events: (start, end) per kernel in `kernels` order, or None."""
         f = self.fp8
         if events: events[0].record()
-        f.fp8_quant_act_1x128(self.x, self.qa, self.sa)
+        f.fp8_quant_act_1x128_gather(self.x, self.rows, self.qa, self.sa)
         if events: events[1].record()
         if events: events[2].record()
         f.fp8_grouped_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, self.case.offsets,
@@ -366,8 +373,9 @@ class ExpertsStep:
 
     def run_host(self, host_a, host_w, host_c, dev_a, dev_w):
         dev_a.copy_(host_a, non_blocking=True)
+        self.rows.copy_(host_w, non_blocking=True)   # the routed rows come with the tokens
         f = self.fp8
-        f.fp8_quant_act_1x128(dev_a, self.qa, self.sa)
+        f.fp8_quant_act_1x128_gather(dev_a, self.rows, self.qa, self.sa)
         f.fp8_grouped_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, self.case.offsets,
                                        C=self.c)
         host_c.copy_(self.c, non_blocking=True)
@@ -515,7 +523,7 @@ def run_ours(args):
     if not args.no_e2e:
         if args.workload == "experts":
             host_a = step.x.cpu().pin_memory()
-            host_w = None
+            host_w = step.rows.cpu().pin_memory()
             dev_a, dev_w = torch.empty_like(step.x), None
         elif args.workload == "wgrad":
             host_a, host_w = case.dy.cpu().pin_memory(), case.x.cpu().pin_memory()

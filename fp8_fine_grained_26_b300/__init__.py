@@ -23,6 +23,7 @@ FP8BS_ERR_ARG = -4
 FP8BS_ERR_LAUNCH = -5
 FP8BS_ERR_DEVICE = -6
 FP8BS_ERR_TIMEOUT = -7
+FP8BS_ERR_INDEX = -8
 OUT_BF16, OUT_FP32 = 0, 1
 B_KMAJOR, B_MNMAJOR = 0, 1
 
@@ -30,12 +31,13 @@ _STATUS_NAMES = {
     FP8BS_ERR_NULL: "FP8BS_ERR_NULL", FP8BS_ERR_SHAPE: "FP8BS_ERR_SHAPE",
     FP8BS_ERR_ALIGN: "FP8BS_ERR_ALIGN", FP8BS_ERR_ARG: "FP8BS_ERR_ARG",
     FP8BS_ERR_LAUNCH: "FP8BS_ERR_LAUNCH", FP8BS_ERR_DEVICE: "FP8BS_ERR_DEVICE",
-    FP8BS_ERR_TIMEOUT: "FP8BS_ERR_TIMEOUT",
+    FP8BS_ERR_TIMEOUT: "FP8BS_ERR_TIMEOUT", FP8BS_ERR_INDEX: "FP8BS_ERR_INDEX",
 }
 
 EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
             "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
-            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout")
+            "fp8_quant_act_1x128_gather", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
+            "fp8bs_selftest_wait_timeout")
 
 
 class Fp8bsError(RuntimeError):
@@ -56,6 +58,7 @@ def _load():
         "fp8_gemm_blockscaled": [p, p, p, p, i64, i64, i64, i32, p, i32, i64, p],
         "fp8_gemm_blockscaled_e4m3_out": [p, p, p, p, i64, i64, i64, i32, p, i64, p, p],
         "fp8_quant_tokens_1x128": [p, i64, i64, i64, p, i64, p, p],
+        "fp8_quant_act_1x128_gather": [p, i64, i64, i64, p, i64, p, i64, p, p],
         "fp8_gemm_wgrad": [p, p, p, p, i64, i64, i64, p, i32, i64, p],
         "fp8_grouped_gemm_blockscaled": [p, p, p, p, p, i32, i64, i64, i64, p, i32, i64, p],
         "fp8bs_last_error": [p],
@@ -212,6 +215,29 @@ def fp8_gemm_blockscaled_e4m3_out(qA, sA, qB, sB, b_major=B_KMAJOR, qC=None, sC=
     return qC, sC
 
 
+def fp8_quant_act_1x128_gather(x, rows, q=None, sA=None, stream=None):
+    """1x128 quantisation of the gathered rows ``x[rows]`` of a BF16 ``[T, K]``
+    matrix (``rows``: int32 CUDA tensor), without materialising them; returns
+    ``(q uint8 [M, K], sA float32 [K/128, M])`` with ``M = len(rows)``."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(rows, torch.int32, "rows", 1)
+    _row_major(x, "x")
+    if not rows.is_contiguous():
+        raise ValueError("rows must be contiguous")
+    T, K = x.shape
+    M = rows.numel()
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if sA is None:
+        sA = torch.empty((K // 128, M), dtype=torch.float32, device=x.device)
+    _row_major(q, "q")
+    ldx = x.stride(0) if T > 0 else K
+    ldq = q.stride(0) if M > 0 else K
+    _check(lib.fp8_quant_act_1x128_gather(_ptr(x), T, K, ldx, _ptr(rows), M, _ptr(q), ldq, _ptr(sA),
+                                          _stream(stream)), "fp8_quant_act_1x128_gather")
+    return q, sA
+
+
 def fp8_quant_tokens_1x128(x, qT=None, s=None, stream=None):
     """Quantise a BF16 ``[T, F]`` matrix per 1x128 run of tokens in each
     feature column; returns ``(qT uint8 [F, T], s float32 [T/128, F])``."""
@@ -286,6 +312,7 @@ def fp8bs_selftest_wait_timeout(limit_us=20000, stream=None):
 
 __all__ = ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
            "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
+           "fp8_quant_act_1x128_gather", "FP8BS_ERR_INDEX",
            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout",
            "Fp8bsError", "lib",
            "LIB_PATH", "EXPORTED", "B_KMAJOR", "B_MNMAJOR", "OUT_BF16", "OUT_FP32"]

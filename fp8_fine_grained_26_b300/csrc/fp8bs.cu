@@ -459,6 +459,32 @@ int fp8_gemm_blockscaled_e4m3_out(const void *qA, const float *sA, const void *q
     return launch_dense(dev, qA, sA, qB, sB, M, N, K, b_major, qC, FP8BS_OUT_BF16, ldqc, sC, stream);
 }
 
+int fp8_quant_act_1x128_gather(const void *x_bf16, int64_t T, int64_t K, int64_t ldx, const int32_t *rows,
+                               int64_t M, void *q_e4m3, int64_t ldq, float *sA, cudaStream_t stream)
+{
+    if (T < 0 || M < 0 || K < 0 || K % 128 != 0)
+        return FP8BS_ERR_SHAPE;
+    if (M == 0 || K == 0)
+        return FP8BS_OK;
+    if (!x_bf16 || !rows || !q_e4m3 || !sA)
+        return FP8BS_ERR_NULL;
+    if (ldx < K || ldq < K)
+        return FP8BS_ERR_SHAPE;
+    if (!aligned16(x_bf16) || !aligned16(q_e4m3) || !aligned4(sA) || !aligned4(rows) || (ldx * 2) % 16 != 0 ||
+        ldq % 16 != 0)
+        return FP8BS_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    const int64_t KB = K / 128;
+    const int64_t tasks = M * ((KB + GATHER_TILES - 1) / GATHER_TILES);
+    const int64_t blocks = std::min<int64_t>((tasks * 32 + GATHER_THREADS - 1) / GATHER_THREADS,
+                                             8 * (int64_t)dev->num_sms);
+    quant_act_gather_kernel<<<(unsigned)blocks, GATHER_THREADS, 0, stream>>>(
+        static_cast<const uint16_t *>(x_bf16), T, ldx, rows, M, KB, static_cast<uint8_t *>(q_e4m3), ldq, sA);
+    return launch_status();
+}
+
 int fp8_quant_tokens_1x128(const void *x_bf16, int64_t T, int64_t F, int64_t ldx, void *qT, int64_t ldq,
                            float *s, cudaStream_t stream)
 {
@@ -575,7 +601,7 @@ int fp8bs_last_error(cudaStream_t stream)
         const unsigned int zero = 0;
         if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero) != cudaSuccess)
             return FP8BS_ERR_LAUNCH;
-        return FP8BS_ERR_TIMEOUT;
+        return (word & 1u) ? FP8BS_ERR_TIMEOUT : FP8BS_ERR_INDEX;
     }
     return FP8BS_OK;
 }

@@ -405,6 +405,21 @@ __device__ __forceinline__ void st_v2(void *p, uint32_t a, uint32_t b)
     asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
 
+// Streaming store (cache-streaming: the line is not expected to be reused).
+__device__ __forceinline__ void st_v2_cs(void *p, uint32_t a, uint32_t b)
+{
+    asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+// Read-only 16-byte load with an L2 cache-policy hint.
+__device__ __forceinline__ uint4 ld_nc_v4_hint(const void *p, uint64_t policy)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(policy));
+    return v;
+}
+
 __device__ __forceinline__ void st_v4(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),

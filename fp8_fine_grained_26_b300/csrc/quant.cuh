@@ -316,6 +316,83 @@ __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_w_128x128_kernel(
     qdrain(r, j, issued);
 }
 
+// Gather + 1x128 activation quantisation for expert dispatch: output row i
+// is the quantisation of input row rows[i] (the token routed to that expert
+// slot).  Quantising then gathering equals gathering then quantising, so
+// the codes and scales equal fp8_quant_act_1x128 of the gathered BF16
+// matrix, without materialising it.  The rows are arbitrary, so the loads
+// are plain read-only 16-byte loads, kept in L2 (each token row is read once
+// per routed copy); the codes are streamed out.  A warp takes one output row
+// and eight consecutive 1x128 tiles, four per half-warp; every lane issues
+// its four loads before any use.  An index outside [0, T) is not read: the
+// row encodes as zeros with a zero scale and bit 1 of the error word is set.
+// (A version staging 16-row units through bulk copies into a shared-memory
+// ring measured slower.)
+constexpr int GATHER_THREADS = 256;
+constexpr int GATHER_TILES = 8;                                  // tiles per warp task
+
+__global__ void __launch_bounds__(GATHER_THREADS) quant_act_gather_kernel(
+    const uint16_t *__restrict__ x, int64_t T, int64_t ldx, const int32_t *__restrict__ rows, int64_t M,
+    int64_t KB, uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ sA)
+{
+    const int lane = threadIdx.x & 31;
+    const int half = lane >> 4;
+    const int l16 = lane & 15;
+    const int hbase = lane & 16;
+    const uint64_t keep = ptx::policy_evict_last();
+    const int64_t chunks = (KB + GATHER_TILES - 1) / GATHER_TILES;
+    const int64_t tasks = M * chunks;
+    const int64_t warp0 = ((int64_t)blockIdx.x * GATHER_THREADS + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * GATHER_THREADS) >> 5;
+    for (int64_t task = warp0; task < tasks; task += nwarps) {
+        const int64_t i = task / chunks;
+        const int64_t kb0 = (task - i * chunks) * GATHER_TILES;
+        const int32_t src = rows[i];
+        const bool valid = src >= 0 && (int64_t)src < T;
+        if (!valid && lane == 0)
+            atomicOr(&g_error_word, 2u);
+        constexpr int TPH = GATHER_TILES / 2;                     // tiles per half-warp
+        uint4 v[TPH];
+#pragma unroll
+        for (int t = 0; t < TPH; ++t) {
+            const int64_t kb = kb0 + 2 * t + half;
+            v[t] = make_uint4(0u, 0u, 0u, 0u);
+            if (valid && kb < KB)
+                v[t] = ptx::ld_nc_v4_hint(x + (int64_t)src * ldx + kb * 128 + l16 * 8, keep);
+        }
+        // amax of each of the half-warp's tiles, known to all its 16 lanes
+        uint32_t am[TPH];
+#pragma unroll
+        for (int t = 0; t < TPH; ++t) {
+            uint32_t a = absmax_bits8(v[t]);
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1)
+                a = max(a, __shfl_xor_sync(0xffffffffu, a, o, 16));
+            am[t] = a;
+        }
+        // lane t of the half-warp forms tile t's divisor; the others fetch it
+        uint32_t mine = am[0];
+#pragma unroll
+        for (int t = 1; t < TPH; ++t)
+            mine = (l16 & (TPH - 1)) == t ? am[t] : mine;
+        const Divisor dm = make_divisor(mine);
+#pragma unroll
+        for (int t = 0; t < TPH; ++t) {
+            const int64_t kb = kb0 + 2 * t + half;
+            Divisor d;
+            d.s = __shfl_sync(0xffffffffu, dm.s, hbase + t);
+            d.r = __shfl_sync(0xffffffffu, dm.r, hbase + t);
+            d.mode = divisor_mode(am[t]);
+            if (kb < KB) {
+                const uint2 c = quant_8(v[t], d);
+                ptx::st_v2_cs(q + i * ldq + kb * 128 + l16 * 8, c.x, c.y);
+                if (l16 == 0)
+                    sA[kb * M + i] = d.s;
+            }
+        }
+    }
+}
+
 // Token-dimension quantiser (the weight-gradient GEMM's operands): X is
 // [T][F] (features contiguous); every feature column is cut into runs of 128
 // tokens, each quantised with the 1x128 rule, and the codes are written

@@ -59,7 +59,8 @@ typedef enum {
     FP8BS_ERR_ARG = -4,         /* an enum value is out of range, or bad offsets size */
     FP8BS_ERR_LAUNCH = -5,      /* the CUDA runtime refused a launch                  */
     FP8BS_ERR_DEVICE = -6,      /* the current device is not sm_103                   */
-    FP8BS_ERR_TIMEOUT = -7      /* (fp8bs_last_error only) a device-side wait timed out */
+    FP8BS_ERR_TIMEOUT = -7,     /* (fp8bs_last_error only) a device-side wait timed out */
+    FP8BS_ERR_INDEX = -8        /* (fp8bs_last_error only) a device-side row index was out of range */
 } fp8bs_status;
 
 enum { FP8BS_OUT_BF16 = 0, FP8BS_OUT_FP32 = 1 };
@@ -139,6 +140,25 @@ int fp8_gemm_blockscaled_e4m3_out(const void *qA, const float *sA, const void *q
                                   float *sC, cudaStream_t stream);
 
 /*
+ * Gather + 1x128 activation quantisation, for routed-expert dispatch: output
+ * row i is the 1x128 quantisation of input row rows[i].  The pages dispatch
+ * activations to experts in FP8 ("DeepSeek-V3 training walkthrough", section
+ * 二(四), last item; qqstock.cn walkthrough, FP8 section, report figure 10);
+ * since quantising then gathering rows equals gathering then quantising, the
+ * result is bit-identical to fp8_quant_act_1x128 of the gathered BF16 matrix
+ * x[rows], which is never materialised.
+ *   x_bf16 : [T][K] BF16 token rows, row stride ldx (elements).
+ *   rows   : [M] int32 on the device, each in [0, T).
+ *   q_e4m3 : [M][K] E4M3, row stride ldq (bytes); sA : [K/128][M] FP32.
+ * K a multiple of 128.  An index outside [0, T) produces zero codes and zero
+ * scales for that row and makes the next fp8bs_last_error report
+ * FP8BS_ERR_INDEX.  Alignment rules as fp8_quant_act_1x128 (rows 4-byte
+ * aligned).
+ */
+int fp8_quant_act_1x128_gather(const void *x_bf16, int64_t T, int64_t K, int64_t ldx, const int32_t *rows,
+                               int64_t M, void *q_e4m3, int64_t ldq, float *sA, cudaStream_t stream);
+
+/*
  * Token-dimension 1x128 quantisation, for the operands of the weight-gradient
  * GEMM dW = dY^T . X, whose contraction runs over tokens.  The pages run all
  * three GEMM kinds (forward, data gradient, weight gradient) in FP8 with
@@ -198,7 +218,8 @@ int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA,
 
 /*
  * Synchronises `stream`, then reports and clears the current device's error
- * word: FP8BS_OK, FP8BS_ERR_TIMEOUT (a kernel's pipeline wait exceeded its
+ * word: FP8BS_OK, FP8BS_ERR_INDEX (a gather index was out of range),
+ * FP8BS_ERR_TIMEOUT (a kernel's pipeline wait exceeded its
  * time limit; that kernel's outputs are incomplete), or FP8BS_ERR_LAUNCH (the
  * CUDA runtime reported an error for the stream).
  */

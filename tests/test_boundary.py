@@ -22,7 +22,8 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
         "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
-        "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout"])
+        "fp8_quant_act_1x128_gather", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
+        "fp8bs_selftest_wait_timeout"])
 
 
 def test_library_loads_and_exports_every_declared_symbol():
@@ -125,6 +126,17 @@ def test_token_quantiser_and_wgrad_reject_bad_arguments():
     assert w(P(16), P(16), P(16), P(16), 4, 4, 128, P(16), 5, 8, P(0)) == -4     # c_dtype
     assert w(P(0), P(16), P(16), P(16), 4, 4, 128, P(16), 0, 8, P(0)) == -1      # NULL
     assert w(P(16), P(16), P(16), P(16), 0, 4, 128, P(16), 0, 8, P(0)) == 0      # M == 0
+
+
+def test_gather_quantiser_rejects_bad_arguments():
+    lib = _raw()
+    g = lib.fp8_quant_act_1x128_gather
+    assert g(P(16), 8, 100, 128, P(16), 4, P(16), 128, P(16), P(0)) == -2    # K % 128
+    assert g(P(16), 8, 128, 128, P(16), 0, P(16), 128, P(16), P(0)) == 0     # M == 0
+    assert g(P(16), 8, 128, 128, P(0), 4, P(16), 128, P(16), P(0)) == -1     # NULL rows
+    assert g(P(16), 8, 128, 64, P(16), 4, P(16), 128, P(16), P(0)) == -2     # ldx < K
+    assert g(P(16), 8, 128, 128, P(18), 4, P(16), 128, P(16), P(0)) == -3    # rows align
+    assert g(P(16), 8, 128, 132, P(16), 4, P(16), 128, P(16), P(0)) == -3    # ldx * 2 % 16
 
 
 def test_selftest_rejects_out_of_range_limits():

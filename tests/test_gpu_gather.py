@@ -1,0 +1,58 @@
+"""Fused gather + 1x128 quantisation (expert dispatch) on the GPU: bit-exact
+against the oracle quantising the gathered BF16 rows, equal to the GPU
+quantiser on the gathered matrix, and an out-of-range index reported as
+FP8BS_ERR_INDEX by the kernel's own bounds check (no out-of-bounds access)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from parity import host_u8
+from synthetic import bf16_bits, generator, normal_bf16
+
+pytestmark = pytest.mark.gpu
+fp8 = pytest.importorskip("fp8_fine_grained_26_b300")
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("T,K,M", [(64, 128, 100), (300, 384, 777), (50, 1152, 64), (4096, 7168, 256)])
+def test_gather_quantiser_matches_oracle(T, K, M):
+    g = generator(T + K + M, DEV)
+    x = normal_bf16((T, K), 1.0, g, DEV, outlier_p=0.003, outlier_scale=50.0)
+    x[3 % T] = 0
+    rows = torch.randint(0, T, (M,), generator=g, device=DEV, dtype=torch.int64).to(torch.int32)
+    rows[0] = 3 % T
+    q, s = fp8.fp8_quant_act_1x128_gather(x, rows)
+    assert fp8.fp8bs_last_error() == 0
+    xg = bf16_bits(x)[rows.cpu().numpy()]
+    oq, os_ = oracle.quant_act_1x128(xg)
+    assert np.array_equal(host_u8(q), oq)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+    q2, s2 = fp8.fp8_quant_act_1x128(x.index_select(0, rows.long()))
+    torch.cuda.synchronize()
+    assert torch.equal(q, q2) and torch.equal(s.view(torch.int32), s2.view(torch.int32))
+
+
+def test_gather_quantiser_experts_dispatch():
+    case = synthetic.experts(device=DEV, keep_x=True)
+    rows = case.token_of_row.to(torch.int32)
+    q, s = fp8.fp8_quant_act_1x128_gather(case.x, rows)
+    q2, s2 = fp8.fp8_quant_act_1x128(case.x_sorted)
+    assert fp8.fp8bs_last_error() == 0
+    assert torch.equal(q, q2) and torch.equal(s.view(torch.int32), s2.view(torch.int32))
+
+
+def test_gather_quantiser_bad_index_is_reported():
+    g = generator(9, DEV)
+    x = normal_bf16((32, 256), 1.0, g, DEV)
+    rows = torch.tensor([0, 5, 32, -1, 7], dtype=torch.int32, device=DEV)   # 32 and -1 are out of range
+    q = torch.full((5, 256), 0x33, dtype=torch.uint8, device=DEV)
+    s = torch.full((2, 5), 9.0, dtype=torch.float32, device=DEV)
+    fp8.fp8_quant_act_1x128_gather(x, rows, q=q, sA=s)
+    assert fp8.fp8bs_last_error() == fp8.FP8BS_ERR_INDEX
+    assert fp8.fp8bs_last_error() == fp8.FP8BS_OK
+    assert torch.all(q[2] == 0) and torch.all(q[3] == 0) and torch.all(s[:, 2:4] == 0)
+    q2, s2 = fp8.fp8_quant_act_1x128(x.index_select(0, torch.tensor([0, 5, 7], device=DEV)))
+    torch.cuda.synchronize()
+    assert torch.equal(q[[0, 1, 4]], q2) and torch.equal(s[:, [0, 1, 4]], s2)
