@@ -29,6 +29,9 @@ struct DeviceInfo {
 };
 
 constexpr int PAIR_STAGES = 4;      // 4 x 32 KiB operand stages per CTA of a pair
+#ifndef PAIR_M_GROUP
+#define PAIR_M_GROUP 16             // M-pairs (256 rows each) per tile rasterisation group
+#endif
 
 std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
@@ -279,6 +282,11 @@ int launch_dense(DeviceInfo *dev, const void *qA, const float *sA, const void *q
     g.KB = (int)(K / BK);
     g.NB128 = (int)((N + 127) / 128);
     g.num_m_pair = (g.num_m_blk + 1) / 2;
+    {
+        // rasterisation groups of at most PAIR_M_GROUP M-pairs, equal-sized
+        const int ngroups = (g.num_m_pair + PAIR_M_GROUP - 1) / PAIR_M_GROUP;
+        g.m_group = (g.num_m_pair + ngroups - 1) / ngroups;
+    }
     if (pair) {
         g.num_tiles = (int64_t)g.num_m_pair * g.num_n_blk;
         cudaLaunchConfig_t cfg = {};

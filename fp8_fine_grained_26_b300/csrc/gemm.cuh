@@ -105,6 +105,7 @@ struct GemmArgs {
     float *sC;          // E4M3 output: [N/128][M] scales of the 1x128 output tiles
     int num_m_blk;      // dense: ceil(M/128)
     int num_m_pair;     // dense, cluster pairs: ceil(num_m_blk / 2)
+    int m_group;        // dense, cluster pairs: M-pairs per rasterisation group
     int num_n_blk;      // ceil(N/256)
     int KB;             // K/128
     int NB128;          // ceil(N/128)
@@ -218,9 +219,16 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &g, const SharedState<S, 
     } else if constexpr (PAIR) {
         // work unit = one 256 x 256 tile of a CTA pair; CTA `rank` owns its
         // M-block 2 * pair + rank (a block past the last one computes on zero
-        // rows and stores nothing)
-        const int64_t nb = t / g.num_m_pair;
-        tl.m0 = (2 * (t - nb * g.num_m_pair) + rank) * BM;
+        // rows and stores nothing).  Tiles are rasterised in groups of
+        // m_group M-pairs: within a group the M-pairs vary fastest, then the
+        // N-blocks, so the group's A rows stay in L2 while B streams once
+        // per group instead of A being re-read for every N-block.
+        const int64_t per_group = (int64_t)g.m_group * g.num_n_blk;
+        const int64_t grp = t / per_group;
+        const int64_t local = t - grp * per_group;
+        const int64_t gsize = min((int64_t)g.m_group, (int64_t)g.num_m_pair - grp * g.m_group);
+        const int64_t nb = local / gsize;
+        tl.m0 = (2 * (grp * g.m_group + (local - nb * gsize)) + rank) * BM;
         tl.m_end = g.M;
         tl.n0 = (int32_t)(nb * BN);
         tl.expert = 0;
