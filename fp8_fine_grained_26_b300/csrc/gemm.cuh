@@ -650,6 +650,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const Tile tl = tile_at<GROUPED, PAIR>(g, ss, t, rank);
             const int64_t gm = tl.m0 + row;
             const bool row_ok = gm < tl.m_end;
+            // grouped: a warp whose 32 rows all lie past the expert's segment
+            // (the padding of a partial M-block) skips its TMEM reads and FMAs
+            const bool warp_live = !GROUPED || tl.m0 + quarter * 32 < tl.m_end;
             float2 acc2[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j)
@@ -676,14 +679,16 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 // two 64-column TMEM round trips; the buffer is released as
                 // soon as the second one has landed in registers
                 uint32_t r[64];
-                ptx::tmem_ld_32x32b_x64(taddr, r);
-                ptx::tmem_ld_wait(r);
-                if constexpr (TOK)
-                    promote64_cols(acc2, r, sa, col_scales);
-                else
-                    promote64(acc2, r, scale);
-                ptx::tmem_ld_32x32b_x64(taddr + 64, r);
-                ptx::tmem_ld_wait(r);
+                if (warp_live) {
+                    ptx::tmem_ld_32x32b_x64(taddr, r);
+                    ptx::tmem_ld_wait(r);
+                    if constexpr (TOK)
+                        promote64_cols(acc2, r, sa, col_scales);
+                    else
+                        promote64(acc2, r, scale);
+                    ptx::tmem_ld_32x32b_x64(taddr + 64, r);
+                    ptx::tmem_ld_wait(r);
+                }
                 ptx::tc_fence_before();
                 __syncwarp();                            // the warp's partial is in registers
                 if constexpr (PAIR)
@@ -693,7 +698,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 if constexpr (TOK) {
                     promote64_cols(acc2 + 32, r, sa, col_scales + 4 * 64);
                     ptx::mbar_arrive(ss.sfree(slot));    // the column scales have been read
-                } else {
+                } else if (warp_live) {
                     promote64(acc2 + 32, r, scale);
                 }
             }
