@@ -240,25 +240,35 @@ class DenseStep:
             self.fp8.fp8_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major,
                                           C=self.c)
 
-    def run_host(self, host_a, host_w, host_c, dev_a, dev_w):
-        """End-to-end step from pinned host buffers through the C-ABI calls:
-        A is copied and quantised on the side stream while W is copied and
-        quantised on the step's stream."""
+    # ---- end-to-end interface (see run_e2e): inputs on the host, outputs back
+    def host_inputs(self):
+        return [self.case.a.cpu().pin_memory(), self.case.w.cpu().pin_memory()]
+
+    def out_buffers(self):
+        outs = [torch_empty_like(self.torch, self.c)]
+        if self.sc is not None:
+            outs.append(torch_empty_like(self.torch, self.sc))
+        return outs
+
+    def compute(self, dev_in, outs):
+        """The whole path on device inputs [a, w] into outs [c (, sc)]: A is
+        quantised on the side stream while W is quantised on this stream."""
+        a, w = dev_in
         f, torch = self.fp8, self.torch
         main = torch.cuda.current_stream()
         self.side.wait_stream(main)
         with torch.cuda.stream(self.side):
-            dev_a.copy_(host_a, non_blocking=True)
-            f.fp8_quant_act_1x128(dev_a, self.qa, self.sa, stream=self.side)
-        dev_w.copy_(host_w, non_blocking=True)
-        f.fp8_quant_w_128x128(dev_w, self.qb, self.sb)
+            f.fp8_quant_act_1x128(a, self.qa, self.sa, stream=self.side)
+        f.fp8_quant_w_128x128(w, self.qb, self.sb)
         main.wait_stream(self.side)
-        self._gemm()
         if self.e4m3_out == "unfused":
-            f.fp8_quant_act_1x128(self.c16, self.c, self.sc)
-        host_c.copy_(self.c, non_blocking=True)
-        if self.sc is not None:
-            self.host_sc.copy_(self.sc, non_blocking=True)
+            f.fp8_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major, C=self.c16)
+            f.fp8_quant_act_1x128(self.c16, outs[0], outs[1])
+        elif self.e4m3_out:
+            f.fp8_gemm_blockscaled_e4m3_out(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major,
+                                            qC=outs[0], sC=outs[1])
+        else:
+            f.fp8_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major, C=outs[0])
 
 
 class WgradStep:
@@ -310,18 +320,22 @@ class WgradStep:
         f.fp8_gemm_wgrad(self.qa, self.sa, self.qb, self.sb, C=self.c)
         if events: events[5].record(main)
 
-    def run_host(self, host_a, host_w, host_c, dev_a, dev_w):
+    def host_inputs(self):
+        return [self.case.dy.cpu().pin_memory(), self.case.x.cpu().pin_memory()]
+
+    def out_buffers(self):
+        return [torch_empty_like(self.torch, self.c)]
+
+    def compute(self, dev_in, outs):
+        dy, x = dev_in
         f, torch = self.fp8, self.torch
         main = torch.cuda.current_stream()
         self.side.wait_stream(main)
         with torch.cuda.stream(self.side):
-            dev_a.copy_(host_a, non_blocking=True)
-            f.fp8_quant_tokens_1x128(dev_a, self.qa, self.sa, stream=self.side)
-        dev_w.copy_(host_w, non_blocking=True)
-        f.fp8_quant_tokens_1x128(dev_w, self.qb, self.sb)
+            f.fp8_quant_tokens_1x128(dy, self.qa, self.sa, stream=self.side)
+        f.fp8_quant_tokens_1x128(x, self.qb, self.sb)
         main.wait_stream(self.side)
-        f.fp8_gemm_wgrad(self.qa, self.sa, self.qb, self.sb, C=self.c)
-        host_c.copy_(self.c, non_blocking=True)
+        f.fp8_gemm_wgrad(self.qa, self.sa, self.qb, self.sb, C=outs[0])
 
 
 class ExpertsStep:
@@ -371,14 +385,74 @@ class ExpertsStep:
                                        C=self.c)
         if events: events[3].record()
 
-    def run_host(self, host_a, host_w, host_c, dev_a, dev_w):
-        dev_a.copy_(host_a, non_blocking=True)
-        self.rows.copy_(host_w, non_blocking=True)   # the routed rows come with the tokens
+    def host_inputs(self):
+        # the token rows and the routed row list come from the host every step
+        return [self.x.cpu().pin_memory(), self.rows.cpu().pin_memory()]
+
+    def out_buffers(self):
+        return [torch_empty_like(self.torch, self.c)]
+
+    def compute(self, dev_in, outs):
+        x, rows = dev_in
         f = self.fp8
-        f.fp8_quant_act_1x128_gather(dev_a, self.rows, self.qa, self.sa)
-        f.fp8_grouped_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, self.case.offsets,
-                                       C=self.c)
-        host_c.copy_(self.c, non_blocking=True)
+        f.fp8_quant_act_1x128_gather(x, rows, self.qa, self.sa)
+        f.fp8_grouped_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, self.case.offsets, C=outs[0])
+
+
+def torch_empty_like(torch, t):
+    return torch.empty(tuple(t.shape), dtype=t.dtype, device=t.device)
+
+
+def run_e2e(step, n, torch):
+    """End to end through the C-ABI calls, inputs from pinned host memory and
+    the result back to pinned host memory, every step.  Consecutive steps are
+    pipelined on three streams with double-buffered device inputs and outputs:
+    step i+1's host->device copy and step i-1's device->host copy overlap
+    step i's kernels (the PCIe link carries both directions at once).
+    Returns the time per step in ms (first copy in to last copy out)."""
+    host_in = step.host_inputs()
+    dev_in = [[torch.empty(tuple(h.shape), dtype=h.dtype, device="cuda") for h in host_in] for _ in range(2)]
+    outs = [step.out_buffers() for _ in range(2)]
+    host_out = [[torch.empty(tuple(o.shape), dtype=o.dtype).pin_memory() for o in outs[b]] for b in range(2)]
+    main = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def loop(count):
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        for b in range(2):
+            ev_comp[b].record(main)
+            ev_out[b].record(main)
+        s_in.wait_stream(main)
+        s_out.wait_stream(main)
+        for i in range(count):
+            b = i % 2
+            s_in.wait_event(ev_comp[b])            # step i-2's kernels have read dev_in[b]
+            with torch.cuda.stream(s_in):
+                for d, h in zip(dev_in[b], host_in):
+                    d.copy_(h, non_blocking=True)
+            ev_in[b].record(s_in)
+            main.wait_event(ev_in[b])
+            main.wait_event(ev_out[b])             # step i-2's result has left outs[b]
+            step.compute(dev_in[b], outs[b])
+            ev_comp[b].record(main)
+            s_out.wait_event(ev_comp[b])
+            with torch.cuda.stream(s_out):
+                for h, d in zip(host_out[b], outs[b]):
+                    h.copy_(d, non_blocking=True)
+            ev_out[b].record(s_out)
+        main.wait_stream(s_out)
+        main.wait_stream(s_in)
+
+    loop(2)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    loop(n)
+    e1.record(main)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -521,36 +595,13 @@ def run_ours(args):
     # ---- end-to-end through the same C-ABI calls from pinned host buffers
     e2e = None
     if not args.no_e2e:
-        if args.workload == "experts":
-            host_a = step.x.cpu().pin_memory()
-            host_w = step.rows.cpu().pin_memory()
-            dev_a, dev_w = torch.empty_like(step.x), None
-        elif args.workload == "wgrad":
-            host_a, host_w = case.dy.cpu().pin_memory(), case.x.cpu().pin_memory()
-            dev_a, dev_w = torch.empty_like(case.dy), torch.empty_like(case.x)
-        else:
-            host_a = case.a.cpu().pin_memory()
-            host_w = case.w.cpu().pin_memory()
-            dev_a, dev_w = torch.empty_like(case.a), torch.empty_like(case.w)
-        host_c = torch.empty(tuple(step.c.shape), dtype=step.c.dtype).pin_memory()
-        if getattr(step, "sc", None) is not None:
-            step.host_sc = torch.empty(tuple(step.sc.shape), dtype=step.sc.dtype).pin_memory()
-        for _ in range(2):
-            step.run_host(host_a, host_w, host_c, dev_a, dev_w)
-        torch.cuda.synchronize()
         n_e2e = max(3, min(args.steps, 20))
         barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(n_e2e):
-            step.run_host(host_a, host_w, host_c, dev_a, dev_w)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device) / n_e2e
+        e2e_ms = max_over_ranks(run_e2e(step, n_e2e, torch), world, device)
         e2e = {"value": round(world * step.flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                "ms_per_step": round(e2e_ms, 4), "steps": n_e2e,
-               "h2d_bytes_per_step": int(step.h2d_bytes), "d2h_bytes_per_step": int(step.d2h_bytes)}
+               "h2d_bytes_per_step": int(step.h2d_bytes), "d2h_bytes_per_step": int(step.d2h_bytes),
+               "pipelining": "copy in / kernels / copy out of consecutive steps overlap (3 streams)"}
 
     # ---- roofline of the dominant kernel (the GEMM) and the quantisers
     # The GEMM is timed inside a long run of steps (power-capped clocks), so
