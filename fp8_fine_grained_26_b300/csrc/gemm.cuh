@@ -63,6 +63,7 @@ constexpr int SCALE_SLOTS = 8;                           // slices of scales sta
 constexpr int SCALE_SLOT_FLOATS = 132;                   // 128 row scales + 2 column-block scales (+pad)
 constexpr int SCALE_SLOT_FLOATS_TOK = 384;               // weight gradient: 128 row + 256 column scales
 constexpr int SCALE_LOOKAHEAD = 2;                       // loader copy groups in flight
+constexpr uint64_t ABORT_GRACE_NS = 1000000;              // pair kernel: wait after an abort (1 ms)
 constexpr int B_PREFETCH_SLICES = 2;                     // grouped: L2 prefetch distance of expert weights
 
 // Shared-memory layout for S pipeline stages of BSB bytes of B each
@@ -779,10 +780,20 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
 
     ptx::tc_fence_before();
-    if constexpr (PAIR)
-        ptx::cluster_sync();                         // the pair's MMAs, copies and signals are done
-    else
+    if constexpr (PAIR) {
+        // After an abort, the second CTA's last copies complete on the
+        // leader's barriers, which no one waits for any more: give any copy
+        // still in flight time to land before either CTA of the pair exits.
         __syncthreads();
+        if (*ss.abort_flag()) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (ptx::globaltimer_ns() - t0 < ABORT_GRACE_NS) {
+            }
+        }
+        ptx::cluster_sync();                         // the pair's MMAs, copies and signals are done
+    } else {
+        __syncthreads();
+    }
     if (warp == 1) {
         ptx::tc_fence_after();
         if constexpr (PAIR)
