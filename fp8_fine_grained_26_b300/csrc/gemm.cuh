@@ -25,14 +25,15 @@
 //               release the TMEM buffer so the MMA of slice kb+2 can start
 //               while slice kb+1 is promoted.  After the last slice each
 //               warpgroup rounds its 128 x 128 block to BF16 into two
-//               128-row, 128-byte-swizzled staging boxes and one thread issues
-//               the two TMA stores (rows >= M and columns >= N are clipped by
-//               the tensor map); FP32 outputs, unaligned row strides and the
-//               rows of a grouped tile that reach past the expert's segment
-//               are stored directly, masked.
+//               128-row, 128-byte-swizzled staging boxes and goes on to the
+//               next tile; FP32 outputs, unaligned row strides and the rows
+//               of a grouped tile that reach past the expert's segment are
+//               stored directly, masked.
 //   warp 2      scale loader: copies each slice's row and column-block
 //               scales into a shared ring ahead of the promote warps.
-//   warp 3      idle.
+//   warp 3      store issuer: issues the TMA stores of the staged boxes
+//               (rows >= M and columns >= N are clipped by the tensor map)
+//               and hands the boxes back once the stores have read them.
 // CTA pairs (PAIR, dense GEMMs of two or more M-blocks): a 2-CTA cluster
 // computes a 256 x 256 tile with tcgen05 cta_group::2 MMAs (M = 256).  Each
 // CTA stages only its own 128 rows of A and half (128 rows) of the B block,
@@ -244,6 +245,16 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &g, const SharedState<S, 
     return tl;
 }
 
+// Whether a warpgroup's 128 x 128 output block of tile `tl` goes out through
+// the staged boxes and TMA stores: a block with columns inside N and rows
+// inside the tile's range, where the tensor map clips rows at M but a grouped
+// tile may not write past its expert's segment.  The promote warps and the
+// store issuer take the same decision from this one predicate.
+__device__ __forceinline__ bool epi_uses_boxes(const GemmArgs &g, const Tile &tl, int64_t n_first)
+{
+    return g.c_tma && n_first < g.N && tl.m0 < tl.m_end && (tl.m0 + BM <= tl.m_end || tl.m_end == g.M);
+}
+
 // Grouped: per-expert tile counts ceil(n_e / 128) * num_n_blk, exclusive
 // prefix over experts into shared memory.  Offsets are clamped into
 // [0, M_total] and made nondecreasing, so malformed offsets cannot move any
@@ -411,7 +422,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             ptx::mbar_init(ss.sfree(j), 256);          // every promote thread
         }
         for (int wg = 0; wg < 2; ++wg) {
-            ptx::mbar_init(ss.epi_free(wg), 1);        // the warpgroup's store issuer
+            ptx::mbar_init(ss.epi_free(wg), 1);        // the store issuer (warp 3)
             ptx::mbar_init(ss.epi_full(wg), 4);        // one arrive per warp
         }
         *ss.abort_flag() = 0u;
@@ -456,7 +467,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             // L2 policy: A row blocks are re-read by the tiles of later
             // N-blocks (keep them); dense B column blocks are shared by the
             // concurrently running M-tiles (default policy); an expert's
-            // weights are not needed again once its tiles are done.
+            // weight slice is read once more by each later M-block of the
+            // expert, which runs on a neighbouring CTA a little later (keep
+            // it), and is not needed again after its last M-block (evict
+            // first).
             const uint64_t keep = ptx::policy_evict_last();
             const uint64_t stream = ptx::policy_evict_first();
             // Grouped: the expert weights stream from HBM once, so the shared-
@@ -504,7 +518,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     ptx::mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
                     ptx::tma_load_2d_hint(sa, &tmA, fb, kb * BK, (int32_t)tl.m0, keep);
                     if constexpr (GROUPED) {
-                        ptx::tma_load_3d_hint(sb, &tmB, fb, kb * BK, tl.n0, tl.expert, stream);
+                        ptx::tma_load_3d_hint(sb, &tmB, fb, kb * BK, tl.n0, tl.expert,
+                                              tl.m0 + BM < tl.m_end ? keep : stream);
                         if (pf_t < ntiles) {
                             ptx::tma_prefetch_3d(&tmB, pf_kb * BK, pf_tl.n0, pf_tl.expert);
                             if (++pf_kb == g.KB) {
@@ -635,7 +650,36 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             while (done < sit)
                 publish(done++);
         }
-        __syncwarp();                                // warp 3 has no role
+        if (warp == 3 && lane == 0 && g.c_tma) {
+            // -------------------------------------------- output store issuer
+            // A warpgroup signals epi_full once its four warps have staged
+            // their rows; this thread issues the tile's TMA stores and
+            // returns the boxes (epi_free) when the stores have read them,
+            // so no promote warp waits on another warp's epilogue.
+            const uint64_t c_policy = ptx::policy_evict_first();   // C is written once, never re-read
+            ptx::mbar_arrive(ss.epi_free(0));                      // the boxes start free
+            ptx::mbar_arrive(ss.epi_free(1));
+            uint32_t eit[2] = {0u, 0u};
+            bool ok = true;
+            for (int64_t t = t_first; ok && t < ntiles; t += t_stride) {
+                const Tile tl = tile_at<GROUPED, PAIR>(g, ss, t, rank);
+                for (int wg = 0; wg < 2; ++wg) {
+                    const int64_t n_first = tl.n0 + wg * 128;
+                    if (!epi_uses_boxes(g, tl, n_first))
+                        continue;
+                    if (!wait_bounded(ss, ss.epi_full(wg), eit[wg]++ & 1u)) { ok = false; break; }
+                    ptx::tma_store_2d_hint(&tmC, ss.epi_box(wg, 0), (int32_t)n_first, (int32_t)tl.m0, c_policy);
+                    if (!QOUT && n_first + 64 < g.N)       // second 64-column BF16 box exists
+                        ptx::tma_store_2d_hint(&tmC, ss.epi_box(wg, 1), (int32_t)(n_first + 64), (int32_t)tl.m0,
+                                               c_policy);
+                    ptx::bulk_commit();
+                    ptx::bulk_wait_read_all();
+                    ptx::mbar_arrive(ss.epi_free(wg));
+                }
+            }
+            ptx::bulk_wait_all();                        // every store has completed before exit
+        }
+        __syncwarp();
     } else {
         ptx::setmaxnreg_inc<224>();
         // ------------------------------------------------ promote + epilogue
@@ -643,8 +687,6 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const int quarter = warp & 3;                // TMEM lane quarter
         const int row = quarter * 32 + lane;         // tile row owned by this thread
         const int col_half = wg * 128;
-        const uint64_t c_policy = ptx::policy_evict_first();   // C is written once, never re-read
-        const bool issuer = quarter == 0 && lane == 0;     // the warpgroup's store issuer
         uint32_t pit = 0, eit = 0;
         bool ok = true;
         for (int64_t t = t_first; ok && t < ntiles; t += t_stride) {
@@ -709,19 +751,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const int64_t n_first = tl.n0 + col_half;
             if (n_first >= g.N || tl.m0 >= tl.m_end)
                 continue;                                // uniform over the warpgroup
-            // TMA clips rows at M; a grouped tile may not write past its segment.
-            const bool wg_tma = g.c_tma && (tl.m0 + BM <= tl.m_end || tl.m_end == g.M);
-            if (wg_tma) {
+            if (epi_uses_boxes(g, tl, n_first)) {
                 // Stage both 64-column halves as 128-row, 128-byte-swizzled
-                // boxes shared by the warpgroup's four warps, then one thread
-                // issues the two TMA stores.  The hand-offs are mbarriers with
-                // bounded waits, so an aborting warp cannot strand the others.
+                // boxes shared by the warpgroup's four warps; warp 3 issues
+                // the TMA stores.  The hand-offs are mbarriers with bounded
+                // waits, so an aborting warp cannot strand the others.
                 const uint32_t ph = eit & 1u;
                 ++eit;
-                if (issuer) {
-                    ptx::bulk_wait_read_all();              // the previous tile's stores read the boxes
-                    ptx::mbar_arrive(ss.epi_free(wg));
-                }
                 if constexpr (QOUT) {
                     // The thread's 128 columns are exactly one 1x128 tile of
                     // its row: round to BF16, take the amax of the magnitude
@@ -759,23 +795,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         }
                     }
                 }
-                ptx::fence_proxy_async_smem();
+                ptx::fence_proxy_async_smem();           // the boxes are visible to the TMA stores
                 __syncwarp();
                 ptx::mbar_arrive_cluster_if(ss.epi_full(wg), lane == 0);
-                if (issuer) {
-                    if (!wait_bounded(ss, ss.epi_full(wg), ph)) { ok = false; break; }
-                    ptx::tma_store_2d_hint(&tmC, ss.epi_box(wg, 0), (int32_t)n_first, (int32_t)tl.m0, c_policy);
-                    if (!QOUT && n_first + 64 < g.N)       // second 64-column BF16 box exists
-                        ptx::tma_store_2d_hint(&tmC, ss.epi_box(wg, 1), (int32_t)(n_first + 64), (int32_t)tl.m0,
-                                               c_policy);
-                    ptx::bulk_commit();
-                }
             } else if (row_ok) {
                 store_row_direct(g, acc2, gm, n_first);
             }
         }
-        if (lane == 0)
-            ptx::bulk_wait_all();
         __syncwarp();
     }
 
