@@ -155,14 +155,16 @@ def make_workload(name, device):
 
 
 class DenseStep:
-    """quant_act(A) || quant_w(W) -> GEMM, over rotating input sets (> 2x L2).
+    """quantise A and W -> GEMM, over rotating input sets (> 2x L2).
 
-    The two quantisations are independent: the activation's runs on a side
-    stream forked from the step's stream, concurrently with the weight's, and
-    the GEMM waits for both."""
+    quant "pair": both operands in one launch (fp8_quant_act_w).  quant
+    "split": the two single-operand quantisers, the activation's on a side
+    stream forked from the step's stream, concurrently with the weight's; the
+    GEMM waits for both."""
 
-    def __init__(self, case, fp8, torch, e4m3_out=None):
+    def __init__(self, case, fp8, torch, e4m3_out=None, quant="pair"):
         self.fp8, self.torch, self.case = fp8, torch, case
+        self.quant = quant
         M, K, N = case.M, case.K, case.N
         self.M, self.N, self.K, self.b_major = M, N, K, case.b_major
         self.out_dtype = torch.float32 if case.out_fp32 else torch.bfloat16
@@ -191,12 +193,15 @@ class DenseStep:
             self.sc = None
             out_bytes = M * N * self.c.element_size()
         self.flops = 2.0 * M * N * K
-        self.kernels = ["quant_act", "quant_w", "gemm"]
-        self.kernel_bytes = {
-            "quant_act": M * K * 3 + (K // 128) * M * 4,
-            "quant_w": R * C * 3 + self.sb.numel() * 4,
-            "gemm": M * K + R * C + (self.sa.numel() + self.sb.numel()) * 4 + out_bytes,
-        }
+        qa_bytes = M * K * 3 + (K // 128) * M * 4
+        qw_bytes = R * C * 3 + self.sb.numel() * 4
+        if quant == "pair":
+            self.kernels = ["quant_act_w", "gemm"]
+            self.kernel_bytes = {"quant_act_w": qa_bytes + qw_bytes}
+        else:
+            self.kernels = ["quant_act", "quant_w", "gemm"]
+            self.kernel_bytes = {"quant_act": qa_bytes, "quant_w": qw_bytes}
+        self.kernel_bytes["gemm"] = M * K + R * C + (self.sa.numel() + self.sb.numel()) * 4 + out_bytes
         if e4m3_out == "unfused":
             self.kernels.append("quant_out")
             self.kernel_bytes["gemm"] += M * N * 2 - out_bytes
@@ -205,13 +210,19 @@ class DenseStep:
         self.d2h_bytes = out_bytes
         self.launches_per_step = len(self.kernels)
         self.side = torch.cuda.Stream(device=dev)
-        self.schedule = "quant_act || quant_w -> gemm" + (" -> quant_out" if e4m3_out == "unfused" else "")
+        self.schedule = ("quant_act_w" if quant == "pair" else "quant_act || quant_w") + " -> gemm" + \
+            (" -> quant_out" if e4m3_out == "unfused" else "")
 
-    def run(self, i, events=None):
-        """events: (start, end) per kernel in `kernels` order, or None."""
-        a, w = self.sets[i % self.nsets]
+    def _quantise(self, a, w, events=None):
+        """Both operands into qa / sa and qb / sb; records the quantiser
+        kernels' (start, end) events, if given, and returns how many it used."""
         f, torch = self.fp8, self.torch
         main = torch.cuda.current_stream()
+        if self.quant == "pair":
+            if events: events[0].record(main)
+            f.fp8_quant_act_w(a, w, self.qa, self.sa, self.qb, self.sb)
+            if events: events[1].record(main)
+            return 2
         self.side.wait_stream(main)            # the previous step's GEMM has read qa / sa
         with torch.cuda.stream(self.side):
             if events: events[0].record(self.side)
@@ -221,13 +232,20 @@ class DenseStep:
         f.fp8_quant_w_128x128(w, self.qb, self.sb)
         if events: events[3].record(main)
         main.wait_stream(self.side)
-        if events: events[4].record(main)
+        return 4
+
+    def run(self, i, events=None):
+        """events: (start, end) per kernel in `kernels` order, or None."""
+        a, w = self.sets[i % self.nsets]
+        main = self.torch.cuda.current_stream()
+        e = self._quantise(a, w, events)
+        if events: events[e].record(main)
         self._gemm()
-        if events: events[5].record(main)
+        if events: events[e + 1].record(main)
         if self.e4m3_out == "unfused":
-            if events: events[6].record(main)
-            f.fp8_quant_act_1x128(self.c16, self.c, self.sc)
-            if events: events[7].record(main)
+            if events: events[e + 2].record(main)
+            self.fp8.fp8_quant_act_1x128(self.c16, self.c, self.sc)
+            if events: events[e + 3].record(main)
 
     def _gemm(self):
         if self.e4m3_out == "unfused":
@@ -251,16 +269,10 @@ class DenseStep:
         return outs
 
     def compute(self, dev_in, outs):
-        """The whole path on device inputs [a, w] into outs [c (, sc)]: A is
-        quantised on the side stream while W is quantised on this stream."""
+        """The whole path on device inputs [a, w] into outs [c (, sc)]."""
         a, w = dev_in
-        f, torch = self.fp8, self.torch
-        main = torch.cuda.current_stream()
-        self.side.wait_stream(main)
-        with torch.cuda.stream(self.side):
-            f.fp8_quant_act_1x128(a, self.qa, self.sa, stream=self.side)
-        f.fp8_quant_w_128x128(w, self.qb, self.sb)
-        main.wait_stream(self.side)
+        f = self.fp8
+        self._quantise(a, w)
         if self.e4m3_out == "unfused":
             f.fp8_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major, C=self.c16)
             f.fp8_quant_act_1x128(self.c16, outs[0], outs[1])
@@ -540,7 +552,7 @@ def run_ours(args):
     elif args.workload == "wgrad":
         step = WgradStep(case, fp8, torch)
     else:
-        step = DenseStep(case, fp8, torch, e4m3_out=args.e4m3_out)
+        step = DenseStep(case, fp8, torch, e4m3_out=args.e4m3_out, quant=args.quant)
     stream = torch.cuda.current_stream()
 
     for i in range(args.warmup):
@@ -740,6 +752,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end run")
+    ap.add_argument("--quant", choices=["pair", "split"], default="pair",
+                    help="dense workloads: quantise A and W in one launch (pair) or as two "
+                         "concurrent kernels (split)")
     ap.add_argument("--e4m3-out", choices=["fused", "unfused"], default=None,
                     help="dense workloads: the step's output is C quantised per 1x128 row tile (E4M3 codes "
                          "+ scales), by the GEMM's epilogue (fused) or by the activation quantiser on the "

@@ -34,7 +34,7 @@ _STATUS_NAMES = {
     FP8BS_ERR_TIMEOUT: "FP8BS_ERR_TIMEOUT", FP8BS_ERR_INDEX: "FP8BS_ERR_INDEX",
 }
 
-EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
+EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8_gemm_blockscaled",
             "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
             "fp8_quant_act_1x128_gather", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
             "fp8bs_selftest_wait_timeout")
@@ -55,6 +55,7 @@ def _load():
     sigs = {
         "fp8_quant_act_1x128": [p, i64, i64, i64, p, i64, p, p],
         "fp8_quant_w_128x128": [p, i64, i64, i64, p, i64, p, p],
+        "fp8_quant_act_w": [p, i64, i64, i64, p, i64, p, p, i64, i64, i64, p, i64, p, p],
         "fp8_gemm_blockscaled": [p, p, p, p, i64, i64, i64, i32, p, i32, i64, p],
         "fp8_gemm_blockscaled_e4m3_out": [p, p, p, p, i64, i64, i64, i32, p, i64, p, p],
         "fp8_quant_tokens_1x128": [p, i64, i64, i64, p, i64, p, p],
@@ -143,6 +144,44 @@ def fp8_quant_w_128x128(w, q=None, sW=None, stream=None):
     _check(lib.fp8_quant_w_128x128(_ptr(w), R, C, ldw, _ptr(q), ldq, _ptr(sW), _stream(stream)),
            "fp8_quant_w_128x128")
     return q, sW
+
+
+def fp8_quant_act_w(x, w, qa=None, sA=None, qw=None, sW=None, stream=None):
+    """Both operands of one GEMM in one launch: 1x128 quantisation of BF16
+    ``x [M, K]`` and 128x128 quantisation of BF16 ``w [R, C]``, bit-equal to
+    fp8_quant_act_1x128(x) and fp8_quant_w_128x128(w).
+
+    Returns ``(qa, sA, qw, sW)`` with the shapes of those two calls."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(w, torch.bfloat16, "w", 2)
+    _row_major(x, "x")
+    _row_major(w, "w")
+    M, K = x.shape
+    R, C = w.shape
+    if qa is None:
+        qa = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if sA is None:
+        sA = torch.empty((K // 128, M), dtype=torch.float32, device=x.device)
+    if qw is None:
+        qw = torch.empty((R, C), dtype=torch.uint8, device=w.device)
+    if sW is None:
+        sW = torch.empty(((R + 127) // 128, C // 128), dtype=torch.float32, device=w.device)
+    _need(qa, torch.uint8, "qa", 2)
+    _need(qw, torch.uint8, "qw", 2)
+    _row_major(qa, "qa")
+    _row_major(qw, "qw")
+    if tuple(qa.shape) != (M, K) or not sA.is_contiguous() or sA.numel() != (K // 128) * M:
+        raise ValueError("activation output shapes do not match x")
+    if tuple(qw.shape) != (R, C) or not sW.is_contiguous() or sW.numel() != ((R + 127) // 128) * (C // 128):
+        raise ValueError("weight output shapes do not match w")
+    ldx = x.stride(0) if M > 0 else K
+    ldqa = qa.stride(0) if M > 0 else K
+    ldw = w.stride(0) if R > 0 else C
+    ldqw = qw.stride(0) if R > 0 else C
+    _check(lib.fp8_quant_act_w(_ptr(x), M, K, ldx, _ptr(qa), ldqa, _ptr(sA),
+                               _ptr(w), R, C, ldw, _ptr(qw), ldqw, _ptr(sW), _stream(stream)),
+           "fp8_quant_act_w")
+    return qa, sA, qw, sW
 
 
 def _out(C, M, N, out_dtype, device):
@@ -310,7 +349,7 @@ def fp8bs_selftest_wait_timeout(limit_us=20000, stream=None):
     _check(lib.fp8bs_selftest_wait_timeout(int(limit_us), _stream(stream)), "fp8bs_selftest_wait_timeout")
 
 
-__all__ = ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
+__all__ = ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8_gemm_blockscaled",
            "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
            "fp8_quant_act_1x128_gather", "FP8BS_ERR_INDEX",
            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout",

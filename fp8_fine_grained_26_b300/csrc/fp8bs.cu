@@ -97,6 +97,8 @@ int current_device(DeviceInfo **info)
             cudaFuncSetAttribute(quant_act_1x128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  quant_smem_bytes()) != cudaSuccess ||
             cudaFuncSetAttribute(quant_w_128x128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 quant_smem_bytes()) != cudaSuccess ||
+            cudaFuncSetAttribute(quant_act_w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  quant_smem_bytes()) != cudaSuccess)
             return FP8BS_ERR_LAUNCH;
         // how many CTA pairs (2-CTA clusters) fit at once
@@ -412,6 +414,70 @@ int fp8_quant_w_128x128(const void *w_bf16, int64_t R, int64_t C, int64_t ldw, v
     const int grid = (int)std::min<int64_t>(units, 3 * (int64_t)dev->num_sms);
     quant_w_128x128_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
         tmW, R, CB, static_cast<uint8_t *>(q_e4m3), ldq, sW, units);
+    return launch_status();
+}
+
+// Argument checks shared by the activation and weight quantisers: 0 when the
+// operand is valid and non-empty, 1 when it is empty, else a status.
+static int check_quant_operand(const void *x, int64_t rows, int64_t cols, int64_t ldx, const void *q, int64_t ldq,
+                               const float *s)
+{
+    if (rows < 0 || cols < 0 || cols % 128 != 0)
+        return FP8BS_ERR_SHAPE;
+    if (rows == 0 || cols == 0)
+        return 1;
+    if (!x || !q || !s)
+        return FP8BS_ERR_NULL;
+    if (ldx < cols || ldq < cols)
+        return FP8BS_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(q) || !aligned4(s) || (ldx * 2) % 16 != 0 || ldq % 16 != 0)
+        return FP8BS_ERR_ALIGN;
+    return 0;
+}
+
+int fp8_quant_act_w(const void *x_bf16, int64_t M, int64_t K, int64_t ldx, void *qa_e4m3, int64_t ldqa, float *sA,
+                    const void *w_bf16, int64_t R, int64_t C, int64_t ldw, void *qw_e4m3, int64_t ldqw, float *sW,
+                    cudaStream_t stream)
+{
+    const int ca = check_quant_operand(x_bf16, M, K, ldx, qa_e4m3, ldqa, sA);
+    if (ca < 0)
+        return ca;
+    const int cw = check_quant_operand(w_bf16, R, C, ldw, qw_e4m3, ldqw, sW);
+    if (cw < 0)
+        return cw;
+    if (ca == 1 && cw == 1)
+        return FP8BS_OK;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    CUtensorMap tmX, tmW;
+    QuantPairArgs a = {};
+    if (ca == 0) {
+        if (!encode_bf16_units(&tmX, x_bf16, (uint64_t)K, (uint64_t)M, (uint64_t)ldx))
+            return FP8BS_ERR_ARG;
+        a.M = M;
+        a.KB = K / 128;
+        a.qa = static_cast<uint8_t *>(qa_e4m3);
+        a.ldqa = ldqa;
+        a.sA = sA;
+        a.units_a = ((M + 127) / 128) * a.KB;
+    }
+    if (cw == 0) {
+        if (!encode_bf16_units(&tmW, w_bf16, (uint64_t)C, (uint64_t)R, (uint64_t)ldw))
+            return FP8BS_ERR_ARG;
+        a.R = R;
+        a.CB = C / 128;
+        a.qw = static_cast<uint8_t *>(qw_e4m3);
+        a.ldqw = ldqw;
+        a.sW = sW;
+    }
+    if (ca != 0)
+        tmX = tmW;                                // never read: no activation units
+    if (cw != 0)
+        tmW = tmX;                                // never read: no weight units
+    a.units = a.units_a + (cw == 0 ? ((R + 127) / 128) * a.CB : 0);
+    const int grid = (int)std::min<int64_t>(a.units, 3 * (int64_t)dev->num_sms);
+    quant_act_w_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(tmX, tmW, a);
     return launch_status();
 }
 

@@ -177,15 +177,120 @@ __device__ __forceinline__ void qdrain(const QRing &r, int64_t consumed, int64_t
 // Warp w owns rows [16 w, 16 w + 16); at step i its two half-warps take rows
 // 16 w + 2 i and 16 w + 2 i + 1 (512 contiguous bytes of the staged unit).
 // The eight row divisors of a half-warp are formed by eight different lanes
-// and broadcast with shuffles.
+// and broadcast with shuffles.  `issue_next` runs once the staged unit has
+// been read (the stage is free again) and queues the CTA's next copy.
+template <class Next>
+__device__ __forceinline__ void act_unit(const QRing &r, int64_t j, int64_t mb, int64_t kb, int64_t M,
+                                         uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ sA,
+                                         Next &&issue_next)
+{
+    const int tid = threadIdx.x;
+    const int lane16 = tid & 15;
+    const int hw = tid >> 4;
+    const uint32_t st = r.stage((int)(j % QSTAGES));
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = 2 * i + (hw & 1) + 16 * (hw >> 1);
+        const uint32_t a = st + (uint32_t)(row * 256 + lane16 * 16);
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w) : "r"(a));
+    }
+    __syncthreads();                                   // the stage is free again
+    issue_next();
+    float *scales = r.red_f((int)(j & 1));
+    // amax of each of this half-warp's 8 rows, known to all its 16 lanes
+    uint32_t am[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t a = absmax_bits8(v[i]);
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1)
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, o, 16));
+        am[i] = a;
+    }
+    // lane i of the half-warp forms row i's divisor once; the others fetch it
+    uint32_t mine_a = am[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+        mine_a = (lane16 & 7) == i ? am[i] : mine_a;
+    const Divisor dm = make_divisor(mine_a);
+    const int half_base = (tid & 16);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        Divisor d;
+        d.s = __shfl_sync(0xffffffffu, dm.s, half_base + i);
+        d.r = __shfl_sync(0xffffffffu, dm.r, half_base + i);
+        d.mode = divisor_mode(am[i]);
+        const int row = 2 * i + (hw & 1) + 16 * (hw >> 1);
+        const int64_t gm = mb * 128 + row;
+        if (gm < M) {
+            const uint2 c = quant_8(v[i], d);
+            ptx::st_v2(q + gm * ldq + kb * 128 + lane16 * 8, c.x, c.y);
+        }
+        if (lane16 == 0)
+            scales[row] = d.s;
+    }
+    __syncthreads();
+    if (tid < 128 && mb * 128 + tid < M)
+        sA[kb * M + mb * 128 + tid] = scales[tid];
+}
+
+// Weight quantiser.  Unit (rb, cb): one 128x128 block.  Thread t owns the
+// 16-byte column chunk (t & 15) of rows (t >> 4) + 16 i, i = 0..7: 64 values
+// held in registers between the amax and the encode passes.
+template <class Next>
+__device__ __forceinline__ void w_unit(const QRing &r, int64_t j, int64_t rb, int64_t cb, int64_t R, int64_t CB,
+                                       uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ sW,
+                                       Next &&issue_next)
+{
+    const int tid = threadIdx.x;
+    const int chunk = tid & 15;
+    const int r0 = tid >> 4;
+    const uint32_t st = r.stage((int)(j % QSTAGES));
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t a = st + (uint32_t)((r0 + 16 * i) * 256 + chunk * 16);
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w) : "r"(a));
+    }
+    uint32_t a = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        a = max(a, absmax_bits8(v[i]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+    uint32_t *wmax = r.red_u((int)(j & 1));
+    if ((tid & 31) == 0)
+        wmax[tid >> 5] = a;
+    __syncthreads();                                   // stage read, warp maxima written
+    issue_next();
+    a = wmax[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+        a = max(a, wmax[i]);
+    const Divisor d = make_divisor(a);
+    const int64_t col = cb * 128 + chunk * 8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t row = rb * 128 + r0 + 16 * i;
+        if (row < R) {
+            const uint2 c = quant_8(v[i], d);
+            ptx::st_v2(q + row * ldq + col, c.x, c.y);
+        }
+    }
+    if (tid == 0)
+        sW[rb * CB + cb] = d.s;
+}
+
 __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_act_1x128_kernel(
     const __grid_constant__ CUtensorMap tmX, int64_t M, int64_t KB, uint8_t *__restrict__ q,
     int64_t ldq, float *__restrict__ sA, int64_t units)
 {
     const QRing r = qring_setup();
     const int tid = threadIdx.x;
-    const int lane16 = tid & 15;
-    const int hw = tid >> 4;
     const int64_t mine = (int64_t)blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     int64_t issued = 0;
     if (tid == 0)
@@ -195,73 +300,24 @@ __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_act_1x128_kernel(
     for (; j < mine; ++j) {
         if (!qwait(r, j))
             break;
-        const uint32_t st = r.stage((int)(j % QSTAGES));
-        uint4 v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int row = 2 * i + (hw & 1) + 16 * (hw >> 1);
-            const uint32_t a = st + (uint32_t)(row * 256 + lane16 * 16);
-            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w) : "r"(a));
-        }
-        __syncthreads();                                   // the stage is free again
-        if (tid == 0 && issued < mine && issued < j + 1 + QSTAGES) {
-            qissue(r, &tmX, issued, KB);
-            ++issued;
-        }
         int64_t mb, kb;
         qunit(j, KB, mb, kb);
-        float *scales = r.red_f((int)(j & 1));
-        // amax of each of this half-warp's 8 rows, known to all its 16 lanes
-        uint32_t am[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint32_t a = absmax_bits8(v[i]);
-#pragma unroll
-            for (int o = 8; o >= 1; o >>= 1)
-                a = max(a, __shfl_xor_sync(0xffffffffu, a, o, 16));
-            am[i] = a;
-        }
-        // lane i of the half-warp forms row i's divisor once; the others fetch it
-        uint32_t mine_a = am[0];
-#pragma unroll
-        for (int i = 1; i < 8; ++i)
-            mine_a = (lane16 & 7) == i ? am[i] : mine_a;
-        const Divisor dm = make_divisor(mine_a);
-        const int half_base = (tid & 16);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            Divisor d;
-            d.s = __shfl_sync(0xffffffffu, dm.s, half_base + i);
-            d.r = __shfl_sync(0xffffffffu, dm.r, half_base + i);
-            d.mode = divisor_mode(am[i]);
-            const int row = 2 * i + (hw & 1) + 16 * (hw >> 1);
-            const int64_t gm = mb * 128 + row;
-            if (gm < M) {
-                const uint2 c = quant_8(v[i], d);
-                ptx::st_v2(q + gm * ldq + kb * 128 + lane16 * 8, c.x, c.y);
+        act_unit(r, j, mb, kb, M, q, ldq, sA, [&] {
+            if (tid == 0 && issued < mine && issued < j + 1 + QSTAGES) {
+                qissue(r, &tmX, issued, KB);
+                ++issued;
             }
-            if (lane16 == 0)
-                scales[row] = d.s;
-        }
-        __syncthreads();
-        if (tid < 128 && mb * 128 + tid < M)
-            sA[kb * M + mb * 128 + tid] = scales[tid];
+        });
     }
     qdrain(r, j, issued);
 }
 
-// Weight quantiser.  Unit (rb, cb): one 128x128 block.  Thread t owns the
-// 16-byte column chunk (t & 15) of rows (t >> 4) + 16 i, i = 0..7: 64 values
-// held in registers between the amax and the encode passes.
 __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_w_128x128_kernel(
     const __grid_constant__ CUtensorMap tmW, int64_t R, int64_t CB, uint8_t *__restrict__ q,
     int64_t ldq, float *__restrict__ sW, int64_t units)
 {
     const QRing r = qring_setup();
     const int tid = threadIdx.x;
-    const int chunk = tid & 15;
-    const int r0 = tid >> 4;
     const int64_t mine = (int64_t)blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     int64_t issued = 0;
     if (tid == 0)
@@ -271,47 +327,87 @@ __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_w_128x128_kernel(
     for (; j < mine; ++j) {
         if (!qwait(r, j))
             break;
-        const uint32_t st = r.stage((int)(j % QSTAGES));
-        uint4 v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t a = st + (uint32_t)((r0 + 16 * i) * 256 + chunk * 16);
-            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w) : "r"(a));
-        }
-        uint32_t a = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            a = max(a, absmax_bits8(v[i]));
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1)
-            a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
-        uint32_t *wmax = r.red_u((int)(j & 1));
-        if ((tid & 31) == 0)
-            wmax[tid >> 5] = a;
-        __syncthreads();                                   // stage read, warp maxima written
-        if (tid == 0 && issued < mine && issued < j + 1 + QSTAGES) {
-            qissue(r, &tmW, issued, CB);
-            ++issued;
-        }
-        a = wmax[0];
-#pragma unroll
-        for (int i = 1; i < 8; ++i)
-            a = max(a, wmax[i]);
-        const Divisor d = make_divisor(a);
         int64_t rb, cb;
         qunit(j, CB, rb, cb);
-        const int64_t col = cb * 128 + chunk * 8;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int64_t row = rb * 128 + r0 + 16 * i;
-            if (row < R) {
-                const uint2 c = quant_8(v[i], d);
-                ptx::st_v2(q + row * ldq + col, c.x, c.y);
+        w_unit(r, j, rb, cb, R, CB, q, ldq, sW, [&] {
+            if (tid == 0 && issued < mine && issued < j + 1 + QSTAGES) {
+                qissue(r, &tmW, issued, CB);
+                ++issued;
             }
+        });
+    }
+    qdrain(r, j, issued);
+}
+
+// Both operands of one GEMM in one launch: the activation's 1x128 units
+// (units_a of them, first) and the weight's 128x128 blocks share one unit
+// list and one TMA ring, so the small, latency-bound activation pass fills
+// in around the weight stream instead of competing with it as a second
+// kernel.  Every unit is encoded exactly as the two kernels above encode it.
+struct QuantPairArgs {
+    int64_t M, KB;                       // activation: rows, 1x128 tiles per row
+    uint8_t *qa;
+    int64_t ldqa;
+    float *sA;
+    int64_t units_a;
+    int64_t R, CB;                       // weight: rows, 128-column blocks
+    uint8_t *qw;
+    int64_t ldqw;
+    float *sW;
+    int64_t units;                       // activation units + weight blocks
+};
+
+__device__ __forceinline__ void qissue_pair(const QRing &r, const CUtensorMap *tmX, const CUtensorMap *tmW,
+                                            const QuantPairArgs &a, int64_t j)
+{
+    const int64_t u = (int64_t)blockIdx.x + j * gridDim.x;
+    int64_t rb, cb;
+    const CUtensorMap *tm;
+    if (u < a.units_a) {
+        rb = u / a.KB;
+        cb = u - rb * a.KB;
+        tm = tmX;
+    } else {
+        rb = (u - a.units_a) / a.CB;
+        cb = (u - a.units_a) - rb * a.CB;
+        tm = tmW;
+    }
+    const int s = (int)(j % QSTAGES);
+    ptx::fence_proxy_async_smem();             // earlier generic reads of the stage come first
+    ptx::mbar_arrive_expect_tx(r.full(s), QUNIT_BYTES);
+    ptx::tma_load_2d(r.stage(s), tm, r.full(s), (int32_t)(cb * 128), (int32_t)(rb * 128));
+}
+
+__global__ void __launch_bounds__(QUANT_THREADS, 3) quant_act_w_kernel(
+    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const QuantPairArgs a)
+{
+    const QRing r = qring_setup();
+    const int tid = threadIdx.x;
+    const int64_t units = a.units;
+    const int64_t mine = (int64_t)blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    int64_t issued = 0;
+    if (tid == 0)
+        for (; issued < mine && issued < QSTAGES; ++issued)
+            qissue_pair(r, &tmX, &tmW, a, issued);
+    auto next = [&](int64_t j) {
+        if (tid == 0 && issued < mine && issued < j + 1 + QSTAGES) {
+            qissue_pair(r, &tmX, &tmW, a, issued);
+            ++issued;
         }
-        if (tid == 0)
-            sW[rb * CB + cb] = d.s;
+    };
+    int64_t j = 0;
+    for (; j < mine; ++j) {
+        if (!qwait(r, j))
+            break;
+        const int64_t u = (int64_t)blockIdx.x + j * gridDim.x;
+        if (u < a.units_a) {
+            const int64_t mb = u / a.KB;
+            act_unit(r, j, mb, u - mb * a.KB, a.M, a.qa, a.ldqa, a.sA, [&] { next(j); });
+        } else {
+            const int64_t w = u - a.units_a;
+            const int64_t rb = w / a.CB;
+            w_unit(r, j, rb, w - rb * a.CB, a.R, a.CB, a.qw, a.ldqw, a.sW, [&] { next(j); });
+        }
     }
     qdrain(r, j, issued);
 }

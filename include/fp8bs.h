@@ -93,6 +93,24 @@ int fp8_quant_w_128x128(const void *w_bf16, int64_t R, int64_t C, int64_t ldw,
                         void *q_e4m3, int64_t ldq, float *sW, cudaStream_t stream);
 
 /*
+ * Both operands of one GEMM quantised in a single launch: the activation x
+ * with the 1x128 rule and the weight w with the 128x128 rule.  The pages
+ * quantise both inputs of every FP8 GEMM this way before the GEMM runs
+ * ("DeepSeek-V3 Technical Report digest", section 3, fine-grained
+ * quantisation: 1x128 tiles for activations, 128x128 blocks for weights).
+ * The outputs are exactly those of fp8_quant_act_1x128(x, M, K, ...) and
+ * fp8_quant_w_128x128(w, R, C, ...), bit for bit, and every argument has the
+ * same meaning, layout, checks and error codes as in those two calls.  One
+ * kernel walks both operands' 32 KiB units through one TMA ring, which keeps
+ * the small activation pass from running as a second kernel beside the
+ * weight pass.  Either operand may be empty (M == 0 or K == 0; R == 0 or
+ * C == 0).  Nothing is launched when an argument is rejected.
+ */
+int fp8_quant_act_w(const void *x_bf16, int64_t M, int64_t K, int64_t ldx, void *qa_e4m3, int64_t ldqa, float *sA,
+                    const void *w_bf16, int64_t R, int64_t C, int64_t ldw, void *qw_e4m3, int64_t ldqw, float *sW,
+                    cudaStream_t stream);
+
+/*
  * Block-scaled FP8 GEMM:  C[m][n] = sum_kb  sA[kb][m] * sB(n, kb) *
  *                                   sum_{k in kb} qA[m][k] * qB(n, k)
  * with each 128-wide K slice's FP8 product formed on the tensor cores in FP32

@@ -20,7 +20,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
-        "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_gemm_blockscaled",
+        "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8_gemm_blockscaled",
         "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
         "fp8_quant_act_1x128_gather", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
         "fp8bs_selftest_wait_timeout"])
@@ -80,6 +80,24 @@ def test_quant_w_rejects_bad_shapes():
     assert lib.fp8_quant_w_128x128(P(0), 4, 130, 130, P(0), 130, P(0), P(0)) == -2
     assert lib.fp8_quant_w_128x128(P(0), 0, 128, 128, P(0), 128, P(0), P(0)) == 0
     assert lib.fp8_quant_w_128x128(P(16), 4, 128, 128, P(16), 136, P(16), P(0)) == -3
+
+
+def test_quant_act_w_rejects_either_bad_operand():
+    lib = _raw()
+    q = lib.fp8_quant_act_w
+    good_a = (P(16), 4, 128, 128, P(16), 128, P(16))
+    good_w = (P(16), 4, 128, 128, P(16), 128, P(16))
+    empty_a = (P(0), 0, 128, 128, P(0), 128, P(0))
+    empty_w = (P(0), 0, 128, 128, P(0), 128, P(0))
+    assert q(*empty_a, *empty_w, P(0)) == 0                                          # both empty
+    assert q(P(16), 4, 100, 128, P(16), 128, P(16), *good_w, P(0)) == -2             # K % 128
+    assert q(*good_a, P(16), 4, 130, 130, P(16), 130, P(16), P(0)) == -2             # C % 128
+    assert q(P(0), 4, 128, 128, P(16), 128, P(16), *good_w, P(0)) == -1              # NULL x
+    assert q(*good_a, P(16), 4, 128, 128, P(0), 128, P(16), P(0)) == -1              # NULL qw
+    assert q(*good_a, P(16), 4, 128, 64, P(16), 128, P(16), P(0)) == -2              # ldw < C
+    assert q(P(8), 4, 128, 128, P(16), 128, P(16), *empty_w, P(0)) == -3             # x align
+    assert q(*empty_a, P(16), 4, 128, 128, P(16), 136, P(16), P(0)) == -3            # ldqw % 16
+    assert q(P(16), -1, 128, 128, P(16), 128, P(16), *good_w, P(0)) == -2     # M < 0
 
 
 def test_gemm_rejects_bad_arguments():
