@@ -40,7 +40,8 @@ __device__ __forceinline__ uint32_t absmax_bits8(const uint4 &v)
 //     q0 = RN(x * r),  rem = fma(-q0, s, x),  q = copysign(fma(rem, r, q0), x),
 // which an exhaustive check over every BF16 amax >= 2^-90 and every BF16
 // |x| <= amax shows to equal IEEE division bit for bit (up to the sign of
-// zero-encoding quotients below 2^-11).  Groups with a smaller amax use
+// zero-encoding quotients below 2^-11).  The copysign is applied to the
+// E4M3 code (x's sign bit OR-ed in), which gives the same byte.  Groups with a smaller amax use
 // IEEE division; an all-zero group (s == 0) encodes x itself (a signed zero).
 // Two elements are processed at once with packed f32x2 arithmetic (each lane
 // rounds exactly as the scalar operation).
@@ -83,9 +84,16 @@ __device__ __forceinline__ uint2 quant_8(const uint4 &v, const Divisor &d)
             const float2 q0 = __fmul2_rn(x2, r2);
             const float2 rem = __ffma2_rn(q0, ns2, x2);             // x - q0 * s, exact
             const float2 q = __ffma2_rn(rem, r2, q0);
-            // the quotient carries x's sign (keeps -0, where +0 + -0 rounds to +0)
-            c[k] = ptx::cvt_e4m3x2(copysignf(q.x, x2.x), copysignf(q.y, x2.y));
+            c[k] = ptx::cvt_e4m3x2(q.x, q.y);
         }
+        // The code must carry x's sign.  A nonzero quotient has it already,
+        // and a zero quotient of a positive x is +0.  Only a negative x can
+        // end at +0: x = -0, where -0 + +0 rounds to +0, or an underflow.
+        // OR-ing x's sign bits (bit 7 of each BF16's high byte) into the
+        // codes therefore gives every code the sign of its x.
+        const uint32_t sgn0 = __byte_perm(w[0], w[1], 0x7531) & 0x80808080u;
+        const uint32_t sgn1 = __byte_perm(w[2], w[3], 0x7531) & 0x80808080u;
+        return make_uint2(__byte_perm(c[0], c[1], 0x5410) | sgn0, __byte_perm(c[2], c[3], 0x5410) | sgn1);
     } else {
 #pragma unroll
         for (int k = 0; k < 4; ++k)

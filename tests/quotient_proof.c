@@ -18,8 +18,13 @@
  * signed zero in E4M3, so where both sides are that small only the sign bits
  * must agree; such pairs are counted separately.
  *
- * Output: one line "pairs=<n> mismatches=<m> tiny_differences=<t> ...".
- * Exit status 0 iff m == 0.
+ * The kernels apply the copysign to the E4M3 code instead (x's sign bit is
+ * OR-ed into the byte converted from the unsigned result RN(rem * r + q0)).
+ * That gives the same byte iff the unsigned result already carries x's sign
+ * or is +0; every pair where it is neither is counted as a sign violation.
+ *
+ * Output: one line "pairs=<n> mismatches=<m> tiny_differences=<t>
+ * sign_violations=<v> ...".  Exit status 0 iff m == 0 and v == 0.
  */
 #include <math.h>
 #include <stdint.h>
@@ -48,7 +53,7 @@ int main(int argc, char **argv)
     unsigned stride = (argc > 1) ? (unsigned)atoi(argv[1]) : 1u;
     if (stride == 0)
         stride = 1;
-    unsigned long long pairs = 0, mism = 0, tiny = 0;
+    unsigned long long pairs = 0, mism = 0, tiny = 0, sign_viol = 0;
     for (uint32_t ha = 0x1280; ha <= 0x7F7F; ha += stride) {   /* amax >= 2^-90 */
         const float amax = bf((uint16_t)ha);
         const float s = amax / 448.0f;
@@ -61,8 +66,14 @@ int main(int argc, char **argv)
             const float ref = x / s;
             const float q0 = x * r;
             const float rem = fmaf(-q0, s, x);
-            const float q1 = copysignf(fmaf(rem, r, q0), x);
+            const float qr = fmaf(rem, r, q0);
+            const float q1 = copysignf(qr, x);
             pairs++;
+            if ((bits(qr) >> 31) != (bits(x) >> 31) && bits(qr) != 0u) {
+                if (sign_viol < 10)
+                    fprintf(stderr, "sign violation amax=%a x=%a unsigned=%a\n", amax, x, qr);
+                sign_viol++;
+            }
             if (bits(q1) != bits(ref)) {
                 if (fabsf(ref) < 0x1p-11f && fabsf(q1) < 0x1p-11f &&
                     (bits(ref) >> 31) == (bits(q1) >> 31))
@@ -75,7 +86,7 @@ int main(int argc, char **argv)
             }
         }
     }
-    printf("pairs=%llu mismatches=%llu tiny_differences=%llu stride=%u\n", pairs, mism, tiny,
-           stride);
-    return mism == 0 ? 0 : 1;
+    printf("pairs=%llu mismatches=%llu tiny_differences=%llu sign_violations=%llu stride=%u\n", pairs, mism,
+           tiny, sign_viol, stride);
+    return (mism == 0 && sign_viol == 0) ? 0 : 1;
 }
