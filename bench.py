@@ -149,6 +149,8 @@ def make_workload(name, device):
         return synthetic.tiny(device=device)
     if name == "experts":
         return synthetic.experts(device=device, keep_x=True)
+    if name == "experts_small":
+        return synthetic.experts_small(device=device, keep_x=True)
     if name == "wgrad":
         return synthetic.wgrad(device=device)
     raise ValueError(name)
@@ -515,7 +517,7 @@ def dense_host_inputs(case):
 def kernel_src_sha():
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm.cuh", "ptx.cuh", "common.cuh"):
+    for f in ("gemm.cuh", "ptx.cuh", "common.cuh", "quant.cuh"):     # quant.cuh: the E4M3-output epilogue
         with open(os.path.join(ROOT, "fp8_fine_grained_26_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -545,9 +547,9 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
 
     case = make_workload(args.workload, device)
-    if args.e4m3_out and args.workload in ("experts", "wgrad"):
+    if args.e4m3_out and args.workload in ("experts", "experts_small", "wgrad"):
         raise SystemExit("--e4m3-out applies to the dense forward workloads")
-    if args.workload == "experts":
+    if args.workload in ("experts", "experts_small"):
         step = ExpertsStep(case, fp8, torch)
     elif args.workload == "wgrad":
         step = WgradStep(case, fp8, torch)
@@ -660,7 +662,7 @@ def run_ours(args):
         flops, secs, desc = oracle_sample_wgrad(case)
         cpu = {"value": round(flops / secs / 1e12, 9), "unit": "TFLOP/s", "cores": 1,
                "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
-    elif rank == 0 and world == 1 and not args.no_cpu and args.workload != "experts":
+    elif rank == 0 and world == 1 and not args.no_cpu and args.workload not in ("experts", "experts_small"):
         flops, secs, desc = oracle_sample(args.workload, lambda: dense_host_inputs(case))
         cpu = {"value": round(flops / secs / 1e12, 9), "unit": "TFLOP/s", "cores": 1,
                "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
@@ -697,7 +699,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    if args.workload in ("experts", "wgrad"):
+    if args.workload in ("experts", "experts_small", "wgrad"):
         print(json.dumps({"impl": "reference", "unavailable":
                           "the oracle arm samples the dense forward workloads only"}), flush=True)
         return
@@ -748,7 +750,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="mla_q",
-                    choices=["mla_q", "mla_kv", "dgrad", "experts", "tiny", "wgrad"])
+                    choices=["mla_q", "mla_kv", "dgrad", "experts", "tiny", "wgrad", "experts_small"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end run")

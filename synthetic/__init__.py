@@ -204,6 +204,15 @@ def experts(device="cpu", seed=0, keep_x=False):
                         2048, 7168, seed=seed, device=device, keep_x=keep_x)
 
 
+def experts_small(device="cpu", seed=0, keep_x=False):
+    """The routed-expert workload at a quarter of the experts and tokens
+    (1024 tokens, top-8 of 64 experts): the same ~128 routed rows per expert
+    and the same weight shape, with 0.94 GB of FP8 weights (still far above
+    L2).  It is the case the profiler captures of the expert kernels run on."""
+    return grouped_case("routed experts 1024 tok top-8 of 64, 2048x7168", 1024, 64, 8,
+                        2048, 7168, seed=seed, device=device, keep_x=keep_x)
+
+
 def dgrad(device="cpu", seed=0):
     return dense_case("dgrad 8192x18432x7168 student-t", 8192, 18432, 7168, seed=seed,
                       device=device, heavy_tail=True, b_major=1)
