@@ -428,7 +428,6 @@ __device__ __forceinline__ void st_v4(void *p, uint32_t a, uint32_t b, uint32_t 
 }
 
 // Lane-wise unsigned 16-bit max of two packed pairs.
-// Lane-wise unsigned 16-bit max of two packed pairs.
 __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b)
 {
     uint32_t d;

@@ -16,7 +16,10 @@ fp8 = pytest.importorskip("fp8_fine_grained_26_b300")
 DEV = "cuda"
 
 
-@pytest.mark.parametrize("T,K,M", [(64, 128, 100), (300, 384, 777), (50, 1152, 64), (4096, 7168, 256)])
+# K in tiles: 1, 3, 9, 56 (= 32 + 24), 33 (= 32 + 1), 64 (= 2 x 32): one lane
+# per tile and up to 32 tiles per warp task, so every partial last task shape
+@pytest.mark.parametrize("T,K,M", [(64, 128, 100), (300, 384, 777), (50, 1152, 64), (4096, 7168, 256),
+                                   (100, 4224, 50), (20, 8192, 40)])
 def test_gather_quantiser_matches_oracle(T, K, M):
     g = generator(T + K + M, DEV)
     x = normal_bf16((T, K), 1.0, g, DEV, outlier_p=0.003, outlier_scale=50.0)
@@ -32,6 +35,22 @@ def test_gather_quantiser_matches_oracle(T, K, M):
     q2, s2 = fp8.fp8_quant_act_1x128(x.index_select(0, rows.long()))
     torch.cuda.synchronize()
     assert torch.equal(q, q2) and torch.equal(s.view(torch.int32), s2.view(torch.int32))
+
+
+def test_gather_quantiser_adversarial_rows():
+    # ties at every E4M3 midpoint, signed zeros, subnormals and extremes,
+    # gathered in a scrambled order with repeats
+    from test_gpu_quant import _adversarial_rows
+    base = _adversarial_rows()
+    x = torch.cat([base, base.flip(0)], dim=1).repeat(1, 17).to(DEV)    # K = 34 tiles
+    T = x.shape[0]
+    g = generator(123, DEV)
+    rows = torch.randint(0, T, (3 * T,), generator=g, device=DEV, dtype=torch.int64).to(torch.int32)
+    q, s = fp8.fp8_quant_act_1x128_gather(x, rows)
+    assert fp8.fp8bs_last_error() == 0
+    oq, os_ = oracle.quant_act_1x128(bf16_bits(x)[rows.cpu().numpy()])
+    assert np.array_equal(host_u8(q), oq)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), os_.view(np.uint32))
 
 
 def test_gather_quantiser_experts_dispatch():
