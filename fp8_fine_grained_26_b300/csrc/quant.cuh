@@ -70,12 +70,13 @@ __device__ __forceinline__ float quotient_slow(float x, const Divisor &d)
     return d.mode == 1 ? __fdiv_rn(x, d.s) : x;
 }
 
-// E4M3 codes of the 8 BF16 values in v, as 8 bytes (element 0 lowest).
-__device__ __forceinline__ uint2 quant_8(const uint4 &v, const Divisor &d)
+// E4M3 codes of the 8 BF16 values in v for a divisor of mode 2
+// (reciprocal + correction), as 8 bytes (element 0 lowest).
+__device__ __forceinline__ uint2 quant_8_recip(const uint4 &v, const Divisor &d)
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t c[4];
-    if (d.mode == 2) {
+    {
         const float2 r2 = make_float2(d.r, d.r);
         const float2 ns2 = make_float2(-d.s, -d.s);
 #pragma unroll
@@ -94,11 +95,19 @@ __device__ __forceinline__ uint2 quant_8(const uint4 &v, const Divisor &d)
         const uint32_t sgn0 = __byte_perm(w[0], w[1], 0x7531) & 0x80808080u;
         const uint32_t sgn1 = __byte_perm(w[2], w[3], 0x7531) & 0x80808080u;
         return make_uint2(__byte_perm(c[0], c[1], 0x5410) | sgn0, __byte_perm(c[2], c[3], 0x5410) | sgn1);
-    } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            c[k] = ptx::cvt_e4m3x2(quotient_slow(bf16lo(w[k]), d), quotient_slow(bf16hi(w[k]), d));
     }
+}
+
+// E4M3 codes of the 8 BF16 values in v, as 8 bytes (element 0 lowest).
+__device__ __forceinline__ uint2 quant_8(const uint4 &v, const Divisor &d)
+{
+    if (d.mode == 2)
+        return quant_8_recip(v, d);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        c[k] = ptx::cvt_e4m3x2(quotient_slow(bf16lo(w[k]), d), quotient_slow(bf16hi(w[k]), d));
     return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
@@ -445,12 +454,19 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_gather_kernel(
     const int hbase = lane & 16;
     const uint64_t keep = ptx::policy_evict_last();
     const int64_t chunks = (KB + GATHER_TILES - 1) / GATHER_TILES;
-    const int64_t tasks = M * chunks;
     const int64_t warp0 = ((int64_t)blockIdx.x * GATHER_THREADS + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * GATHER_THREADS) >> 5;
-    for (int64_t task = warp0; task < tasks; task += nwarps) {
-        const int64_t i = task / chunks;
-        const int64_t kb0 = (task - i * chunks) * GATHER_TILES;
+    // the warp's tasks are warp0, warp0 + nwarps, ...: (row, chunk) advance
+    // by a fixed step with one carry instead of a division per task
+    const int64_t step_i = nwarps / chunks, step_c = nwarps - step_i * chunks;
+    int64_t i = warp0 / chunks, chunk = warp0 - i * chunks;
+    for (; i < M; i += step_i, chunk += step_c) {
+        if (chunk >= chunks) {
+            chunk -= chunks;
+            if (++i >= M)
+                break;
+        }
+        const int64_t kb0 = chunk * GATHER_TILES;
         const int32_t src = rows[i];
         const bool valid = src >= 0 && (int64_t)src < T;
         if (!valid && lane == 0)
@@ -480,6 +496,14 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_gather_kernel(
         for (int t = 1; t < TPH; ++t)
             mine = (l16 & (TPH - 1)) == t ? am[t] : mine;
         const Divisor dm = make_divisor(mine);
+        // the usual case, every tile of the task on the reciprocal path,
+        // encodes without a per-tile branch
+        bool recip = true;
+#pragma unroll
+        for (int t = 0; t < TPH; ++t)
+            recip = recip && divisor_mode(am[t]) == 2;
+        recip = __all_sync(0xffffffffu, recip);
+        uint8_t *qrow = q + i * ldq + l16 * 8;
 #pragma unroll
         for (int t = 0; t < TPH; ++t) {
             const int64_t kb = kb0 + 2 * t + half;
@@ -488,8 +512,8 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_gather_kernel(
             d.r = __shfl_sync(0xffffffffu, dm.r, hbase + t);
             d.mode = divisor_mode(am[t]);
             if (kb < KB) {
-                const uint2 c = quant_8(v[t], d);
-                ptx::st_v2_cs(q + i * ldq + kb * 128 + l16 * 8, c.x, c.y);
+                const uint2 c = recip ? quant_8_recip(v[t], d) : quant_8(v[t], d);
+                ptx::st_v2_cs(qrow + kb * 128, c.x, c.y);
                 if (l16 == 0)
                     sA[kb * M + i] = d.s;
             }
