@@ -514,10 +514,13 @@ def dense_host_inputs(case):
     return synthetic.bf16_bits(case.a), synthetic.bf16_bits(case.w), case.b_major
 
 
-def kernel_src_sha():
+def kernel_src_sha(e4m3_out=False):
+    """First 16 hex digits of sha256 over the sources a GEMM kernel is built
+    from: gemm.cuh, ptx.cuh and common.cuh, plus quant.cuh (the encoder) for
+    the E4M3-output epilogue, the only GEMM variant that uses it."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm.cuh", "ptx.cuh", "common.cuh", "quant.cuh"):     # quant.cuh: the E4M3-output epilogue
+    for f in ("gemm.cuh", "ptx.cuh", "common.cuh") + (("quant.cuh",) if e4m3_out else ()):
         with open(os.path.join(ROOT, "fp8_fine_grained_26_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -531,7 +534,7 @@ def gemm_traffic(kernel, workload):
         return None
     with open(prof) as f:
         rec = json.load(f).get(f"{kernel}:{workload}")
-    if rec is None or rec.get("src_sha") != kernel_src_sha():
+    if rec is None or rec.get("src_sha") != kernel_src_sha(kernel.endswith("_e4m3")):
         return None
     return rec["bytes"]
 
@@ -744,6 +747,106 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------- quantisers alone
+# Each operand of the five configurations that the quantisers see, as
+# (label, kind, rows, cols): "act" takes the 1x128 rule, "w" the 128x128 rule,
+# "act+w" both operands of one GEMM in one fp8_quant_act_w launch.
+QUANT_ALONE_CASES = [
+    ("mla_q A 4096x1536", "act", (4096, 1536)),
+    ("mla_q W 24576x1536", "w", (24576, 1536)),
+    ("mla_q A+W (one launch)", "act+w", ((4096, 1536), (24576, 1536))),
+    ("mla_kv A 8192x512", "act", (8192, 512)),
+    ("mla_kv W 32768x512", "w", (32768, 512)),
+    ("mla_kv A+W (one launch)", "act+w", ((8192, 512), (32768, 512))),
+    ("experts X 4096x7168", "act", (4096, 7168)),
+    ("dgrad dY 8192x7168", "act", (8192, 7168)),
+    ("dgrad W stored 7168x18432", "w", (7168, 18432)),
+]
+
+
+def run_quant_alone(args):
+    """The quantisers timed alone: for each operand, `steps` back-to-back
+    calls captured in one CUDA graph, cycling over copies of the input whose
+    total size is at least twice L2 (so every call reads from HBM), timed with
+    CUDA events around the replay; the steady-state time per call and the
+    algorithmic GB/s (2 B read + 1 B written per element + 4 B per scale)
+    against the measured HBM peak.  One JSON line; `value` is the aggregate
+    GB/s over all the listed operands."""
+    import torch
+    import fp8_fine_grained_26_b300 as fp8
+    import synthetic
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    peaks, peak_src = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    dev = torch.device("cuda", local)
+    g = synthetic.generator(0, dev)
+
+    def qbytes(shape, kind):
+        R, C = shape
+        nscale = (C // 128) * R if kind == "act" else ((R + 127) // 128) * (C // 128)
+        return R * C * 3 + nscale * 4
+
+    results, tot_bytes, tot_ms = {}, 0.0, 0.0
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    clocks.start()
+    for label, kind, shape in QUANT_ALONE_CASES:
+        shapes = list(shape) if kind == "act+w" else [shape]
+        in_bytes = sum(r * c * 2 for r, c in shapes)
+        nsets = max(1, min(32, -(-2 * L2_BYTES // in_bytes)))
+        sets = [[synthetic.normal_bf16(sh, 1.0, g, dev) for sh in shapes] for _ in range(nsets)]
+        outs = [(torch.empty(sh, dtype=torch.uint8, device=dev),) for sh in shapes]
+        if kind == "act+w":
+            (M, K), (R, C) = shapes
+            sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+            sw = torch.empty(((R + 127) // 128, C // 128), dtype=torch.float32, device=dev)
+            call = lambda xs: fp8.fp8_quant_act_w(xs[0], xs[1], outs[0][0], sa, outs[1][0], sw)
+            nbytes = qbytes(shapes[0], "act") + qbytes(shapes[1], "w")
+        elif kind == "act":
+            (M, K), = shapes
+            sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+            call = lambda xs: fp8.fp8_quant_act_1x128(xs[0], outs[0][0], sa)
+            nbytes = qbytes(shapes[0], "act")
+        else:
+            (R, C), = shapes
+            sw = torch.empty(((R + 127) // 128, C // 128), dtype=torch.float32, device=dev)
+            call = lambda xs: fp8.fp8_quant_w_128x128(xs[0], outs[0][0], sw)
+            nbytes = qbytes(shapes[0], "w")
+        for i in range(max(3, args.warmup)):
+            call(sets[i % nsets])
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(args.steps):
+                call(sets[i % nsets])
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        if fp8.fp8bs_last_error() != 0:
+            raise RuntimeError(f"device error while timing {label}")
+        ms = e0.elapsed_time(e1) / args.steps
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        results[label] = {"us": round(ms * 1e3, 3), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+                          "bytes": int(nbytes), "input_copies": nsets}
+        tot_bytes += nbytes
+        tot_ms += ms
+        del sets, graph
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    value = tot_bytes / (tot_ms * 1e-3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "quantiser GB/s alone (back-to-back calls, inputs rotating over > 2x L2)",
+            "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "frac_hbm": round(value / hbm, 4),
+            "peak": {"hbm_gbs": hbm, "source": peak_src},
+            "dtype": "bf16 -> e4m3", "data": "synthetic N(0,1)", "quantisers": results, "clocks": clk,
+            "gpu_launches": args.steps * len(QUANT_ALONE_CASES)}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -761,6 +864,9 @@ def main(argv=None):
                     help="dense workloads: the step's output is C quantised per 1x128 row tile (E4M3 codes "
                          "+ scales), by the GEMM's epilogue (fused) or by the activation quantiser on the "
                          "BF16 C (unfused)")
+    ap.add_argument("--quant-alone", action="store_true",
+                    help="time the quantisers alone on every operand of the configurations "
+                         "(back-to-back calls in a CUDA graph, inputs rotating over > 2x L2)")
     ap.add_argument("--eager", action="store_true",
                     help="launch the timed steps one by one instead of replaying a CUDA graph")
     args = ap.parse_args(argv)
@@ -768,6 +874,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.quant_alone:
+        run_quant_alone(args)
     else:
         run_ours(args)
 
