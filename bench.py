@@ -18,6 +18,11 @@ bounded sample on the host cores, and SM clocks sampled during the timed
 region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+``--quant-alone`` instead times the quantisers alone on every operand of the
+configurations (back-to-back calls, inputs rotating over more than 2x L2) and
+prints their GB/s against HBM as its own JSON line.
+
 Multi-GPU: launched by torch.distributed.run, each rank runs an independent
 replica (the path has no exchange step); the time is the max over ranks.
 """
