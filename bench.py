@@ -475,6 +475,18 @@ def run_e2e(step, n, torch):
 
 
 # ---------------------------------------------------------------- CPU oracle
+def cpu_model():
+    """The host CPU's model name (from /proc/cpuinfo), for the baseline line."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
 def oracle_sample(workload_name, case_cpu_fn, rows=8):
     """The oracle, as it stands, on a bounded sample of the workload: quantise
     `rows` rows of A and the whole weight, then the float64 GEMM of those rows
@@ -669,11 +681,11 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu and args.workload == "wgrad":
         flops, secs, desc = oracle_sample_wgrad(case)
         cpu = {"value": round(flops / secs / 1e12, 9), "unit": "TFLOP/s", "cores": 1,
-               "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+               "kind": "oracle", "sample": desc, "seconds": round(secs, 2), "cpu_model": cpu_model()}
     elif rank == 0 and world == 1 and not args.no_cpu and args.workload not in ("experts", "experts_small"):
         flops, secs, desc = oracle_sample(args.workload, lambda: dense_host_inputs(case))
         cpu = {"value": round(flops / secs / 1e12, 9), "unit": "TFLOP/s", "cores": 1,
-               "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+               "kind": "oracle", "sample": desc, "seconds": round(secs, 2), "cpu_model": cpu_model()}
 
     if rank == 0:
         out = {
@@ -745,6 +757,7 @@ def run_reference(args):
            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
            "config": {"workload": case.name, "M": case.M, "N": case.N, "K": case.K},
            "cpu_baseline": {"value": round(v, 9), "unit": "TFLOP/s", "kind": "oracle", "cores": 1,
+                            "cpu_model": cpu_model(),
                             "sample": "per step: one row of A and one 128-column block of the "
                                       "weight quantised, and their 1x128 float64 GEMM block"},
            "e2e": {"value": round(v, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
