@@ -782,6 +782,15 @@ QUANT_ALONE_CASES = [
 ]
 
 
+def quant_alg_bytes(shape, kind):
+    """Algorithmic bytes of one quantisation of a BF16 [R][C] operand: 2 B
+    read and 1 B written per element, plus 4 B per scale (one per 1x128 tile
+    for "act", one per 128x128 block for "w")."""
+    R, C = shape
+    nscale = (C // 128) * R if kind == "act" else ((R + 127) // 128) * (C // 128)
+    return R * C * 3 + nscale * 4
+
+
 def run_quant_alone(args):
     """The quantisers timed alone: for each operand, `steps` back-to-back
     calls captured in one CUDA graph, cycling over copies of the input whose
@@ -800,11 +809,6 @@ def run_quant_alone(args):
     dev = torch.device("cuda", local)
     g = synthetic.generator(0, dev)
 
-    def qbytes(shape, kind):
-        R, C = shape
-        nscale = (C // 128) * R if kind == "act" else ((R + 127) // 128) * (C // 128)
-        return R * C * 3 + nscale * 4
-
     results, tot_bytes, tot_ms = {}, 0.0, 0.0
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
     clocks.start()
@@ -819,17 +823,17 @@ def run_quant_alone(args):
             sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
             sw = torch.empty(((R + 127) // 128, C // 128), dtype=torch.float32, device=dev)
             call = lambda xs: fp8.fp8_quant_act_w(xs[0], xs[1], outs[0][0], sa, outs[1][0], sw)
-            nbytes = qbytes(shapes[0], "act") + qbytes(shapes[1], "w")
+            nbytes = quant_alg_bytes(shapes[0], "act") + quant_alg_bytes(shapes[1], "w")
         elif kind == "act":
             (M, K), = shapes
             sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
             call = lambda xs: fp8.fp8_quant_act_1x128(xs[0], outs[0][0], sa)
-            nbytes = qbytes(shapes[0], "act")
+            nbytes = quant_alg_bytes(shapes[0], "act")
         else:
             (R, C), = shapes
             sw = torch.empty(((R + 127) // 128, C // 128), dtype=torch.float32, device=dev)
             call = lambda xs: fp8.fp8_quant_w_128x128(xs[0], outs[0][0], sw)
-            nbytes = qbytes(shapes[0], "w")
+            nbytes = quant_alg_bytes(shapes[0], "w")
         for i in range(max(3, args.warmup)):
             call(sets[i % nsets])
         graph = torch.cuda.CUDAGraph()

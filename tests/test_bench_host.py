@@ -1,0 +1,65 @@
+"""Host-side logic of bench.py that needs no GPU: the DRAM-traffic record
+lookup and its source hash, the quantisers' algorithmic byte count, and the
+reporting helpers."""
+import json
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _record():
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        return json.load(f)
+
+
+def test_traffic_lookup_returns_the_record_for_its_sources(monkeypatch):
+    # a capture is reported only while the kernel sources hash to the value
+    # stored with it; otherwise the bench reports null
+    rec = _record()
+    keys = [k for k in rec if not k.startswith("_")]
+    assert keys
+    for k in keys:
+        kernel, workload = k.split(":")
+        assert rec[k]["bytes"] == rec[k]["read"] + rec[k]["write"]
+        assert len(rec[k]["src_sha"]) == 16
+        assert bench.gemm_traffic(kernel, workload) in (rec[k]["bytes"], None), k
+        with monkeypatch.context() as m:
+            m.setattr(bench, "kernel_src_sha", lambda e4m3_out=False, s=rec[k]["src_sha"]: s)
+            assert bench.gemm_traffic(kernel, workload) == rec[k]["bytes"], k
+
+
+def test_traffic_lookup_is_null_for_unknown_workloads_and_stale_sources(monkeypatch):
+    assert bench.gemm_traffic("gemm", "no_such_workload") is None
+    monkeypatch.setattr(bench, "kernel_src_sha", lambda e4m3_out=False: "0" * 16)
+    assert bench.gemm_traffic("gemm", "mla_q") is None
+    assert bench.gemm_traffic("gemm_e4m3", "mla_kv") is None
+
+
+def test_source_hash_covers_the_encoder_only_for_the_e4m3_epilogue():
+    plain, e4m3 = bench.kernel_src_sha(), bench.kernel_src_sha(True)
+    assert len(plain) == 16 and len(e4m3) == 16 and plain != e4m3
+    assert bench.kernel_src_sha() == plain            # deterministic
+
+
+def test_quantiser_algorithmic_bytes():
+    # 3 bytes per element plus 4 per scale
+    assert bench.quant_alg_bytes((4096, 1536), "act") == 4096 * 1536 * 3 + 12 * 4096 * 4
+    assert bench.quant_alg_bytes((24576, 1536), "w") == 24576 * 1536 * 3 + 192 * 12 * 4
+    # a partial last row block still has its own weight scale
+    assert bench.quant_alg_bytes((200, 384), "w") == 200 * 384 * 3 + 2 * 3 * 4
+    # the operands timed alone are the configurations' own shapes
+    shapes = {label: shape for label, _, shape in bench.QUANT_ALONE_CASES}
+    assert shapes["mla_q A 4096x1536"] == (4096, 1536)
+    assert shapes["dgrad W stored 7168x18432"] == (7168, 18432)
+    assert all(c % 128 == 0 for _, kind, shape in bench.QUANT_ALONE_CASES
+               for (_, c) in (shape if kind == "act+w" else (shape,)))
+
+
+def test_cpu_model_is_a_name_or_none():
+    m = bench.cpu_model()
+    assert m is None or (isinstance(m, str) and m)
