@@ -4,10 +4,14 @@ One step = one pass of the whole path over one batch of synthetic input:
     quantise A per 1x128 tile, quantise W per 128x128 block, block-scaled
     FP8 GEMM with per-128-K promotion -> C (BF16)
 on the MLA query up-projection shape (A 4096x1536 with 0.1% x50 outliers,
-W 24576x1536, C 4096x24576) by default.  ``--workload`` selects another
-shape (mla_kv, dgrad, experts, tiny); for ``experts`` a step is the
-activation quantisation plus the grouped GEMM (expert weights are quantised
-once, before timing, as they are once per weight update).
+W 24576x1536, C 4096x24576) by default; A and W are quantised in one launch
+(``--quant split`` runs the two single-operand quantisers concurrently
+instead).  ``--workload`` selects another shape (mla_kv, dgrad, wgrad,
+experts, tiny, experts_small).  For ``experts`` a step is the gather +
+quantisation of the routed token rows plus the grouped GEMM (expert weights
+are quantised once, before timing, as they are once per weight update); for
+``wgrad`` it is the token-dimension quantisation of dY and X plus the
+weight-gradient GEMM.
 
 Printed (rank 0, one JSON line): whole-job GEMM TFLOP/s over the step time,
 per-kernel times from CUDA events on the launching stream, the GEMM's
