@@ -37,7 +37,7 @@ _STATUS_NAMES = {
 EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8_gemm_blockscaled",
             "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
             "fp8_quant_act_1x128_gather", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
-            "fp8bs_selftest_wait_timeout")
+            "fp8bs_selftest_wait_timeout", "fp8bs_selftest_set_wait_limit")
 
 
 class Fp8bsError(RuntimeError):
@@ -64,6 +64,7 @@ def _load():
         "fp8_grouped_gemm_blockscaled": [p, p, p, p, p, i32, i64, i64, i64, p, i32, i64, p],
         "fp8bs_last_error": [p],
         "fp8bs_selftest_wait_timeout": [i64, p],
+        "fp8bs_selftest_set_wait_limit": [i64],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -349,9 +350,15 @@ def fp8bs_selftest_wait_timeout(limit_us=20000, stream=None):
     _check(lib.fp8bs_selftest_wait_timeout(int(limit_us), _stream(stream)), "fp8bs_selftest_wait_timeout")
 
 
+def fp8bs_selftest_set_wait_limit(limit_ns):
+    """Test hook: time limit (ns) of the pipeline waits of quantisers and
+    single-CTA GEMMs launched from now on; 0 restores the default (2 s)."""
+    _check(lib.fp8bs_selftest_set_wait_limit(int(limit_ns)), "fp8bs_selftest_set_wait_limit")
+
+
 __all__ = ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8_gemm_blockscaled",
            "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
            "fp8_quant_act_1x128_gather", "FP8BS_ERR_INDEX",
            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout",
-           "Fp8bsError", "lib",
+           "fp8bs_selftest_set_wait_limit", "Fp8bsError", "lib",
            "LIB_PATH", "EXPORTED", "B_KMAJOR", "B_MNMAJOR", "OUT_BF16", "OUT_FP32"]

@@ -1,6 +1,7 @@
 // fp8bs.cu -- the C ABI of the library (see include/fp8bs.h): argument
 // validation, TMA tensor-map encoding and kernel launches.  One translation
 // unit so that the device error word is a single symbol per device.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -19,6 +20,7 @@ namespace {
 using namespace fp8bs;
 
 constexpr int kMaxDevices = 64;
+static_assert(MAX_EXPERTS == FP8BS_MAX_EXPERTS, "the header's expert limit is the kernel's");
 
 struct DeviceInfo {
     bool probed = false;
@@ -35,6 +37,15 @@ constexpr int PAIR_STAGES = 4;      // 4 x 32 KiB operand stages per CTA of a pa
 
 std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
+// Wait limit for single-CTA kernels set by fp8bs_selftest_set_wait_limit (0:
+// the default WAIT_LIMIT_NS).  CTA-pair GEMMs always use the default.
+std::atomic<uint64_t> g_test_wait_ns{0};
+
+uint64_t wait_limit_single()
+{
+    const uint64_t t = g_test_wait_ns.load(std::memory_order_relaxed);
+    return t ? t : WAIT_LIMIT_NS;
+}
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -269,6 +280,7 @@ int launch_dense(DeviceInfo *dev, const void *qA, const float *sA, const void *q
     g.offsets = nullptr;
     g.E = 1;
     g.c_fp32 = c_dtype == FP8BS_OUT_FP32;
+    g.wait_ns = pair ? WAIT_LIMIT_NS : wait_limit_single();
     CUtensorMap tmC = tmA;                        // unused unless a TMA epilogue runs
     if (qout) {
         // [M][N] codes, 128 x 128-byte boxes: one per warpgroup and tile
@@ -358,6 +370,13 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns)
     __syncwarp();
 }
 
+// Clears the given bits of the error word, atomically with respect to kernels
+// on other streams that may set bits meanwhile.
+__global__ void clear_error_bits_kernel(unsigned int bits)
+{
+    atomicAnd(&g_error_word, ~bits);
+}
+
 } // namespace fp8bs
 
 extern "C" {
@@ -385,7 +404,7 @@ int fp8_quant_act_1x128(const void *x_bf16, int64_t M, int64_t K, int64_t ldx, v
     const int64_t units = ((M + 127) / 128) * (K / 128);
     const int grid = (int)std::min<int64_t>(units, 3 * (int64_t)dev->num_sms);
     quant_act_1x128_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
-        tmX, M, K / 128, static_cast<uint8_t *>(q_e4m3), ldq, sA, units);
+        tmX, M, K / 128, static_cast<uint8_t *>(q_e4m3), ldq, sA, units, wait_limit_single());
     return launch_status();
 }
 
@@ -413,7 +432,7 @@ int fp8_quant_w_128x128(const void *w_bf16, int64_t R, int64_t C, int64_t ldw, v
     const int64_t units = RB * CB;
     const int grid = (int)std::min<int64_t>(units, 3 * (int64_t)dev->num_sms);
     quant_w_128x128_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
-        tmW, R, CB, static_cast<uint8_t *>(q_e4m3), ldq, sW, units);
+        tmW, R, CB, static_cast<uint8_t *>(q_e4m3), ldq, sW, units, wait_limit_single());
     return launch_status();
 }
 
@@ -476,6 +495,7 @@ int fp8_quant_act_w(const void *x_bf16, int64_t M, int64_t K, int64_t ldx, void 
     if (cw != 0)
         tmW = tmX;                                // never read: no weight units
     a.units = a.units_a + (cw == 0 ? ((R + 127) / 128) * a.CB : 0);
+    a.wait_ns = wait_limit_single();
     const int grid = (int)std::min<int64_t>(a.units, 3 * (int64_t)dev->num_sms);
     quant_act_w_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(tmX, tmW, a);
     return launch_status();
@@ -582,7 +602,7 @@ int fp8_quant_tokens_1x128(const void *x_bf16, int64_t T, int64_t F, int64_t ldx
     const int64_t units = (T / 128) * FB;
     const int grid = (int)std::min<int64_t>(units, 3 * (int64_t)dev->num_sms);
     quant_tokens_1x128_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
-        tmX, T, F, FB, static_cast<uint8_t *>(qT), ldq, s, units);
+        tmX, T, F, FB, static_cast<uint8_t *>(qT), ldq, s, units, wait_limit_single());
     return launch_status();
 }
 
@@ -639,6 +659,7 @@ int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA, const void *qB
     g.offsets = seg_offsets;
     g.E = E;
     g.c_fp32 = c_dtype == FP8BS_OUT_FP32;
+    g.wait_ns = wait_limit_single();
     CUtensorMap tmC = tmA;                        // unused unless the BF16 TMA epilogue runs
     g.c_tma = !g.c_fp32 && c_vector_ok(C, c_dtype, ldc) &&
               encode_c_bf16(&tmC, C, (uint64_t)N, (uint64_t)M_total, (uint64_t)ldc);
@@ -671,12 +692,22 @@ int fp8bs_last_error(cudaStream_t stream)
     unsigned int word = 0;
     if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof word) != cudaSuccess)
         return FP8BS_ERR_LAUNCH;
-    if (word != 0) {
-        const unsigned int zero = 0;
-        if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero) != cudaSuccess)
-            return FP8BS_ERR_LAUNCH;
-        return (word & 1u) ? FP8BS_ERR_TIMEOUT : FP8BS_ERR_INDEX;
-    }
+    if (word == 0)
+        return FP8BS_OK;
+    // Report one condition per call, the time-out first; clear only its bit,
+    // so that a second condition is reported by the next call.
+    const unsigned int bit = (word & 1u) ? 1u : (word & 2u) ? 2u : word;
+    clear_error_bits_kernel<<<1, 1, 0, stream>>>(bit);
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(stream) != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    return bit == 1u ? FP8BS_ERR_TIMEOUT : FP8BS_ERR_INDEX;
+}
+
+int fp8bs_selftest_set_wait_limit(int64_t limit_ns)
+{
+    if (limit_ns < 0 || limit_ns > (int64_t)WAIT_LIMIT_NS)
+        return FP8BS_ERR_ARG;
+    g_test_wait_ns.store((uint64_t)limit_ns, std::memory_order_relaxed);
     return FP8BS_OK;
 }
 

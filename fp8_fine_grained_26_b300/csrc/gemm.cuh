@@ -112,6 +112,7 @@ struct GemmArgs {
     int KB;             // K/128
     int NB128;          // ceil(N/128)
     int64_t num_tiles;  // dense: num_m_blk * num_n_blk (cluster pairs: num_m_pair * num_n_blk)
+    uint64_t wait_ns;   // time limit of every pipeline wait (WAIT_LIMIT_NS unless a test shortens it)
 };
 
 // tcgen05 instruction descriptor, kind::f8f6f4: D = F32 (bits 4-5 = 1),
@@ -179,10 +180,11 @@ struct SharedState {
     }
 };
 
-template <int S, int BSB, int SSF>
-__device__ __forceinline__ bool wait_bounded(const SharedState<S, BSB, SSF> &ss, uint32_t bar, uint32_t parity)
+template <int S, int BSB, int SSF, class Args>
+__device__ __forceinline__ bool wait_bounded(const SharedState<S, BSB, SSF> &ss, const Args &g, uint32_t bar,
+                                             uint32_t parity)
 {
-    return wait_bounded(bar, parity, ss.abort_flag());
+    return wait_bounded(bar, parity, ss.abort_flag(), g.wait_ns);
 }
 
 template <bool GROUPED, int S, int BSB, int SSF>
@@ -498,7 +500,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 for (int kb = 0; kb < g.KB; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_bounded(ss, ss.empty(s), ph ^ 1u)) { ok = false; break; }
+                    if (!wait_bounded(ss, g, ss.empty(s), ph ^ 1u)) { ok = false; break; }
                     const uint32_t fb = ss.full(s);
                     const uint32_t sa = ss.a_stage(s);
                     const uint32_t sb = ss.b_stage(s);
@@ -555,8 +557,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const uint32_t ph = (it / STAGES) & 1u;
                     const int p = pit & 1;
                     const uint32_t pph = (pit >> 1) & 1u;
-                    if (!wait_bounded(ss, ss.full(s), ph)) { ok = false; break; }
-                    if (!wait_bounded(ss, ss.pempty(p), pph ^ 1u)) { ok = false; break; }
+                    if (!wait_bounded(ss, g, ss.full(s), ph)) { ok = false; break; }
+                    if (!wait_bounded(ss, g, ss.pempty(p), pph ^ 1u)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t d = tmem_base + (uint32_t)(p * BN);
                     const uint32_t sa = ss.a_stage(s);
@@ -606,7 +608,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const Tile tl = tile_at<GROUPED, PAIR>(g, ss, t, rank);
                 for (int kb = 0; kb < g.KB; ++kb, ++sit) {
                     const int slot = (int)(sit % SCALE_SLOTS);
-                    if (!wait_bounded(ss, ss.sfree(slot), ((sit / SCALE_SLOTS) & 1u) ^ 1u)) { ok = false; break; }
+                    if (!wait_bounded(ss, g, ss.sfree(slot), ((sit / SCALE_SLOTS) & 1u) ^ 1u)) { ok = false; break; }
                     const uint32_t dst = ss.scale_slot(slot);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -667,7 +669,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const int64_t n_first = tl.n0 + wg * 128;
                     if (!epi_uses_boxes(g, tl, n_first))
                         continue;
-                    if (!wait_bounded(ss, ss.epi_full(wg), eit[wg]++ & 1u)) { ok = false; break; }
+                    if (!wait_bounded(ss, g, ss.epi_full(wg), eit[wg]++ & 1u)) { ok = false; break; }
                     ptx::tma_store_2d_hint(&tmC, ss.epi_box(wg, 0), (int32_t)n_first, (int32_t)tl.m0, c_policy);
                     if (!QOUT && n_first + 64 < g.N)       // second 64-column BF16 box exists
                         ptx::tma_store_2d_hint(&tmC, ss.epi_box(wg, 1), (int32_t)(n_first + 64), (int32_t)tl.m0,
@@ -703,7 +705,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             for (int kb = 0; kb < g.KB; ++kb, ++pit) {
                 // this slice's scales from the shared ring (staged by warp 2)
                 const int slot = (int)(pit % SCALE_SLOTS);
-                if (!wait_bounded(ss, ss.sready(slot), (pit / SCALE_SLOTS) & 1u)) { ok = false; break; }
+                if (!wait_bounded(ss, g, ss.sready(slot), (pit / SCALE_SLOTS) & 1u)) { ok = false; break; }
                 float sa, sb = 1.0f;
                 asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sa) : "r"(ss.scale_slot(slot) + 4 * row));
                 if constexpr (!TOK) {
@@ -715,7 +717,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const uint32_t col_scales = ss.scale_slot(slot) + 4 * (128 + col_half);
                 const int p = pit & 1;
                 const uint32_t pph = (pit >> 1) & 1u;
-                if (!wait_bounded(ss, ss.pfull(p), pph)) { ok = false; break; }
+                if (!wait_bounded(ss, g, ss.pfull(p), pph)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                        (uint32_t)(p * BN + col_half);
@@ -773,7 +775,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const Divisor d = make_divisor(max(mx & 0xFFFFu, mx >> 16));
                     if (row_ok)
                         g.sC[(n_first >> 7) * g.M + gm] = d.s;
-                    if (!wait_bounded(ss, ss.epi_free(wg), ph)) { ok = false; break; }
+                    if (!wait_bounded(ss, g, ss.epi_free(wg), ph)) { ok = false; break; }
                     const uint32_t buf = ss.epi_box(wg, 0) + (uint32_t)row * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
@@ -782,7 +784,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         ptx::st_shared_v4(buf + ((c ^ (lane & 7)) << 4), lo.x, lo.y, hi.x, hi.y);
                     }
                 } else {
-                    if (!wait_bounded(ss, ss.epi_free(wg), ph)) { ok = false; break; }
+                    if (!wait_bounded(ss, g, ss.epi_free(wg), ph)) { ok = false; break; }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t buf = ss.epi_box(wg, h) + (uint32_t)row * 128;

@@ -123,6 +123,7 @@ constexpr int quant_smem_bytes() { return 1024 + QSMEM_END; }
 struct QRing {
     uint32_t base;
     uint8_t *gbase;
+    uint64_t wait_ns;   // time limit of the ring's waits
     __device__ uint32_t stage(int s) const { return base + s * QUNIT_BYTES; }
     __device__ uint32_t full(int s) const { return base + QSMEM_BAR + 8 * s; }
     __device__ volatile uint32_t *abort() const
@@ -136,10 +137,11 @@ struct QRing {
     }
 };
 
-__device__ __forceinline__ QRing qring_setup()
+__device__ __forceinline__ QRing qring_setup(uint64_t wait_ns)
 {
     extern __shared__ uint8_t smem_raw[];
     QRing r;
+    r.wait_ns = wait_ns;
     const uint32_t raw = ptx::smem_u32(smem_raw);
     r.base = (raw + 1023u) & ~1023u;
     r.gbase = smem_raw + (r.base - raw);
@@ -176,7 +178,7 @@ __device__ __forceinline__ void qissue(const QRing &r, const CUtensorMap *tm, in
 __device__ __forceinline__ bool qwait(const QRing &r, int64_t j)
 {
     const int s = (int)(j % QSTAGES);
-    wait_bounded(r.full(s), (uint32_t)((j / QSTAGES) & 1), r.abort());
+    wait_bounded(r.full(s), (uint32_t)((j / QSTAGES) & 1), r.abort(), r.wait_ns);
     __syncthreads();
     return *r.abort() == 0u;
 }
@@ -304,9 +306,9 @@ __device__ __forceinline__ void w_unit(const QRing &r, int64_t j, int64_t rb, in
 
 __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_act_1x128_kernel(
     const __grid_constant__ CUtensorMap tmX, int64_t M, int64_t KB, uint8_t *__restrict__ q,
-    int64_t ldq, float *__restrict__ sA, int64_t units)
+    int64_t ldq, float *__restrict__ sA, int64_t units, uint64_t wait_ns)
 {
-    const QRing r = qring_setup();
+    const QRing r = qring_setup(wait_ns);
     const int tid = threadIdx.x;
     const int64_t mine = (int64_t)blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     int64_t issued = 0;
@@ -331,9 +333,9 @@ __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_act_1x128_kernel(
 
 __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_w_128x128_kernel(
     const __grid_constant__ CUtensorMap tmW, int64_t R, int64_t CB, uint8_t *__restrict__ q,
-    int64_t ldq, float *__restrict__ sW, int64_t units)
+    int64_t ldq, float *__restrict__ sW, int64_t units, uint64_t wait_ns)
 {
-    const QRing r = qring_setup();
+    const QRing r = qring_setup(wait_ns);
     const int tid = threadIdx.x;
     const int64_t mine = (int64_t)blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     int64_t issued = 0;
@@ -372,6 +374,7 @@ struct QuantPairArgs {
     int64_t ldqw;
     float *sW;
     int64_t units;                       // activation units + weight blocks
+    uint64_t wait_ns;                    // time limit of the ring's waits
 };
 
 __device__ __forceinline__ void qissue_pair(const QRing &r, const CUtensorMap *tmX, const CUtensorMap *tmW,
@@ -398,7 +401,7 @@ __device__ __forceinline__ void qissue_pair(const QRing &r, const CUtensorMap *t
 __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_act_w_kernel(
     const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const QuantPairArgs a)
 {
-    const QRing r = qring_setup();
+    const QRing r = qring_setup(a.wait_ns);
     const int tid = threadIdx.x;
     const int64_t units = a.units;
     const int64_t mine = (int64_t)blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
@@ -532,9 +535,9 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_gather_kernel(
 // max over the four quarters, exchanged through shared memory.
 __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_tokens_1x128_kernel(
     const __grid_constant__ CUtensorMap tmX, int64_t T, int64_t F, int64_t FB, uint8_t *__restrict__ q,
-    int64_t ldq, float *__restrict__ s, int64_t units)
+    int64_t ldq, float *__restrict__ s, int64_t units, uint64_t wait_ns)
 {
-    const QRing r = qring_setup();
+    const QRing r = qring_setup(wait_ns);
     const int tid = threadIdx.x;
     const int fp = tid & 63;
     const int qtr = tid >> 6;

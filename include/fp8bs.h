@@ -64,6 +64,7 @@ typedef enum {
 } fp8bs_status;
 
 enum { FP8BS_OUT_BF16 = 0, FP8BS_OUT_FP32 = 1 };
+enum { FP8BS_MAX_EXPERTS = 2048 };
 enum { FP8BS_B_KMAJOR = 0, FP8BS_B_MNMAJOR = 1 };
 
 /*
@@ -215,7 +216,11 @@ int fp8_gemm_wgrad(const void *qA, const float *sA, const void *qB, const float 
 
 /*
  * Grouped block-scaled FP8 GEMM for routed experts (one expert per segment of
- * rows).  Rows [seg_offsets[e], seg_offsets[e+1]) of qA belong to expert e:
+ * rows).  The pages' MoE layer routes every token to 8 of 256 routed experts,
+ * each a separate FFN with its own weights ("DeepSeek-V3 training
+ * walkthrough", section 一, DeepSeekMoE item), and runs its GEMMs in FP8 with
+ * the same fine-grained tiles; the rows routed to one expert are one segment
+ * here.  Rows [seg_offsets[e], seg_offsets[e+1]) of qA belong to expert e:
  *   C[m][n] = sum_kb sA[kb][m] * sB[e][n/128][kb] * sum_{k in kb} qA[m][k] * qB[e][n][k]
  *   qA          : [M_total][K] E4M3, sA [K/128][M_total] (quantise the
  *                 gathered rows, or gather rows and scale columns of a
@@ -226,7 +231,8 @@ int fp8_gemm_wgrad(const void *qA, const float *sA, const void *qB, const float 
  *                 that break these rules give unspecified output rows (never
  *                 an out-of-bounds access: rows are clamped to [0, M_total)).
  *   C           : [M_total][N], row stride ldc, BF16 or FP32.
- * Segments may be empty.  1 <= E <= 4096.
+ * Segments may be empty.  1 <= E <= FP8BS_MAX_EXPERTS (2048: the per-expert
+ * tile table lives in shared memory); any other E returns FP8BS_ERR_ARG.
  */
 int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA,
                                  const void *qB, const float *sB,
@@ -235,11 +241,18 @@ int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA,
                                  void *C, int c_dtype, int64_t ldc, cudaStream_t stream);
 
 /*
- * Synchronises `stream`, then reports and clears the current device's error
- * word: FP8BS_OK, FP8BS_ERR_INDEX (a gather index was out of range),
- * FP8BS_ERR_TIMEOUT (a kernel's pipeline wait exceeded its
- * time limit; that kernel's outputs are incomplete), or FP8BS_ERR_LAUNCH (the
- * CUDA runtime reported an error for the stream).
+ * Synchronises `stream`, then reports and clears one condition of the current
+ * device's error word: FP8BS_OK (no condition), FP8BS_ERR_TIMEOUT (a kernel's
+ * pipeline wait exceeded its time limit; that kernel's outputs are
+ * incomplete), FP8BS_ERR_INDEX (a gather index was out of range), or
+ * FP8BS_ERR_LAUNCH (the CUDA runtime reported an error for the stream).
+ * When both device conditions are set, the time-out is reported and cleared
+ * first and the index error stays set for the next call.
+ * The error word is ONE word per device, shared by every stream and every
+ * caller in the process: a condition raised by a kernel on another stream is
+ * reported (and cleared) by whichever call reads it first.  Only `stream` is
+ * synchronised, so kernels still running on other streams may set a bit
+ * after this call returns.
  */
 int fp8bs_last_error(cudaStream_t stream);
 
@@ -257,6 +270,23 @@ int fp8bs_last_error(cudaStream_t stream);
  * [1, 1000000]), FP8BS_ERR_DEVICE or FP8BS_ERR_LAUNCH.
  */
 int fp8bs_selftest_wait_timeout(int64_t limit_us, cudaStream_t stream);
+
+/*
+ * Test hook for the abort paths of the real kernels (no counterpart in the
+ * pages).  Sets the time limit, in nanoseconds, of every pipeline wait of the
+ * kernels launched AFTER this call by the quantisers (fp8_quant_act_1x128,
+ * fp8_quant_w_128x128, fp8_quant_act_w, fp8_quant_tokens_1x128) and by the
+ * single-CTA GEMMs (fp8_gemm_blockscaled / _e4m3_out / fp8_gemm_wgrad with
+ * M <= 128, and fp8_grouped_gemm_blockscaled).  CTA-pair GEMMs (M > 128)
+ * always keep the default limit.  limit_ns == 0 restores the default (2 s).
+ * With a limit of a few microseconds a wait that has to wait for memory runs
+ * out: the kernel records FP8BS_ERR_TIMEOUT, drains its own copies and
+ * MMAs, frees its tensor memory and returns; its outputs are incomplete but
+ * nothing outside them is written.  The setting is process-wide and not
+ * meant for concurrent use.  Returns FP8BS_OK, or FP8BS_ERR_ARG for a limit
+ * outside [0, 2e9].
+ */
+int fp8bs_selftest_set_wait_limit(int64_t limit_ns);
 
 #ifdef __cplusplus
 }

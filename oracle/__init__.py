@@ -46,6 +46,10 @@ def _load():
         lib.oracle_act_row_norms.restype = None
         lib.oracle_b_row_norms.argtypes = [p, p, i64, ctypes.c_int, i64, i64, p]
         lib.oracle_b_row_norms.restype = None
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_threads.restype = None
+        lib.oracle_get_threads.argtypes = []
+        lib.oracle_get_threads.restype = ctypes.c_int
         for f in ("oracle_quant_act_1x128", "oracle_quant_w_128x128", "oracle_gemm_f64",
                   "oracle_gemm_f64_at", "oracle_grouped_gemm_f64", "oracle_gemm_f64_tokens"):
             getattr(lib, f).restype = ctypes.c_int
@@ -67,6 +71,18 @@ def _as_c(a, dtype):
     if a.dtype != dtype:
         raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
     return np.ascontiguousarray(a)
+
+
+def set_threads(n: int) -> None:
+    """Number of OpenMP threads the GEMMs and row norms use (0 = all the
+    process may use).  Threads take whole output rows; each output element is
+    the same in-order sum over k on one thread, so results do not depend on it."""
+    _load().oracle_set_threads(int(n))
+
+
+def get_threads() -> int:
+    """Threads the GEMMs currently use."""
+    return int(_load().oracle_get_threads())
 
 
 def e4m3_encode(v: float) -> int:
@@ -223,6 +239,6 @@ def b_row_norms(qB, sB, b_major: int = 0) -> np.ndarray:
     return out
 
 
-__all__ = ["e4m3_encode", "e4m3_decode", "e4m3_encode_array", "e4m3_decode_table",
+__all__ = ["set_threads", "get_threads", "e4m3_encode", "e4m3_decode", "e4m3_encode_array", "e4m3_decode_table",
            "quant_act_1x128", "quant_w_128x128", "gemm_f64", "gemm_f64_at",
            "grouped_gemm_f64", "act_row_norms", "b_row_norms"]

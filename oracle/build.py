@@ -13,8 +13,9 @@ LIB = os.path.join(HERE, "liboracle.so")
 
 # IEEE arithmetic only: no fast-math, no contraction of a*b+c into an FMA,
 # no flush-to-zero.
+# OpenMP only spreads whole output rows over threads (see fp8_oracle.c).
 CFLAGS = ["-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math",
-          "-ffp-contract=off", "-fno-finite-math-only", "-Wall", "-Wextra"]
+          "-ffp-contract=off", "-fno-finite-math-only", "-fopenmp", "-Wall", "-Wextra"]
 
 
 def build(force: bool = False) -> str:

@@ -24,12 +24,19 @@
  *   are the plainest ones and are listed with the others in the design notes.
  *
  * Every function is the definition written out: no blocking, no reordering.
+ * The GEMMs spread whole output rows over OpenMP threads; every output
+ * element is one in-order sum over k on one thread, so the thread count does
+ * not change any result.
  * Floating-point environment: IEEE-754 binary32/binary64, round-to-nearest,
  * no flush-to-zero (x86-64 SSE arithmetic; compiled without fast-math).
  */
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* ------------------------------------------------------------------------ */
 /* bf16 -> fp32: a bf16 value is the top 16 bits of the binary32 pattern.    */
@@ -192,12 +199,44 @@ int oracle_quant_w_128x128(const uint16_t *w, int64_t R, int64_t C, int64_t ldw,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Threads.  The GEMMs below split their OUTPUT ROWS over OpenMP threads; each
+ * output element is still one sum over k = 0, 1, ..., K-1 in that order, on
+ * one thread, so the result does not depend on the thread count (pinned by a
+ * test that compares 1 thread with many).  0 = the OpenMP default. */
+static int g_threads = 0;
+
+void oracle_set_threads(int n) { g_threads = n < 0 ? 0 : n; }
+
+int oracle_get_threads(void)
+{
+#ifdef _OPENMP
+    return g_threads > 0 ? g_threads : omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Value of every code, from oracle_e4m3_decode: filled once, before any
+ * parallel loop reads it. */
+static double g_dec[256];
+static int g_dec_ready = 0;
+
+static void dec_table_init(void)
+{
+    if (g_dec_ready)
+        return;
+    for (int c = 0; c < 256; ++c)
+        g_dec[c] = oracle_e4m3_decode((uint8_t)c);
+    g_dec_ready = 1;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Dequantised operands, float64 (each value dec(q) * scale is exact: a 4-bit
  * by 24-bit significand product). */
 static double deq_a(const uint8_t *qA, const float *sA, int64_t M, int64_t lda,
                     int64_t m, int64_t k)
 {
-    return oracle_e4m3_decode(qA[m * lda + k]) * (double)sA[(k / 128) * M + m];
+    return g_dec[qA[m * lda + k]] * (double)sA[(k / 128) * M + m];
 }
 
 /* B element (n, k) of the GEMM's B^T operand.
@@ -208,28 +247,47 @@ static double deq_b(const uint8_t *qB, const float *sB, int64_t N, int64_t K,
 {
     const int64_t KB = K / 128, NB = (N + 127) / 128;
     if (b_major == 0)
-        return oracle_e4m3_decode(qB[n * ldb + k]) * (double)sB[(n / 128) * KB + k / 128];
-    return oracle_e4m3_decode(qB[k * ldb + n]) * (double)sB[(k / 128) * NB + n / 128];
+        return g_dec[qB[n * ldb + k]] * (double)sB[(n / 128) * KB + k / 128];
+    return g_dec[qB[k * ldb + n]] * (double)sB[(k / 128) * NB + n / 128];
 }
 
 /* C[m][n] = sum_k A^[m][k] * B^[n][k], in float64, over the dequantised
  * operands.  This is the result the block-scaled GEMM defines: per 128-wide
  * K-slice the FP8 product is scaled by sA * sB and summed in higher precision;
- * summing dequantised products gives the same exact-arithmetic value. */
+ * summing dequantised products gives the same exact-arithmetic value.
+ * Row m's dequantised values A^[m][0..K) are formed once into `arow` and
+ * reused for every n (the same numbers deq_a returns). */
 int oracle_gemm_f64(const uint8_t *qA, const float *sA, int64_t lda,
                     const uint8_t *qB, const float *sB, int64_t ldb, int b_major,
                     int64_t M, int64_t N, int64_t K, double *C, int64_t ldc)
 {
     if (K % 128 != 0)
         return -2;
-    for (int64_t m = 0; m < M; ++m)
-        for (int64_t n = 0; n < N; ++n) {
-            double acc = 0.0;
-            for (int64_t k = 0; k < K; ++k)
-                acc += deq_a(qA, sA, M, lda, m, k) * deq_b(qB, sB, N, K, ldb, b_major, n, k);
-            C[m * ldc + n] = acc;
+    dec_table_init();
+    int fail = 0;
+#pragma omp parallel num_threads(oracle_get_threads())
+    {
+        double *arow = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+        if (!arow) {
+#pragma omp atomic write
+            fail = 1;
         }
-    return 0;
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t m = 0; m < M; ++m) {
+            if (!arow)
+                continue;
+            for (int64_t k = 0; k < K; ++k)
+                arow[k] = deq_a(qA, sA, M, lda, m, k);
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += arow[k] * deq_b(qB, sB, N, K, ldb, b_major, n, k);
+                C[m * ldc + n] = acc;
+            }
+        }
+        free(arow);
+    }
+    return fail ? -5 : 0;
 }
 
 /* The same sum at `count` chosen (row, col) positions, for sampled checks of
@@ -241,10 +299,13 @@ int oracle_gemm_f64_at(const uint8_t *qA, const float *sA, int64_t lda,
 {
     if (K % 128 != 0)
         return -2;
+    for (int64_t i = 0; i < count; ++i)
+        if (rows[i] < 0 || rows[i] >= M || cols[i] < 0 || cols[i] >= N)
+            return -4;
+    dec_table_init();
+#pragma omp parallel for schedule(dynamic, 16) num_threads(oracle_get_threads())
     for (int64_t i = 0; i < count; ++i) {
         const int64_t m = rows[i], n = cols[i];
-        if (m < 0 || m >= M || n < 0 || n >= N)
-            return -4;
         double acc = 0.0;
         for (int64_t k = 0; k < K; ++k)
             acc += deq_a(qA, sA, M, lda, m, k) * deq_b(qB, sB, N, K, ldb, b_major, n, k);
@@ -265,10 +326,12 @@ int oracle_grouped_gemm_f64(const uint8_t *qA, const float *sA, int64_t lda,
 {
     if (K % 128 != 0)
         return -2;
+    dec_table_init();
     const int64_t NB = (N + 127) / 128, KB = K / 128;
     for (int e = 0; e < E; ++e) {
         const uint8_t *qBe = qB + (int64_t)e * N * K;
         const float *sBe = sB + (int64_t)e * NB * KB;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(oracle_get_threads())
         for (int64_t m = off[e]; m < off[e + 1]; ++m)
             for (int64_t n = 0; n < N; ++n) {
                 double acc = 0.0;
@@ -294,6 +357,8 @@ int oracle_gemm_f64_tokens(const uint8_t *qA, const float *sA, int64_t lda,
 {
     if (K % 128 != 0)
         return -2;
+    dec_table_init();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(oracle_get_threads())
     for (int64_t m = 0; m < M; ++m)
         for (int64_t n = 0; n < N; ++n) {
             double acc = 0.0;
@@ -309,6 +374,8 @@ int oracle_gemm_f64_tokens(const uint8_t *qA, const float *sA, int64_t lda,
 void oracle_act_row_norms(const uint8_t *qA, const float *sA, int64_t lda,
                           int64_t M, int64_t K, double *out)
 {
+    dec_table_init();
+#pragma omp parallel for schedule(static) num_threads(oracle_get_threads())
     for (int64_t m = 0; m < M; ++m) {
         double ss = 0.0;
         for (int64_t k = 0; k < K; ++k) {
@@ -322,6 +389,8 @@ void oracle_act_row_norms(const uint8_t *qA, const float *sA, int64_t lda,
 void oracle_b_row_norms(const uint8_t *qB, const float *sB, int64_t ldb, int b_major,
                         int64_t N, int64_t K, double *out)
 {
+    dec_table_init();
+#pragma omp parallel for schedule(static) num_threads(oracle_get_threads())
     for (int64_t n = 0; n < N; ++n) {
         double ss = 0.0;
         for (int64_t k = 0; k < K; ++k) {

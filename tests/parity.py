@@ -67,3 +67,80 @@ def b_norms_at(oracle, qb: np.ndarray, sb: np.ndarray, cols, b_major: int = 0) -
             out[i] = oracle.b_row_norms(np.ascontiguousarray(qb[:, n:n + 1]),
                                         np.ascontiguousarray(sb[:, nb:nb + 1]), b_major=1)[0]
     return out[inv]
+
+
+class ErrorStats:
+    """Running max / mean of the normalised error over many slabs of one output,
+    plus the count of zero-norm outputs that are not exactly 0."""
+
+    def __init__(self, what):
+        self.what, self.max, self.sum, self.n, self.bad_zero = what, 0.0, 0.0, 0, 0
+
+    def add(self, c_gpu: np.ndarray, c_ref: np.ndarray, a_norms: np.ndarray, b_norms: np.ndarray):
+        e, bad = gemm_errors(c_gpu, c_ref, a_norms, b_norms)
+        self.bad_zero += bad
+        if e.size:
+            self.max = max(self.max, float(e.max()))
+            self.sum += float(e.sum())
+            self.n += int(e.size)
+
+    @property
+    def mean(self):
+        return self.sum / self.n if self.n else 0.0
+
+    def check(self, max_e=MAX_E, mean_e=MEAN_E):
+        record_stats(self.what, self.max, self.mean, self.n)
+        assert self.bad_zero == 0, f"{self.what}: {self.bad_zero} zero-norm outputs are not exactly 0"
+        assert self.max <= max_e and self.mean <= mean_e, \
+            f"{self.what}: max e {self.max:.3e} (<= {max_e}), mean e {self.mean:.3e} (<= {mean_e})"
+
+
+def record_stats(what, max_e, mean_e, count):
+    """Appends one JSON line per checked output to the file named by the
+    PARITY_STATS environment variable, if set (a record of the errors seen)."""
+    import json
+    import os
+    path = os.environ.get("PARITY_STATS")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"what": what, "max_e": max_e, "mean_e": mean_e, "outputs": count}) + "\n")
+
+
+def compare_by_slabs(what, c_gpu, ref_rows, a_norms, b_norms, row_ranges):
+    """Every output element of the rows in `row_ranges` (a list of (r0, r1)),
+    one slab at a time: ``ref_rows(r0, r1)`` returns the float64 oracle rows
+    and ``c_gpu`` is the device output.  Returns the ErrorStats (checked)."""
+    st = ErrorStats(what)
+    for r0, r1 in row_ranges:
+        got = c_gpu[r0:r1].double().cpu().numpy()
+        st.add(got, ref_rows(r0, r1), a_norms[r0:r1], b_norms)
+    st.check()
+    return st
+
+
+def slabs(r0, r1, rows):
+    return [(a, min(a + rows, r1)) for a in range(r0, r1, rows)]
+
+
+def assert_e4m3_out_within_bound(codes, scales, ref, a_norms, b_norms, dec_table):
+    """Quantised-output check against the float64 oracle.  With x the BF16
+    output value, s = amax_tile(|x|)/448 and v = x/s, the E4M3 code is within
+    half a step of v: 2^-4 |v| in the normal range and 2^-10 below 2^-6.  So
+    |dec(q)*s - x| <= 2^-4 |x| + 2^-10 s, and the GEMM acceptance bound
+    E = 2e-3 ||a_m|| ||b_n|| covers |x - ref|.  codes [M][N] uint8, scales
+    [N/128][M] float; returns the largest error / bound ratio."""
+    M, N = ref.shape
+    e_bound = MAX_E * np.outer(a_norms, b_norms)
+    sc = np.asarray(scales, np.float64)
+    deq = dec_table[codes] * np.repeat(sc.T, 128, axis=1)
+    tiles = np.abs(ref).reshape(M, N // 128, 128)
+    amax_ref = np.repeat(tiles.max(axis=2), 128, axis=1)
+    e_tile = np.repeat(e_bound.reshape(M, N // 128, 128).max(axis=2), 128, axis=1)
+    bound = (2.0 ** -4) * (np.abs(ref) + e_bound) + (amax_ref + e_tile) / (448.0 * 1024.0) * 1.001 \
+        + e_bound * 1.001 + 1e-7 * np.abs(ref)
+    err = np.abs(deq - ref)
+    assert np.all(err <= bound), f"max excess {np.max(err - bound):.3e}"
+    sc_ref = tiles.max(axis=2).T / 448.0
+    et = e_bound.reshape(M, N // 128, 128).max(axis=2).T / 448.0
+    assert np.all(np.abs(sc - sc_ref) <= et + 2e-7 * sc_ref)
+    return float(np.max(err / np.maximum(bound, 1e-300)))

@@ -23,7 +23,7 @@ def test_header_declares_the_entry_points():
         "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8_gemm_blockscaled",
         "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
         "fp8_quant_act_1x128_gather", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
-        "fp8bs_selftest_wait_timeout"])
+        "fp8bs_selftest_wait_timeout", "fp8bs_selftest_set_wait_limit"])
 
 
 def test_library_loads_and_exports_every_declared_symbol():
@@ -116,6 +116,21 @@ def test_gemm_rejects_bad_arguments():
     assert gg(P(16), P(16), P(16), P(16), P(0), 2, 4, 4, 128, P(16), 0, 8, P(0)) == -1    # offsets
 
 
+def test_grouped_gemm_expert_count_limit():
+    """The header's FP8BS_MAX_EXPERTS (2048) is the largest accepted E: one
+    more is FP8BS_ERR_ARG before any device call; E == 2048 passes the host
+    checks (and, with no GPU, stops at the device check).  256 routed experts
+    per MoE layer is the pages' configuration ("DeepSeek-V3 training
+    walkthrough", section 一, DeepSeekMoE item)."""
+    text = open(HEADER).read()
+    assert "FP8BS_MAX_EXPERTS = 2048" in text
+    gg = _raw().fp8_grouped_gemm_blockscaled
+    assert gg(P(16), P(16), P(16), P(16), P(16), 2049, 4, 4, 128, P(16), 0, 8, P(0)) == -4
+    assert gg(P(16), P(16), P(16), P(16), P(16), 4096, 4, 4, 128, P(16), 0, 8, P(0)) == -4
+    if not os.path.exists("/dev/nvidia0"):
+        assert gg(P(16), P(16), P(16), P(16), P(16), 2048, 4, 4, 128, P(16), 0, 8, P(0)) == -6
+
+
 def test_e4m3_out_gemm_rejects_bad_arguments():
     lib = _raw()
     g = lib.fp8_gemm_blockscaled_e4m3_out
@@ -162,6 +177,9 @@ def test_selftest_rejects_out_of_range_limits():
     assert lib.fp8bs_selftest_wait_timeout(0, P(0)) == -4
     assert lib.fp8bs_selftest_wait_timeout(-5, P(0)) == -4
     assert lib.fp8bs_selftest_wait_timeout(1000001, P(0)) == -4
+    s = lib.fp8bs_selftest_set_wait_limit
+    assert s(-1) == -4 and s(2000000001) == -4
+    assert s(0) == 0                                  # the default; host-only
 
 
 @pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="checks the no-GPU answer")

@@ -12,7 +12,7 @@ from parity import host_u8
 from synthetic import bf16_bits, generator, normal_bf16
 
 pytestmark = pytest.mark.gpu
-fp8 = pytest.importorskip("fp8_fine_grained_26_b300")
+import fp8_fine_grained_26_b300 as fp8  # a missing or broken build fails loudly
 DEV = "cuda"
 
 

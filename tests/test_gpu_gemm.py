@@ -13,11 +13,11 @@ import torch
 import oracle
 import synthetic
 from synthetic import bf16_bits, generator, normal_bf16
-from parity import (assert_gemm_ok, b_norms_at, gemm_errors, host_f64, host_u8, sampled_errors)
+from parity import assert_gemm_ok, gemm_errors, host_f64, host_u8
 
 pytestmark = pytest.mark.gpu
 
-fp8 = pytest.importorskip("fp8_fine_grained_26_b300")
+import fp8_fine_grained_26_b300 as fp8  # a missing or broken build fails loudly
 DEV = "cuda"
 
 
@@ -193,45 +193,6 @@ def test_gemm_tiny_workload_full():
     full_check(c.a, c.w, 0, torch.float32, "tiny 128x256x512 fp32")
 
 
-def _sample_positions(M, N, count, seed):
-    rng = np.random.default_rng(seed)
-    rows = rng.integers(0, M, count)
-    cols = rng.integers(0, N, count)
-    # tile corners and ragged edges
-    edge_r = np.array([0, 127, 128, M - 1, M - 1, (M - 1) // 128 * 128])
-    edge_c = np.array([0, 255, 256, N - 1, 128, (N - 1) // 256 * 256])
-    return np.concatenate([rows, edge_r]), np.concatenate([cols, edge_c])
-
-
-def sampled_check(case, what, count=1500):
-    a, w, b_major = case.a, case.w, case.b_major
-    out = torch.float32 if case.out_fp32 else torch.bfloat16
-    qa, sa, qb, sb, c = gpu_path(a, w, b_major, out)
-    oqa, osa, oqb, osb = oracle_operands(a, w)
-    assert np.array_equal(host_u8(qa), oqa) and np.array_equal(host_u8(qb), oqb)
-    M, N = c.shape
-    rows, cols = _sample_positions(M, N, count, seed=M + N)
-    ref = oracle.gemm_f64_at(oqa, osa, oqb, osb, rows, cols, b_major=b_major)
-    got = c[torch.from_numpy(rows).to(DEV), torch.from_numpy(cols).to(DEV)].double().cpu().numpy()
-    ur, ui = np.unique(rows, return_inverse=True)
-    an = oracle.act_row_norms(oqa[ur], np.ascontiguousarray(osa[:, ur]))[ui]
-    bn = b_norms_at(oracle, oqb, osb, cols, b_major)
-    e, bad = sampled_errors(got, ref, an, bn)
-    assert_gemm_ok(e, bad, what)
-
-
-def test_gemm_mla_q_full_size_sampled():
-    sampled_check(synthetic.mla_q(device=DEV), "mla_q 4096x24576x1536")
-
-
-def test_gemm_mla_kv_full_size_sampled():
-    sampled_check(synthetic.mla_kv(device=DEV), "mla_kv 8192x32768x512")
-
-
-def test_gemm_dgrad_full_size_sampled():
-    sampled_check(synthetic.dgrad(device=DEV), "dgrad 8192x18432x7168 MN-major", count=800)
-
-
 # ------------------------------------------------------------------ grouped
 def grouped_gpu(case, out_dtype=torch.bfloat16):
     E, N, K = case.w.shape
@@ -274,33 +235,3 @@ def test_grouped_all_rows_in_one_expert_equals_dense():
     d = fp8.fp8_gemm_blockscaled(qa, sa, qb, sb, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert torch.equal(c, d)
-
-
-def test_grouped_experts_full_size_sampled():
-    case = synthetic.experts(device=DEV, keep_x=True)
-    c = grouped_gpu(case)
-    E, N, K = case.w.shape
-    off = case.offsets.cpu().numpy()
-    counts = np.diff(off)
-    assert counts.sum() == 4096 * 8
-    # oracle operands: quantise the 4096 tokens, then gather rows and scale
-    # columns (identical to quantising the gathered rows; pinned on the CPU)
-    tok = case.token_of_row.cpu().numpy()
-    qx, sx = oracle.quant_act_1x128(bf16_bits(case.x))
-    qa, sa = qx[tok], np.ascontiguousarray(sx[:, tok])
-    picks = sorted({int(np.argmax(counts)), int(np.argmin(counts)), 0, E - 1, 100})
-    rng = np.random.default_rng(0)
-    for e in picks:
-        r0, r1 = int(off[e]), int(off[e + 1])
-        if r1 == r0:
-            continue
-        qb, sb = oracle.quant_w_128x128(bf16_bits(case.w[e]))
-        rows = np.concatenate([rng.integers(r0, r1, 40), [r0, r1 - 1]])
-        cols = np.concatenate([rng.integers(0, N, 40), [0, N - 1]])
-        ref = oracle.gemm_f64_at(qa[r0:r1], np.ascontiguousarray(sa[:, r0:r1]), qb, sb,
-                                 rows - r0, cols)
-        got = c[torch.from_numpy(rows).to(DEV), torch.from_numpy(cols).to(DEV)].double().cpu().numpy()
-        an = oracle.act_row_norms(qa[rows], np.ascontiguousarray(sa[:, rows]))
-        bn = b_norms_at(oracle, qb, sb, cols)
-        e_, bad = sampled_errors(got, ref, an, bn)
-        assert_gemm_ok(e_, bad, f"experts e={e} n_e={r1 - r0}")

@@ -11,7 +11,7 @@ from parity import host_u8
 
 pytestmark = pytest.mark.gpu
 
-fp8 = pytest.importorskip("fp8_fine_grained_26_b300")
+import fp8_fine_grained_26_b300 as fp8  # a missing or broken build fails loudly
 DEV = "cuda"
 
 

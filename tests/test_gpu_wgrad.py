@@ -12,7 +12,7 @@ from parity import assert_gemm_ok, gemm_errors, host_f64, host_u8
 from synthetic import bf16_bits, generator, normal_bf16
 
 pytestmark = pytest.mark.gpu
-fp8 = pytest.importorskip("fp8_fine_grained_26_b300")
+import fp8_fine_grained_26_b300 as fp8  # a missing or broken build fails loudly
 DEV = "cuda"
 
 
@@ -82,24 +82,3 @@ def test_wgrad_promotion_exact():
     torch.cuda.synchronize()
     ref = oracle.gemm_f64_tokens(host_u8(qa), sa.cpu().numpy(), host_u8(qb), sb.cpu().numpy())
     assert np.array_equal(c.cpu().numpy().astype(np.float64), ref)
-
-
-def test_wgrad_full_size_sampled():
-    case = synthetic.wgrad(device=DEV)
-    qa, sa = fp8.fp8_quant_tokens_1x128(case.dy)
-    qb, sb = fp8.fp8_quant_tokens_1x128(case.x)
-    c = fp8.fp8_gemm_wgrad(qa, sa, qb, sb)
-    assert fp8.fp8bs_last_error() == 0
-    rng = np.random.default_rng(5)
-    rows = np.unique(np.concatenate([rng.integers(0, case.M, 6), [0, case.M - 1]]))
-    cols = np.unique(np.concatenate([rng.integers(0, case.N, 6), [0, case.N - 1]]))
-    qa_h, sa_h, qb_h, sb_h = host_u8(qa), sa.cpu().numpy(), host_u8(qb), sb.cpu().numpy()
-    # the sampled rows and columns of both quantised operands, re-quantised by the oracle from the inputs
-    oqa, osa = oracle.quant_tokens_1x128(bf16_bits(case.dy[:, rows]))
-    oqb, osb = oracle.quant_tokens_1x128(bf16_bits(case.x[:, cols]))
-    assert np.array_equal(qa_h[rows], oqa) and np.array_equal(qb_h[cols], oqb)
-    assert np.array_equal(sa_h[:, rows], osa) and np.array_equal(sb_h[:, cols], osb)
-    ref = oracle.gemm_f64_tokens(oqa, osa, oqb, osb)
-    got = host_f64(c)[np.ix_(rows, cols)]
-    e, bad = gemm_errors(got, ref, oracle.act_row_norms(oqa, osa), oracle.act_row_norms(oqb, osb))
-    assert_gemm_ok(e, bad, "wgrad full size, sampled")

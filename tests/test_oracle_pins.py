@@ -518,3 +518,62 @@ def test_weight_gradient_close_to_unquantised_product():
     eb = 2.0 ** -4 * np.abs(xf) + 2.0 ** -10 * np.repeat(sb.astype(np.float64), 128, axis=0)
     bound = np.abs(dyf).T @ eb + ea.T @ np.abs(xf) + ea.T @ eb
     assert np.all(np.abs(got - ref) <= bound * (1 + 1e-9))
+
+
+# ---------------------------------------------------------------- threads
+def _with_threads(n, fn):
+    old = oracle.get_threads()
+    try:
+        oracle.set_threads(n)
+        return fn()
+    finally:
+        oracle.set_threads(0 if old == oracle.get_threads() else old)
+
+
+@pytest.mark.parametrize("b_major", [0, 1])
+def test_gemm_result_does_not_depend_on_thread_count(b_major):
+    """The GEMMs split whole output rows over threads; each element is the
+    same in-order sum, so 1 thread and many give identical bits (the
+    single-threaded result is the plain loop)."""
+    qa, sa, qb, sb = _tiny_operands(37, 300, 512, seed=5)
+    if b_major == 1:
+        qb, sb = np.ascontiguousarray(qb.T), np.ascontiguousarray(sb.T)
+    one = _with_threads(1, lambda: oracle.gemm_f64(qa, sa, qb, sb, b_major=b_major))
+    many = _with_threads(max(2, os.cpu_count() or 2), lambda: oracle.gemm_f64(qa, sa, qb, sb, b_major=b_major))
+    np.testing.assert_array_equal(one, many)
+    rows, cols = np.arange(37) % 37, (np.arange(37) * 7) % 300
+    np.testing.assert_array_equal(_with_threads(3, lambda: oracle.gemm_f64_at(qa, sa, qb, sb, rows, cols,
+                                                                               b_major=b_major)),
+                                  one[rows, cols])
+
+
+def test_grouped_tokens_and_norms_do_not_depend_on_thread_count():
+    counts = [9, 0, 14, 3]
+    E, N, K = len(counts), 260, 256
+    M = sum(counts)
+    qa, sa = oracle.quant_act_1x128(_random_act(M, K, seed=3))
+    qbs, sbs = zip(*[oracle.quant_w_128x128(_random_w(N, K, seed=200 + e)) for e in range(E)])
+    qb, sb = np.stack(qbs), np.stack(sbs)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    runs = [_with_threads(n, lambda: oracle.grouped_gemm_f64(qa, sa, qb, sb, off)) for n in (1, 4)]
+    np.testing.assert_array_equal(runs[0], runs[1])
+    ta, tsa = oracle.quant_tokens_1x128(_random_act(256, 40, seed=4))
+    tb, tsb = oracle.quant_tokens_1x128(_random_act(256, 70, seed=6))
+    runs = [_with_threads(n, lambda: oracle.gemm_f64_tokens(ta, tsa, tb, tsb)) for n in (1, 5)]
+    np.testing.assert_array_equal(runs[0], runs[1])
+    norms = [_with_threads(n, lambda: oracle.act_row_norms(qa, sa)) for n in (1, 6)]
+    np.testing.assert_array_equal(norms[0], norms[1])
+
+
+def test_k_major_view_of_a_stored_kxn_weight_gives_the_same_gemm():
+    """The GPU parity tests compare the MN-major GEMM with the oracle's K-major
+    GEMM of the transposed weight (codes transposed, scale grid transposed):
+    both layouts of the oracle give the same bits."""
+    g = generator(23, "cpu")
+    a = bf16_bits(normal_bf16((20, 384), 1.0, g, "cpu"))
+    w_kn = bf16_bits(normal_bf16((384, 256), 0.02, g, "cpu"))            # stored [K][N]
+    qa, sa = oracle.quant_act_1x128(a)
+    qb, sb = oracle.quant_w_128x128(w_kn)
+    c_mn = oracle.gemm_f64(qa, sa, qb, sb, b_major=1)
+    c_k = oracle.gemm_f64(qa, sa, np.ascontiguousarray(qb.T), np.ascontiguousarray(sb.T), b_major=0)
+    np.testing.assert_array_equal(c_mn, c_k)
