@@ -187,6 +187,17 @@ __device__ __forceinline__ bool wait_bounded(const SharedState<S, BSB, SSF> &ss,
     return wait_bounded(bar, parity, ss.abort_flag(), g.wait_ns);
 }
 
+// A bounded wait whose outcome is the same for every lane of the warp: after a
+// time-out or an abort one lane may still have seen the phase complete, and
+// the warp-wide (.sync.aligned) tcgen05 loads that follow must be executed by
+// all lanes or by none.
+template <int S, int BSB, int SSF, class Args>
+__device__ __forceinline__ bool warp_wait(const SharedState<S, BSB, SSF> &ss, const Args &g, uint32_t bar,
+                                          uint32_t parity)
+{
+    return __all_sync(0xffffffffu, wait_bounded(ss, g, bar, parity));
+}
+
 template <bool GROUPED, int S, int BSB, int SSF>
 __device__ __forceinline__ int64_t total_tiles(const GemmArgs &g, const SharedState<S, BSB, SSF> &ss)
 {
@@ -705,7 +716,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             for (int kb = 0; kb < g.KB; ++kb, ++pit) {
                 // this slice's scales from the shared ring (staged by warp 2)
                 const int slot = (int)(pit % SCALE_SLOTS);
-                if (!wait_bounded(ss, g, ss.sready(slot), (pit / SCALE_SLOTS) & 1u)) { ok = false; break; }
+                if (!warp_wait(ss, g, ss.sready(slot), (pit / SCALE_SLOTS) & 1u)) { ok = false; break; }
                 float sa, sb = 1.0f;
                 asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sa) : "r"(ss.scale_slot(slot) + 4 * row));
                 if constexpr (!TOK) {
@@ -717,7 +728,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const uint32_t col_scales = ss.scale_slot(slot) + 4 * (128 + col_half);
                 const int p = pit & 1;
                 const uint32_t pph = (pit >> 1) & 1u;
-                if (!wait_bounded(ss, g, ss.pfull(p), pph)) { ok = false; break; }
+                if (!warp_wait(ss, g, ss.pfull(p), pph)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                        (uint32_t)(p * BN + col_half);
@@ -775,7 +786,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const Divisor d = make_divisor(max(mx & 0xFFFFu, mx >> 16));
                     if (row_ok)
                         g.sC[(n_first >> 7) * g.M + gm] = d.s;
-                    if (!wait_bounded(ss, g, ss.epi_free(wg), ph)) { ok = false; break; }
+                    if (!warp_wait(ss, g, ss.epi_free(wg), ph)) { ok = false; break; }
                     const uint32_t buf = ss.epi_box(wg, 0) + (uint32_t)row * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
@@ -784,7 +795,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         ptx::st_shared_v4(buf + ((c ^ (lane & 7)) << 4), lo.x, lo.y, hi.x, hi.y);
                     }
                 } else {
-                    if (!wait_bounded(ss, g, ss.epi_free(wg), ph)) { ok = false; break; }
+                    if (!warp_wait(ss, g, ss.epi_free(wg), ph)) { ok = false; break; }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t buf = ss.epi_box(wg, h) + (uint32_t)row * 128;
