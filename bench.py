@@ -3,11 +3,15 @@
 One step = one pass of the whole path over one batch of synthetic input:
     quantise A per 1x128 tile, quantise W per 128x128 block, block-scaled
     FP8 GEMM with per-128-K promotion -> C (BF16)
-on the MLA query up-projection shape (A 4096x1536 with 0.1% x50 outliers,
-W 24576x1536, C 4096x24576) by default; A and W are quantised in one launch
+on the data-gradient shape by default -- dY 8192x7168 (Student-t, nu = 3),
+W stored 7168x18432, dX = dY . W 8192x18432 BF16 -- the largest of the
+configurations that fit one GPU; A and W are quantised in one launch
 (``--quant split`` runs the two single-operand quantisers concurrently
-instead).  ``--workload`` selects another shape (mla_kv, dgrad, wgrad,
-experts, tiny, experts_small).  For ``experts`` a step is the gather +
+instead).  The default run adds, in the same JSON line, one sub-record per
+other configuration (MLA q, MLA kv, routed experts, weight gradient, tiny),
+each timed in its own region, and the quantisers-alone table.
+``--workload`` selects another headline shape (mla_q, mla_kv, wgrad,
+experts, tiny, experts_small) and then measures only that one.  For ``experts`` a step is the gather +
 quantisation of the routed token rows plus the grouped GEMM (expert weights
 are quantised once, before timing, as they are once per weight update); for
 ``wgrad`` it is the token-dimension quantisation of dY and X plus the
@@ -15,7 +19,8 @@ weight-gradient GEMM.
 
 Printed (rank 0, one JSON line): whole-job GEMM TFLOP/s over the step time,
 per-kernel times from CUDA events on the launching stream, the GEMM's
-roofline fraction against the measured peaks, quantiser GB/s against HBM,
+roofline fraction against the measured peaks (the burst peak unless the timed
+region lasts a second or more under the power cap), quantiser GB/s against HBM,
 an end-to-end number through the same C-ABI calls with pinned host buffers
 (host<->device copies inside the timed region), the oracle timed on a
 bounded sample on the host cores, and SM clocks sampled during the timed
@@ -491,10 +496,11 @@ def cpu_model():
     return None
 
 
-def oracle_sample(workload_name, case_cpu_fn, rows=8):
+def oracle_sample(workload_name, case_cpu_fn, rows=32):
     """The oracle, as it stands, on a bounded sample of the workload: quantise
-    `rows` rows of A and the whole weight, then the float64 GEMM of those rows
-    against every column.  Returns (flops, seconds, description)."""
+    `rows` rows of A and the whole weight (single-threaded C), then the
+    float64 GEMM of those rows against every column (its OpenMP threads over
+    the host cores).  Returns (flops, seconds, description)."""
     import numpy as np
     import oracle
     import synthetic
@@ -508,8 +514,8 @@ def oracle_sample(workload_name, case_cpu_fn, rows=8):
     N = c.shape[1]
     del np, synthetic
     return 2.0 * rows * N * K, dt, (f"{rows} rows of A x all {N} columns (quantise those rows and "
-                                    f"the whole {w_bits.shape[0]}x{w_bits.shape[1]} weight, "
-                                    f"float64 GEMM), single-threaded C")
+                                    f"the whole {w_bits.shape[0]}x{w_bits.shape[1]} weight, single-threaded; "
+                                    f"float64 GEMM on {oracle.get_threads()} threads)")
 
 
 def oracle_sample_wgrad(case, cols=2):
@@ -527,7 +533,7 @@ def oracle_sample_wgrad(case, cols=2):
     dt = time.perf_counter() - t0
     return 2.0 * c.shape[0] * c.shape[1] * case.T, dt, (
         f"all {case.M} dY features x {cols} X features over {case.T} tokens (quantise dY and those "
-        f"columns along tokens, float64 GEMM), single-threaded C")
+        f"columns along tokens, single-threaded; float64 GEMM on {oracle.get_threads()} threads)")
 
 
 def dense_host_inputs(case):
@@ -561,30 +567,50 @@ def gemm_traffic(kernel, workload):
 
 
 # ---------------------------------------------------------------- main arms
-def run_ours(args):
-    import torch
-    world, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dist = init_dist(world, "nccl")
-    import fp8_fine_grained_26_b300 as fp8
-    device = torch.device("cuda", local)
-    peaks, peak_src = load_peaks()
+# Peak rule: the measured burst peaks apply to a kernel in a short timed
+# region; the sustained ones only when the timed region is long (>= 1 s) AND
+# the clocks sampled during it show the power cap.
+SUSTAINED_MIN_S = 1.0
 
-    case = make_workload(args.workload, device)
-    if args.e4m3_out and args.workload in ("experts", "experts_small", "wgrad"):
+HEADLINE = "dgrad"                                  # the largest configuration that fits one GPU
+SUBRECORD_WORKLOADS = ("mla_q", "mla_kv", "experts", "wgrad", "tiny")
+
+
+def choose_peaks(peaks, region_s, clk):
+    """(fp8 tensor peak TFLOP/s, which one, why) for a timed region of
+    region_s seconds with clock record clk."""
+    burst = peaks["bf16_tflops"] * FP8_OVER_BF16
+    sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP8_OVER_BF16
+    capped = "sw_power_cap" in (clk.get("reasons") or [])
+    if region_s >= SUSTAINED_MIN_S and capped:
+        return sust, "sustained", f"timed region {region_s:.2f} s under sw_power_cap"
+    why = (f"timed region {region_s:.3f} s" + (" (< 1 s)" if region_s < SUSTAINED_MIN_S else "") +
+           ("" if capped else ", no power cap seen"))
+    return burst, "burst", why
+
+
+def build_step(name, case, fp8, torch, args):
+    if name in ("experts", "experts_small"):
+        return ExpertsStep(case, fp8, torch)
+    if name == "wgrad":
+        return WgradStep(case, fp8, torch)
+    return DenseStep(case, fp8, torch, e4m3_out=args.e4m3_out, quant=args.quant)
+
+
+def measure(args, name, fp8, torch, peaks, peak_src, world, rank, local, device, with_cpu, with_e2e):
+    """One workload: warm-up, K timed steps (one CUDA graph, events around
+    every kernel), end to end from host buffers, rooflines.  Returns the
+    record (the JSON line's body for the headline, a sub-record otherwise)."""
+    case = make_workload(name, device)
+    if args.e4m3_out and name in ("experts", "experts_small", "wgrad"):
         raise SystemExit("--e4m3-out applies to the dense forward workloads")
-    if args.workload in ("experts", "experts_small"):
-        step = ExpertsStep(case, fp8, torch)
-    elif args.workload == "wgrad":
-        step = WgradStep(case, fp8, torch)
-    else:
-        step = DenseStep(case, fp8, torch, e4m3_out=args.e4m3_out, quant=args.quant)
+    step = build_step(name, case, fp8, torch, args)
     stream = torch.cuda.current_stream()
 
     for i in range(args.warmup):
         step.run(i)
     if fp8.fp8bs_last_error() != 0:
-        raise RuntimeError("device error during warm-up")
+        raise RuntimeError(f"{name}: device error during warm-up")
 
     # The K timed steps are captured once into a CUDA graph (no host launch
     # gaps between kernels), with a timing event recorded before and after
@@ -620,19 +646,20 @@ def run_ours(args):
     clk = clocks.stop()
     barrier(world)
     if fp8.fp8bs_last_error() != 0:
-        raise RuntimeError("device error in the timed region")
+        raise RuntimeError(f"{name}: device error in the timed region")
 
     elapsed_ms = t_start.elapsed_time(t_end)
     elapsed_ms = max_over_ranks(elapsed_ms, world, device)
     per_kernel = {}
-    for j, name in enumerate(step.kernels):
-        per_kernel[name] = sum(e[2 * j].elapsed_time(e[2 * j + 1]) for e in evs) / args.steps
+    for j, kname in enumerate(step.kernels):
+        per_kernel[kname] = sum(e[2 * j].elapsed_time(e[2 * j + 1]) for e in evs) / args.steps
     ms_per_step = elapsed_ms / args.steps
     value = world * step.flops / (ms_per_step * 1e-3) / 1e12
+    del graph
 
     # ---- end-to-end through the same C-ABI calls from pinned host buffers
     e2e = None
-    if not args.no_e2e:
+    if with_e2e:
         n_e2e = max(3, min(args.steps, 20))
         barrier(world)
         e2e_ms = max_over_ranks(run_e2e(step, n_e2e, torch), world, device)
@@ -641,76 +668,110 @@ def run_ours(args):
                "h2d_bytes_per_step": int(step.h2d_bytes), "d2h_bytes_per_step": int(step.d2h_bytes),
                "pipelining": "copy in / kernels / copy out of consecutive steps overlap (3 streams)"}
 
-    # ---- roofline of the dominant kernel (the GEMM) and the quantisers
-    # The GEMM is timed inside a long run of steps (power-capped clocks), so
-    # its tensor peak is the sustained one; the burst fraction is reported
-    # beside it.  The bound is whichever of the tensor and HBM times of the
-    # kernel's algorithmic work is longer (the expert GEMM streams weights).
+    # ---- roofline of the dominant kernel (the GEMM) and the quantisers.  The
+    # bound is whichever of the tensor and HBM times of the kernel's
+    # algorithmic work is longer (the expert GEMM streams weights).
+    region_s = elapsed_ms * 1e-3
+    fp8_peak, peak_kind, peak_why = choose_peaks(peaks, region_s, clk)
+    fp8_burst = peaks["bf16_tflops"] * FP8_OVER_BF16
+    fp8_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP8_OVER_BF16
     gemm_name = "grouped_gemm" if "grouped_gemm" in step.kernels else "gemm"
     gemm_ms = per_kernel[gemm_name]
-    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
-    fp8_peak_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP8_OVER_BF16
     achieved = step.flops / (gemm_ms * 1e-3) / 1e12
     gemm_bytes = step.kernel_bytes[gemm_name]
     achieved_gbs = gemm_bytes / (gemm_ms * 1e-3) / 1e9
-    traffic = gemm_traffic(gemm_name + ("_e4m3" if getattr(step, "e4m3_out", None) == "fused" else ""),
-                           args.workload)
-    hbm_bound = gemm_bytes / (peaks["hbm_gbs"] * 1e9) > step.flops / (fp8_peak_sust * 1e12)
+    traffic = gemm_traffic(gemm_name + ("_e4m3" if getattr(step, "e4m3_out", None) == "fused" else ""), name)
+    hbm_bound = gemm_bytes / (peaks["hbm_gbs"] * 1e9) > step.flops / (fp8_peak * 1e12)
     if hbm_bound:
         roofline = {"kernel": gemm_name, "bound": "hbm", "achieved": round(achieved_gbs, 1),
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
                     "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs",
                     "tensor_tflops": round(achieved, 1),
-                    "tensor_frac_of_sustained": round(achieved / fp8_peak_sust, 4)}
+                    "tensor_frac_of_burst": round(achieved / fp8_burst, 4)}
     else:
         roofline = {"kernel": gemm_name, "bound": "tensor", "achieved": round(achieved, 1),
-                    "peak": round(fp8_peak_sust, 1), "unit": "TFLOP/s",
-                    "frac": round(achieved / fp8_peak_sust, 4), "traffic": traffic,
-                    "peak_source": f"{peak_src} bf16 sustained x {FP8_OVER_BF16} (nominal FP8:BF16)",
-                    "frac_of_burst": round(achieved / fp8_peak, 4)}
+                    "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                    "frac": round(achieved / fp8_peak, 4), "traffic": traffic,
+                    "peak_source": f"{peak_src} bf16 {peak_kind} x {FP8_OVER_BF16} (nominal FP8:BF16)",
+                    "peak_rule": f"{peak_kind}: {peak_why}",
+                    "frac_of_burst": round(achieved / fp8_burst, 4),
+                    "frac_of_sustained": round(achieved / fp8_sust, 4)}
     hbm = peaks["hbm_gbs"]
     kernels = {}
-    for name in step.kernels:
-        ms = per_kernel[name]
-        gbs = step.kernel_bytes[name] / (ms * 1e-3) / 1e9
+    for kname in step.kernels:
+        ms = per_kernel[kname]
+        gbs = step.kernel_bytes[kname] / (ms * 1e-3) / 1e9
         entry = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
-        if name in ("gemm", "grouped_gemm"):
+        if kname in ("gemm", "grouped_gemm"):
             entry["TFLOP/s"] = round(achieved, 1)
-            entry["frac_fp8_sustained"] = round(achieved / fp8_peak_sust, 4)
-            entry["frac_fp8_burst"] = round(achieved / fp8_peak, 4)
-        kernels[name] = entry
+            entry["frac_fp8_burst"] = round(achieved / fp8_burst, 4)
+            entry["frac_fp8_sustained"] = round(achieved / fp8_sust, 4)
+        kernels[kname] = entry
 
     # ---- CPU baseline (oracle) on a bounded sample, rank 0 at N=1 only
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and args.workload == "wgrad":
-        flops, secs, desc = oracle_sample_wgrad(case)
-        cpu = {"value": round(flops / secs / 1e12, 9), "unit": "TFLOP/s", "cores": 1,
-               "kind": "oracle", "sample": desc, "seconds": round(secs, 2), "cpu_model": cpu_model()}
-    elif rank == 0 and world == 1 and not args.no_cpu and args.workload not in ("experts", "experts_small"):
-        flops, secs, desc = oracle_sample(args.workload, lambda: dense_host_inputs(case))
-        cpu = {"value": round(flops / secs / 1e12, 9), "unit": "TFLOP/s", "cores": 1,
-               "kind": "oracle", "sample": desc, "seconds": round(secs, 2), "cpu_model": cpu_model()}
+    if with_cpu and rank == 0 and world == 1:
+        import oracle
+        if name == "wgrad":
+            flops, secs, desc = oracle_sample_wgrad(case)
+        elif name not in ("experts", "experts_small"):
+            flops, secs, desc = oracle_sample(name, lambda: dense_host_inputs(case))
+        else:
+            flops = None
+        if flops is not None:
+            cpu = {"value": round(flops / secs / 1e12, 9), "unit": "TFLOP/s", "cores": oracle.get_threads(),
+                   "kind": "oracle", "sample": desc, "seconds": round(secs, 2), "cpu_model": cpu_model()}
 
+    rec = {
+        "value": round(value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms_per_step, 5),
+        "config": {"workload": case.name if hasattr(case, "name") else name,
+                   "M": step.M, "N": step.N, "K": step.K,
+                   "step": step.schedule,
+                   "out": (f"e4m3 + fp32 scale per 1x128 row tile ({step.e4m3_out})"
+                           if getattr(step, "e4m3_out", None)
+                           else "bf16" if step.c.dtype == torch.bfloat16 else "fp32"),
+                   "l2": (f"inputs rotate over {step.nsets} sets (> 2x the 126 MB L2)"
+                          if step.nsets > 1 else "inputs larger than L2"),
+                   "parallelism": f"replicas x{world}",
+                   "launch": "eager" if args.eager else "CUDA graph of the timed steps"},
+        "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": step.launches_per_step * args.steps * world,
+        "clocks": clk,
+    }
+    del step, case, evs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    import fp8_fine_grained_26_b300 as fp8
+    device = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    common = (fp8, torch, peaks, peak_src, world, rank, local, device)
+
+    head = measure(args, args.workload, *common, with_cpu=not args.no_cpu, with_e2e=not args.no_e2e)
+    out = {"metric": METRIC, "value": head.pop("value"), "unit": head.pop("unit"), "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": head.pop("ms_per_step"),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic"}
+    out.update(head)
+    if args.subrecords:
+        # the other configurations, each its own timed region in this run
+        subs = {}
+        for wl in SUBRECORD_WORKLOADS:
+            if wl == args.workload:
+                continue
+            r = measure(args, wl, *common, with_cpu=False, with_e2e=not args.no_e2e)
+            subs[wl] = {k: r[k] for k in ("value", "unit", "ms_per_step", "config", "kernels", "roofline",
+                                          "e2e", "gpu_launches", "clocks")}
+        out["workloads"] = subs
+        out["quantisers_alone"] = run_quant_alone(args, emit=False)
     if rank == 0:
-        out = {
-            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
-            "config": {"workload": case.name if hasattr(case, "name") else args.workload,
-                       "M": step.M, "N": step.N, "K": step.K,
-                       "step": step.schedule,
-                       "out": (f"e4m3 + fp32 scale per 1x128 row tile ({step.e4m3_out})"
-                               if getattr(step, "e4m3_out", None)
-                               else "bf16" if step.c.dtype == torch.bfloat16 else "fp32"),
-                       "l2": (f"inputs rotate over {step.nsets} sets (> 2x the 126 MB L2)"
-                              if step.nsets > 1 else "inputs larger than L2"),
-                       "parallelism": f"replicas x{world}",
-                       "launch": "eager" if args.eager else "CUDA graph of the timed steps"},
-            "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": step.launches_per_step * args.steps * world,
-            "clocks": clk,
-        }
         print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -795,14 +856,15 @@ def quant_alg_bytes(shape, kind):
     return R * C * 3 + nscale * 4
 
 
-def run_quant_alone(args):
+def run_quant_alone(args, emit=True):
     """The quantisers timed alone: for each operand, `steps` back-to-back
     calls captured in one CUDA graph, cycling over copies of the input whose
     total size is at least twice L2 (so every call reads from HBM), timed with
     CUDA events around the replay; the steady-state time per call and the
     algorithmic GB/s (2 B read + 1 B written per element + 4 B per scale)
-    against the measured HBM peak.  One JSON line; `value` is the aggregate
-    GB/s over all the listed operands."""
+    against the measured HBM peak.  One JSON line (or, with emit=False, the
+    same record returned); `value` is the aggregate GB/s over all the listed
+    operands."""
     import torch
     import fp8_fine_grained_26_b300 as fp8
     import synthetic
@@ -838,11 +900,12 @@ def run_quant_alone(args):
             sw = torch.empty(((R + 127) // 128, C // 128), dtype=torch.float32, device=dev)
             call = lambda xs: fp8.fp8_quant_w_128x128(xs[0], outs[0][0], sw)
             nbytes = quant_alg_bytes(shapes[0], "w")
+        calls = args.steps if emit else max(args.steps, 200)
         for i in range(max(3, args.warmup)):
             call(sets[i % nsets])
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            for i in range(args.steps):
+            for i in range(calls):
                 call(sets[i % nsets])
         graph.replay()
         torch.cuda.synchronize()
@@ -853,7 +916,7 @@ def run_quant_alone(args):
         torch.cuda.synchronize()
         if fp8.fp8bs_last_error() != 0:
             raise RuntimeError(f"device error while timing {label}")
-        ms = e0.elapsed_time(e1) / args.steps
+        ms = e0.elapsed_time(e1) / calls
         gbs = nbytes / (ms * 1e-3) / 1e9
         results[label] = {"us": round(ms * 1e3, 3), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
                           "bytes": int(nbytes), "input_copies": nsets}
@@ -863,14 +926,16 @@ def run_quant_alone(args):
         torch.cuda.empty_cache()
     clk = clocks.stop()
     value = tot_bytes / (tot_ms * 1e-3) / 1e9
-    if rank == 0:
-        print(json.dumps({
-            "metric": "quantiser GB/s alone (back-to-back calls, inputs rotating over > 2x L2)",
-            "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-            "higher_is_better": True, "frac_hbm": round(value / hbm, 4),
-            "peak": {"hbm_gbs": hbm, "source": peak_src},
-            "dtype": "bf16 -> e4m3", "data": "synthetic N(0,1)", "quantisers": results, "clocks": clk,
-            "gpu_launches": args.steps * len(QUANT_ALONE_CASES)}), flush=True)
+    rec = {
+        "metric": "quantiser GB/s alone (back-to-back calls, inputs rotating over > 2x L2)",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "frac_hbm": round(value / hbm, 4),
+        "peak": {"hbm_gbs": hbm, "source": peak_src},
+        "dtype": "bf16 -> e4m3", "data": "synthetic N(0,1)", "quantisers": results, "clocks": clk,
+        "gpu_launches": calls * len(QUANT_ALONE_CASES)}
+    if emit and rank == 0:
+        print(json.dumps(rec), flush=True)
+    return rec
 
 
 def main(argv=None):
@@ -878,8 +943,12 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="mla_q",
-                    choices=["mla_q", "mla_kv", "dgrad", "experts", "tiny", "wgrad", "experts_small"])
+    ap.add_argument("--workload", default=HEADLINE,
+                    choices=["mla_q", "mla_kv", "dgrad", "experts", "tiny", "wgrad", "experts_small"],
+                    help="the headline workload (default: dgrad, the largest configuration)")
+    ap.add_argument("--no-subrecords", action="store_true",
+                    help="with the default workload, skip the other configurations' sub-records and the "
+                         "quantisers-alone table")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end run")
@@ -898,6 +967,7 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    args.subrecords = args.workload == HEADLINE and not args.no_subrecords and not args.e4m3_out
     if args.impl == "reference":
         run_reference(args)
     elif args.quant_alone:

@@ -63,3 +63,26 @@ def test_quantiser_algorithmic_bytes():
 def test_cpu_model_is_a_name_or_none():
     m = bench.cpu_model()
     assert m is None or (isinstance(m, str) and m)
+
+
+def test_peak_rule_burst_unless_long_and_power_capped():
+    import bench
+    peaks = {"bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "hbm_gbs": 6400.0}
+    p, kind, _ = bench.choose_peaks(peaks, 0.004, {"reasons": []})
+    assert (p, kind) == (3600.0, "burst")
+    p, kind, _ = bench.choose_peaks(peaks, 0.2, {"reasons": ["sw_power_cap"]})      # short: burst
+    assert kind == "burst"
+    p, kind, _ = bench.choose_peaks(peaks, 3.0, {"reasons": []})                     # long, no cap
+    assert kind == "burst"
+    p, kind, why = bench.choose_peaks(peaks, 3.0, {"reasons": ["sw_power_cap"]})
+    assert (p, kind) == (2800.0, "sustained") and "power_cap" in why
+
+
+def test_default_headline_is_the_largest_configuration():
+    import bench
+    sizes = {"mla_q": (4096, 24576, 1536), "mla_kv": (8192, 32768, 512), "dgrad": (8192, 18432, 7168),
+             "tiny": (128, 256, 512), "experts": (32768, 2048, 7168)}
+    flops = {k: 2.0 * m * n * k_ for k, (m, n, k_) in sizes.items()}
+    # the expert GEMM has the most FLOPs but is HBM-bound on weights; of the
+    # dense GEMMs dgrad is the largest
+    assert max((v, k) for k, v in flops.items() if k != "experts")[1] == bench.HEADLINE
