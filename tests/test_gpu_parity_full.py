@@ -177,7 +177,7 @@ def test_grouped_max_experts_accepted():
 
 
 def test_wgrad_every_cta_runs_several_tiles():
-    T, M, N = 512, 1000, 14000
+    T, M, N = 512, 1000, 14336
     tiles = cdiv(cdiv(M, BM), 2) * cdiv(N, BN)
     assert tiles >= 3 * (num_sms() // 2)
     case = synthetic.wgrad_case("wgrad multi-tile", T, M, N, seed=19, device=DEV)
