@@ -46,6 +46,13 @@ def _load():
         lib.oracle_act_row_norms.restype = None
         lib.oracle_b_row_norms.argtypes = [p, p, i64, ctypes.c_int, i64, i64, p]
         lib.oracle_b_row_norms.restype = None
+        lib.oracle_quant_per_tensor.argtypes = [p, i64, i64, i64, p, i64, p]
+        lib.oracle_quant_per_tensor.restype = ctypes.c_int
+        lib.oracle_quant_per_tensor_delayed.argtypes = [p, i64, i64, i64, ctypes.c_float, p, i64, p, p]
+        lib.oracle_quant_per_tensor_delayed.restype = ctypes.c_int
+        lib.oracle_gemm_f64_per_tensor.argtypes = [p, ctypes.c_float, i64, p, ctypes.c_float, i64, ctypes.c_int,
+                                                   i64, i64, i64, p, i64]
+        lib.oracle_gemm_f64_per_tensor.restype = ctypes.c_int
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         lib.oracle_set_threads.restype = None
         lib.oracle_get_threads.argtypes = []
@@ -218,6 +225,44 @@ def gemm_f64_tokens(qA, sA, qB, sB) -> np.ndarray:
     return C
 
 
+def quant_per_tensor(x_bf16_bits):
+    """Per-tensor quantisation with the tensor's own amax (current scaling):
+    one scale fp32(amax/448) for every element.  Returns ``(q uint8 [R, C],
+    scale float32)``."""
+    x = _as_c(x_bf16_bits, np.uint16)
+    R, C = x.shape
+    q = np.empty((R, C), np.uint8)
+    s = np.empty(1, np.float32)
+    _check(_load().oracle_quant_per_tensor(_ptr(x), R, C, C, _ptr(q), C, _ptr(s)), "quant_per_tensor")
+    return q, np.float32(s[0])
+
+
+def quant_per_tensor_delayed(x_bf16_bits, amax_in):
+    """Per-tensor quantisation with a given amax (delayed scaling): scale =
+    fp32(amax_in/448), larger values saturate.  Returns ``(q, scale, amax of
+    this tensor)``."""
+    x = _as_c(x_bf16_bits, np.uint16)
+    R, C = x.shape
+    q = np.empty((R, C), np.uint8)
+    s = np.empty(1, np.float32)
+    a = np.empty(1, np.float32)
+    _check(_load().oracle_quant_per_tensor_delayed(_ptr(x), R, C, C, ctypes.c_float(float(amax_in)), _ptr(q), C,
+                                                   _ptr(s), _ptr(a)), "quant_per_tensor_delayed")
+    return q, np.float32(s[0]), np.float32(a[0])
+
+
+def gemm_f64_per_tensor(qA, sA, qB, sB, b_major: int = 0) -> np.ndarray:
+    """float64 ``C = (sA qA^) . (sB qB^)^T`` for per-tensor scales sA, sB
+    (scalars); ``qB`` is ``[N, K]`` (b_major 0) or ``[K, N]`` (b_major 1)."""
+    qA, qB = _as_c(qA, np.uint8), _as_c(qB, np.uint8)
+    M, N, K = _gemm_shapes(qA, qB, b_major)
+    C = np.empty((M, N), np.float64)
+    _check(_load().oracle_gemm_f64_per_tensor(_ptr(qA), ctypes.c_float(float(sA)), K, _ptr(qB),
+                                              ctypes.c_float(float(sB)), qB.shape[1], b_major, M, N, K,
+                                              _ptr(C), N), "gemm_per_tensor")
+    return C
+
+
 def act_row_norms(qA, sA) -> np.ndarray:
     """||A^[m, :]||_2 of the dequantised activation rows."""
     qA, sA = _as_c(qA, np.uint8), _as_c(sA, np.float32)
@@ -241,4 +286,5 @@ def b_row_norms(qB, sB, b_major: int = 0) -> np.ndarray:
 
 __all__ = ["set_threads", "get_threads", "e4m3_encode", "e4m3_decode", "e4m3_encode_array", "e4m3_decode_table",
            "quant_act_1x128", "quant_w_128x128", "gemm_f64", "gemm_f64_at",
-           "grouped_gemm_f64", "act_row_norms", "b_row_norms"]
+           "grouped_gemm_f64", "act_row_norms", "b_row_norms", "quant_per_tensor",
+           "quant_per_tensor_delayed", "gemm_f64_per_tensor"]

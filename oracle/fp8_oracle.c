@@ -400,3 +400,74 @@ void oracle_b_row_norms(const uint8_t *qB, const float *sB, int64_t ldb, int b_m
         out[n] = sqrt(ss);
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Per-tensor scaling: the contrast to the fine-grained scheme.  The pages
+ * describe their 1x128 / 128x128 groups as finer than scaling a whole tensor
+ * by one factor, which lets a few outliers set the scale of every element
+ * [qqstock.cn walkthrough, FP8 section: fine-grained rather than per-tensor
+ * quantisation; "DeepSeek-V3 Technical Report digest", section 3,
+ * fine-grained quantisation bullet].  The same rules apply with the group
+ * being the whole tensor: scale = fp32(amax / 448), q = enc(fp32(x / scale)),
+ * an all-zero tensor gets scale 0 and codes enc(x).                          */
+static float tensor_amax(const uint16_t *x, int64_t R, int64_t C, int64_t ldx)
+{
+    float amax = 0.0f;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            float a = fabsf(bf16_bits_to_float(x[r * ldx + c]));
+            if (a > amax)
+                amax = a;
+        }
+    return amax;
+}
+
+/* Current scaling: the scale comes from this tensor's own amax. */
+int oracle_quant_per_tensor(const uint16_t *x, int64_t R, int64_t C, int64_t ldx,
+                            uint8_t *q, int64_t ldq, float *scale)
+{
+    const float s = group_scale(tensor_amax(x, R, C, ldx));
+    *scale = s;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c)
+            q[r * ldq + c] = quantise_element(bf16_bits_to_float(x[r * ldx + c]), s);
+    return 0;
+}
+
+/* Delayed scaling: the scale comes from an amax given by the caller (the
+ * largest amax of earlier steps), s = fp32(amax_in / 448); values beyond
+ * 448 * s saturate to +-448.  Also returns this tensor's amax, the value a
+ * caller records for later steps. */
+int oracle_quant_per_tensor_delayed(const uint16_t *x, int64_t R, int64_t C, int64_t ldx,
+                                    float amax_in, uint8_t *q, int64_t ldq, float *scale,
+                                    float *amax_out)
+{
+    const float s = group_scale(amax_in);
+    *scale = s;
+    *amax_out = tensor_amax(x, R, C, ldx);
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c)
+            q[r * ldq + c] = quantise_element(bf16_bits_to_float(x[r * ldx + c]), s);
+    return 0;
+}
+
+/* GEMM over per-tensor quantised operands:
+ *   C[m][n] = sum_k dec(qA[m][k]) * sA * dec(qB(n, k)) * sB   (float64)
+ * qB is [N][K] (b_major 0) or stored [K][N] (b_major 1). */
+int oracle_gemm_f64_per_tensor(const uint8_t *qA, float sA, int64_t lda,
+                               const uint8_t *qB, float sB, int64_t ldb, int b_major,
+                               int64_t M, int64_t N, int64_t K, double *C, int64_t ldc)
+{
+    dec_table_init();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(oracle_get_threads())
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const uint8_t b = b_major == 0 ? qB[n * ldb + k] : qB[k * ldb + n];
+                acc += g_dec[qA[m * lda + k]] * (double)sA * (g_dec[b] * (double)sB);
+            }
+            C[m * ldc + n] = acc;
+        }
+    return 0;
+}

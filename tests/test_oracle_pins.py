@@ -577,3 +577,100 @@ def test_k_major_view_of_a_stored_kxn_weight_gives_the_same_gemm():
     c_mn = oracle.gemm_f64(qa, sa, qb, sb, b_major=1)
     c_k = oracle.gemm_f64(qa, sa, np.ascontiguousarray(qb.T), np.ascontiguousarray(sb.T), b_major=0)
     np.testing.assert_array_equal(c_mn, c_k)
+
+
+# ---------------------------------------------------------------- per-tensor scaling
+def _numpy_torch_per_tensor(x_bits, amax):
+    """Independent restatement: scale by numpy fp32 IEEE division, codes by
+    torch's float8_e4m3fn conversion (saturated first: torch maps > 464 to
+    NaN), zero scale -> codes of x itself."""
+    xf = bf16_bits_to_f32(x_bits)
+    s = np.float32(amax) / np.float32(448.0)
+    y = xf / s if s != 0 else xf
+    y = np.clip(y, -448.0, 448.0).astype(np.float32)
+    return torch_encode(y), s
+
+
+def test_per_tensor_matches_numpy_division_and_torch_encoder():
+    x = _random_act(300, 384, seed=91)
+    q, s = oracle.quant_per_tensor(x)
+    want_q, want_s = _numpy_torch_per_tensor(x, np.abs(bf16_bits_to_f32(x)).max())
+    assert np.float32(s).view(np.uint32) == np.float32(want_s).view(np.uint32)
+    np.testing.assert_array_equal(q, want_q)
+
+
+def test_per_tensor_amax_element_maps_to_448():
+    x = _random_act(64, 256, seed=92)
+    q, _ = oracle.quant_per_tensor(x)
+    xf = bf16_bits_to_f32(x)
+    i = np.unravel_index(np.argmax(np.abs(xf)), xf.shape)
+    assert q[i] in (0x7E, 0xFE)
+    # 448's rounding interval starts at the midpoint 432 to the next code
+    # down (416); the tie at 432 goes to 448 (even mantissa)
+    s = np.float32(np.abs(xf[i])) / np.float32(448.0)
+    assert np.count_nonzero((q & 0x7F) == 0x7E) == np.count_nonzero(np.abs(xf / s) >= 432.0)
+
+
+def test_per_tensor_of_one_group_equals_the_group_quantisers():
+    """A 128x128 tensor is one weight block and a 1x128 tensor is one
+    activation tile: per-tensor scaling must give the same codes and scale."""
+    w = _random_w(128, 128, seed=93)
+    q, s = oracle.quant_per_tensor(w)
+    qb, sb = oracle.quant_w_128x128(w)
+    np.testing.assert_array_equal(q, qb)
+    assert np.float32(s).view(np.uint32) == sb[0, 0].view(np.uint32)
+    a = _random_act(1, 128, seed=94)
+    q, s = oracle.quant_per_tensor(a)
+    qa, sa = oracle.quant_act_1x128(a)
+    np.testing.assert_array_equal(q, qa)
+    assert np.float32(s).view(np.uint32) == sa[0, 0].view(np.uint32)
+
+
+def test_per_tensor_zero_tensor():
+    x = np.zeros((3, 128), np.uint16)
+    x[1, 5] = 0x8000                                                  # -0
+    q, s = oracle.quant_per_tensor(x)
+    assert s == 0.0 and q[1, 5] == 0x80 and np.count_nonzero(q) == 1
+
+
+def test_delayed_scaling_rules():
+    x = _random_act(200, 256, seed=95)
+    amax = np.abs(bf16_bits_to_f32(x)).max()
+    # the tensor's own amax: identical to current scaling
+    q0, s0 = oracle.quant_per_tensor(x)
+    q1, s1, a1 = oracle.quant_per_tensor_delayed(x, amax)
+    np.testing.assert_array_equal(q0, q1)
+    assert s0 == s1 and a1 == amax
+    # a quarter of it (a history that missed a growth): the largest values
+    # saturate; every code follows numpy division + torch encoding
+    q2, s2, a2 = oracle.quant_per_tensor_delayed(x, amax / 4)
+    want, want_s = _numpy_torch_per_tensor(x, np.float32(amax / 4))
+    np.testing.assert_array_equal(q2, want)
+    assert s2 == want_s and a2 == amax
+    assert np.any((q2 & 0x7F) == 0x7E)
+    # a larger history amax: nothing saturates except exactly-448 codes
+    q3, _, _ = oracle.quant_per_tensor_delayed(x, amax * 8)
+    want, _ = _numpy_torch_per_tensor(x, np.float32(amax * 8))
+    np.testing.assert_array_equal(q3, want)
+    assert not np.any((q3 & 0x7F) == 0x7E)
+
+
+@pytest.mark.parametrize("b_major", [0, 1])
+def test_per_tensor_gemm_matches_numpy_and_block_gemm_with_constant_scales(b_major):
+    g = generator(96, "cpu")
+    a = bf16_bits(normal_bf16((9, 384), 1.0, g, "cpu", outlier_p=0.02, outlier_scale=50.0))
+    w = bf16_bits(normal_bf16((140, 384) if b_major == 0 else (384, 256), 0.02, g, "cpu"))
+    qa, sa = oracle.quant_per_tensor(a)
+    qb, sb = oracle.quant_per_tensor(w)
+    got = oracle.gemm_f64_per_tensor(qa, sa, qb, sb, b_major=b_major)
+    A = torch_decode(qa) * np.float64(sa)
+    B = torch_decode(qb) * np.float64(sb)
+    np.testing.assert_allclose(got, A @ (B.T if b_major == 0 else B), rtol=1e-12, atol=1e-300)
+    # the block oracle with every group scale equal to the tensor's scale
+    KB = 384 // 128
+    if b_major == 0:
+        sb_grid = np.full(((140 + 127) // 128, KB), sb, np.float32)
+    else:
+        sb_grid = np.full((KB, 256 // 128), sb, np.float32)
+    blk = oracle.gemm_f64(qa, np.full((KB, 9), sa, np.float32), qb, sb_grid, b_major=b_major)
+    np.testing.assert_array_equal(got, blk)
