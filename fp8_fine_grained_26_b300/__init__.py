@@ -37,7 +37,9 @@ _STATUS_NAMES = {
 EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8_gemm_blockscaled",
             "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
             "fp8_quant_act_1x128_gather", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
-            "fp8bs_selftest_wait_timeout", "fp8bs_selftest_set_wait_limit")
+            "fp8bs_selftest_wait_timeout", "fp8bs_selftest_set_wait_limit",
+            "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor", "fp8_quant_per_tensor_delayed",
+            "fp8_gemm_per_tensor")
 
 
 class Fp8bsError(RuntimeError):
@@ -65,6 +67,10 @@ def _load():
         "fp8bs_last_error": [p],
         "fp8bs_selftest_wait_timeout": [i64, p],
         "fp8bs_selftest_set_wait_limit": [i64],
+        "fp8_quant_per_tensor_workspace_size": [i64, i64, p],
+        "fp8_quant_per_tensor": [p, i64, i64, i64, p, i64, p, p, i64, p],
+        "fp8_quant_per_tensor_delayed": [p, i64, i64, i64, p, p, i64, p, p, p],
+        "fp8_gemm_per_tensor": [p, p, p, p, i64, i64, i64, i32, p, i32, i64, p],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -338,6 +344,90 @@ def fp8_grouped_gemm_blockscaled(qA, sA, qB, sB, seg_offsets, out_dtype=torch.bf
     return C
 
 
+def fp8_quant_per_tensor_workspace_size(R, C):
+    """Bytes of device workspace fp8_quant_per_tensor needs for an [R, C] tensor."""
+    n = ctypes.c_int64(0)
+    _check(lib.fp8_quant_per_tensor_workspace_size(int(R), int(C), ctypes.byref(n)),
+           "fp8_quant_per_tensor_workspace_size")
+    return n.value
+
+
+def _per_tensor_outputs(x, q, scale):
+    R, C = x.shape
+    if q is None:
+        q = torch.empty((R, C), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty((1,), dtype=torch.float32, device=x.device)
+    _need(q, torch.uint8, "q", 2)
+    _row_major(q, "q")
+    if tuple(q.shape) != (R, C) or scale.dtype != torch.float32 or scale.numel() < 1 or not scale.is_cuda:
+        raise ValueError("output shapes do not match x")
+    return q, scale
+
+
+def fp8_quant_per_tensor(x, q=None, scale=None, workspace=None, stream=None):
+    """Per-tensor quantisation of BF16 ``x [R, C]`` with its own amax (one
+    scale fp32(amax/448) for every element).  ``workspace``: a device uint8
+    tensor of at least fp8_quant_per_tensor_workspace_size(R, C) bytes
+    (allocated here when not given).  Returns ``(q uint8 [R, C], scale float32 [1])``."""
+    _need(x, torch.bfloat16, "x", 2)
+    _row_major(x, "x")
+    R, C = x.shape
+    q, scale = _per_tensor_outputs(x, q, scale)
+    need = fp8_quant_per_tensor_workspace_size(R, C)
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=x.device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    ldx = x.stride(0) if R > 0 else C
+    ldq = q.stride(0) if R > 0 else C
+    _check(lib.fp8_quant_per_tensor(_ptr(x), R, C, ldx, _ptr(q), ldq, _ptr(scale), _ptr(workspace), nbytes,
+                                    _stream(stream)), "fp8_quant_per_tensor")
+    return q, scale
+
+
+def fp8_quant_per_tensor_delayed(x, amax_in, q=None, scale=None, amax_out=None, stream=None):
+    """Per-tensor quantisation of BF16 ``x [R, C]`` with delayed scaling: the
+    scale is fp32(amax_in/448) for a given device float ``amax_in`` (e.g. the
+    largest amax of earlier steps); this tensor's own amax goes to
+    ``amax_out``.  Returns ``(q, scale, amax_out)``."""
+    _need(x, torch.bfloat16, "x", 2)
+    _row_major(x, "x")
+    R, C = x.shape
+    q, scale = _per_tensor_outputs(x, q, scale)
+    if amax_out is None:
+        amax_out = torch.empty((1,), dtype=torch.float32, device=x.device)
+    for t, n in ((amax_in, "amax_in"), (amax_out, "amax_out")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.numel() < 1 or not t.is_cuda:
+            raise TypeError(f"{n}: expected a CUDA float32 tensor")
+    ldx = x.stride(0) if R > 0 else C
+    ldq = q.stride(0) if R > 0 else C
+    _check(lib.fp8_quant_per_tensor_delayed(_ptr(x), R, C, ldx, _ptr(amax_in), _ptr(q), ldq, _ptr(scale),
+                                            _ptr(amax_out), _stream(stream)), "fp8_quant_per_tensor_delayed")
+    return q, scale, amax_out
+
+
+def fp8_gemm_per_tensor(qA, sA, qB, sB, b_major=B_KMAJOR, out_dtype=torch.bfloat16, C=None, stream=None):
+    """``C = sA sB (qA . qB^T)`` for per-tensor scaled operands (``sA``, ``sB``
+    one-element device float32 tensors), the whole K accumulated on the
+    tensor cores.  ``qB`` is ``[N, K]`` or (b_major=1) stored ``[K, N]``."""
+    _need(qA, torch.uint8, "qA", 2)
+    _need(qB, torch.uint8, "qB", 2)
+    M, K = qA.shape
+    N = qB.shape[0] if b_major == B_KMAJOR else qB.shape[1]
+    Kb = qB.shape[1] if b_major == B_KMAJOR else qB.shape[0]
+    if Kb != K:
+        raise ValueError("qA and qB disagree on K")
+    for t, n in ((sA, "sA"), (sB, "sB")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.numel() < 1 or not t.is_cuda:
+            raise TypeError(f"{n}: expected a CUDA float32 tensor")
+    C, cd, ldc = _out(C, M, N, out_dtype, qA.device)
+    _check(lib.fp8_gemm_per_tensor(_ptr(qA), _ptr(sA), _ptr(qB), _ptr(sB), M, N, K, int(b_major), _ptr(C), cd,
+                                   ldc, _stream(stream)), "fp8_gemm_per_tensor")
+    return C
+
+
 def fp8bs_last_error(stream=None):
     """Synchronise the stream and return (and clear) the device error status."""
     return lib.fp8bs_last_error(_stream(stream))
@@ -360,5 +450,6 @@ __all__ = ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8
            "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
            "fp8_quant_act_1x128_gather", "FP8BS_ERR_INDEX",
            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout",
-           "fp8bs_selftest_set_wait_limit", "Fp8bsError", "lib",
+           "fp8bs_selftest_set_wait_limit", "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor",
+           "fp8_quant_per_tensor_delayed", "fp8_gemm_per_tensor", "Fp8bsError", "lib",
            "LIB_PATH", "EXPORTED", "B_KMAJOR", "B_MNMAJOR", "OUT_BF16", "OUT_FP32"]

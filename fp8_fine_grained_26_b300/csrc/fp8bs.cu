@@ -110,7 +110,23 @@ int current_device(DeviceInfo **info)
             cudaFuncSetAttribute(quant_w_128x128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  quant_smem_bytes()) != cudaSuccess ||
             cudaFuncSetAttribute(quant_act_w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 quant_smem_bytes()) != cudaSuccess)
+                                 quant_smem_bytes()) != cudaSuccess ||
+            cudaFuncSetAttribute(amax_units_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 quant_smem_bytes()) != cudaSuccess ||
+            cudaFuncSetAttribute(quant_fixed_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 quant_smem_bytes()) != cudaSuccess ||
+            cudaFuncSetAttribute(quant_fixed_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 quant_smem_bytes()) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, false, false, 3, false, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 gemm_smem_bytes<false, 3>()) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, true, false, 3, false, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 gemm_smem_bytes<false, 3>()) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, false, true, PAIR_STAGES, false, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem) != cudaSuccess ||
+            cudaFuncSetAttribute(fp8_gemm_kernel<false, true, true, PAIR_STAGES, false, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem) != cudaSuccess)
             return FP8BS_ERR_LAUNCH;
         // how many CTA pairs (2-CTA clusters) fit at once
         cudaLaunchConfig_t cfg = {};
@@ -247,7 +263,7 @@ int check_gemm_common(const void *qA, const float *sA, const void *qB, const flo
 // stride in bytes).
 int launch_dense(DeviceInfo *dev, const void *qA, const float *sA, const void *qB, const float *sB,
                  int64_t M, int64_t N, int64_t K, int b_major, void *C, int c_dtype, int64_t ldc,
-                 float *sC, cudaStream_t stream, bool tok = false)
+                 float *sC, cudaStream_t stream, bool tok = false, bool pt = false)
 {
     const bool qout = sC != nullptr;              // (tok implies K-major B and no qout)
     CUtensorMap tmA, tmB;
@@ -319,6 +335,12 @@ int launch_dense(DeviceInfo *dev, const void *qA, const float *sA, const void *q
         cudaError_t e;
         if (tok)
             e = cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES, false, true>, tmA, tmB, tmC, g);
+        else if (pt)
+            e = b_major == FP8BS_B_KMAJOR
+                    ? cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES, false, false, true>,
+                                         tmA, tmB, tmC, g)
+                    : cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, true, true, PAIR_STAGES, false, false, true>,
+                                         tmA, tmB, tmC, g);
         else if (b_major == FP8BS_B_KMAJOR)
             e = qout ? cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES, true>, tmA, tmB, tmC, g)
                      : cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES>, tmA, tmB, tmC, g);
@@ -333,6 +355,13 @@ int launch_dense(DeviceInfo *dev, const void *qA, const float *sA, const void *q
     if (tok) {
         fp8_gemm_kernel<false, false, false, 3, false, true>
             <<<grid, GEMM_THREADS, gemm_smem_bytes<false, 3, B_STAGE_BYTES, SCALE_SLOT_FLOATS_TOK>(), stream>>>(
+                tmA, tmB, tmC, g);
+    } else if (pt) {
+        if (b_major == FP8BS_B_KMAJOR)
+            fp8_gemm_kernel<false, false, false, 3, false, false, true><<<grid, GEMM_THREADS, smem, stream>>>(
+                tmA, tmB, tmC, g);
+        else
+            fp8_gemm_kernel<false, true, false, 3, false, false, true><<<grid, GEMM_THREADS, smem, stream>>>(
                 tmA, tmB, tmC, g);
     } else if (b_major == FP8BS_B_KMAJOR) {
         if (qout)
@@ -670,6 +699,96 @@ int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA, const void *qB
     g.num_tiles = 0;
     fp8_gemm_kernel<true, false, false, 3><<<dev->num_sms, GEMM_THREADS, gemm_smem_bytes<true, 3>(), stream>>>(tmA, tmB, tmC, g);
     return launch_status();
+}
+
+int fp8_quant_per_tensor_workspace_size(int64_t R, int64_t C, int64_t *bytes)
+{
+    if (!bytes)
+        return FP8BS_ERR_NULL;
+    if (R < 0 || C < 0 || C % 128 != 0)
+        return FP8BS_ERR_SHAPE;
+    *bytes = 4 * (((R + 127) / 128) * (C / 128) + 1);
+    return FP8BS_OK;
+}
+
+int fp8_quant_per_tensor(const void *x_bf16, int64_t R, int64_t C, int64_t ldx, void *q_e4m3, int64_t ldq,
+                         float *scale, void *workspace, int64_t workspace_bytes, cudaStream_t stream)
+{
+    const int st = check_quant_operand(x_bf16, R, C, ldx, q_e4m3, ldq, scale);
+    if (st < 0)
+        return st;
+    if (st == 1)
+        return FP8BS_OK;
+    if (!workspace)
+        return FP8BS_ERR_NULL;
+    if (!aligned4(workspace))
+        return FP8BS_ERR_ALIGN;
+    const int64_t CB = C / 128, U = ((R + 127) / 128) * CB;
+    if (workspace_bytes < 4 * (U + 1))
+        return FP8BS_ERR_ARG;
+    DeviceInfo *dev = nullptr;
+    if (int s = current_device(&dev))
+        return s;
+    CUtensorMap tmX;
+    if (!encode_bf16_units(&tmX, x_bf16, (uint64_t)C, (uint64_t)R, (uint64_t)ldx))
+        return FP8BS_ERR_ARG;
+    uint32_t *ws = static_cast<uint32_t *>(workspace);
+    const int grid = (int)std::min<int64_t>(U, 3 * (int64_t)dev->num_sms);
+    amax_units_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(tmX, CB, ws, U, wait_limit_single());
+    amax_reduce_kernel<<<1, REDUCE_THREADS, 0, stream>>>(ws, U, scale);
+    quant_fixed_kernel<false><<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
+        tmX, R, CB, static_cast<uint8_t *>(q_e4m3), ldq, reinterpret_cast<const float *>(ws + U), scale, nullptr, U,
+        wait_limit_single());
+    return launch_status();
+}
+
+int fp8_quant_per_tensor_delayed(const void *x_bf16, int64_t R, int64_t C, int64_t ldx, const float *amax_in,
+                                 void *q_e4m3, int64_t ldq, float *scale, float *amax_out, cudaStream_t stream)
+{
+    const int st = check_quant_operand(x_bf16, R, C, ldx, q_e4m3, ldq, scale);
+    if (st < 0)
+        return st;
+    if (st == 1)
+        return FP8BS_OK;
+    if (!amax_in || !amax_out)
+        return FP8BS_ERR_NULL;
+    if (!aligned4(amax_in) || !aligned4(amax_out))
+        return FP8BS_ERR_ALIGN;
+    if (static_cast<const void *>(amax_in) == static_cast<const void *>(amax_out))
+        return FP8BS_ERR_ARG;
+    DeviceInfo *dev = nullptr;
+    if (int s = current_device(&dev))
+        return s;
+    CUtensorMap tmX;
+    if (!encode_bf16_units(&tmX, x_bf16, (uint64_t)C, (uint64_t)R, (uint64_t)ldx))
+        return FP8BS_ERR_ARG;
+    const int64_t CB = C / 128, U = ((R + 127) / 128) * CB;
+    if (cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    const int grid = (int)std::min<int64_t>(U, 3 * (int64_t)dev->num_sms);
+    quant_fixed_kernel<true><<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
+        tmX, R, CB, static_cast<uint8_t *>(q_e4m3), ldq, amax_in, scale, reinterpret_cast<uint32_t *>(amax_out), U,
+        wait_limit_single());
+    return launch_status();
+}
+
+int fp8_gemm_per_tensor(const void *qA, const float *sA, const void *qB, const float *sB, int64_t M, int64_t N,
+                        int64_t K, int b_major, void *C, int c_dtype, int64_t ldc, cudaStream_t stream)
+{
+    if (b_major != FP8BS_B_KMAJOR && b_major != FP8BS_B_MNMAJOR)
+        return FP8BS_ERR_ARG;
+    if (int st = check_gemm_common(qA, sA, qB, sB, M, N, K, C, c_dtype, ldc))
+        return st;
+    if (M == 0 || N == 0)
+        return FP8BS_OK;
+    if (b_major == FP8BS_B_MNMAJOR && N % 16 != 0)
+        return FP8BS_ERR_SHAPE;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    if (K == 0)
+        return zero_output(C, c_dtype, ldc, M, N, stream);
+    return launch_dense(dev, qA, sA, qB, sB, M, N, K, b_major, C, c_dtype, ldc, nullptr, stream, false, true);
 }
 
 int fp8bs_selftest_wait_timeout(int64_t limit_us, cudaStream_t stream)

@@ -401,7 +401,13 @@ __device__ __forceinline__ void store_row_direct(const GemmArgs &g, const float2
 // TOK: the weight-gradient GEMM -- B carries one scale per row and 128-wide
 // K-slice (sB [K/128][N]), like A, so each output column has its own B
 // scale; dense, K-major B, BF16 or FP32 output.
-template <bool GROUPED, bool B_MN, bool PAIR, int STAGES, bool QOUT = false, bool TOK = false>
+// PT: per-tensor scaling, the contrast variant -- sA and sB are one scalar
+// each, so there is nothing to promote per slice: the MMAs accumulate the
+// whole K of a tile into one TMEM buffer (the tensor core's FP32
+// accumulation), the promote warps read it once per tile and multiply by
+// sA * sB; tile t uses buffer t & 1, so the next tile's MMAs overlap this
+// tile's epilogue.  Dense, BF16 or FP32 output.
+template <bool GROUPED, bool B_MN, bool PAIR, int STAGES, bool QOUT = false, bool TOK = false, bool PT = false>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs g)
@@ -560,16 +566,20 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         } else if (warp == 1 && lane == 0 && rank == 0) {
             // -------------------------------------------- MMA issuer (pair: leader CTA, M = 256)
             constexpr uint32_t idesc = make_idesc(PAIR ? 2 * BM : BM, BN, B_MN);
-            uint32_t it = 0, pit = 0;
+            uint32_t it = 0, pit = 0;           // pit: uses of the two TMEM buffers (per slice; PT: per tile)
             bool ok = true;
             for (int64_t t = t_first; ok && t < ntiles; t += t_stride) {
-                for (int kb = 0; kb < g.KB; ++kb, ++it, ++pit) {
+                if constexpr (PT) {
+                    // the tile's buffer must have been read out by the previous tile's epilogue
+                    if (!wait_bounded(ss, g, ss.pempty(pit & 1), ((pit >> 1) & 1u) ^ 1u)) { ok = false; break; }
+                }
+                for (int kb = 0; kb < g.KB; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
                     const int p = pit & 1;
                     const uint32_t pph = (pit >> 1) & 1u;
                     if (!wait_bounded(ss, g, ss.full(s), ph)) { ok = false; break; }
-                    if (!wait_bounded(ss, g, ss.pempty(p), pph ^ 1u)) { ok = false; break; }
+                    if (!PT && !wait_bounded(ss, g, ss.pempty(p), pph ^ 1u)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t d = tmem_base + (uint32_t)(p * BN);
                     const uint32_t sa = ss.a_stage(s);
@@ -582,20 +592,29 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             bd = make_sdesc_sw128(sb + kk * 32 * 128, B_STAGE_BYTES / 2, 1024);
                         else
                             bd = make_sdesc_sw128(sb + kk * 32, 16, 1024);
+                        // a fresh partial per slice; PT: one accumulation over all of K
+                        const uint32_t acc = (kk > 0 || (PT && kb > 0)) ? 1u : 0u;
                         if constexpr (PAIR)
-                            ptx::mma_f8f6f4_pair(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                            ptx::mma_f8f6f4_pair(d, ad, bd, idesc, acc);
                         else
-                            ptx::mma_f8f6f4(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                            ptx::mma_f8f6f4(d, ad, bd, idesc, acc);
                     }
+                    const bool publish = !PT || kb == g.KB - 1;
                     if constexpr (PAIR) {
                         // stage free and partial ready, in both CTAs
                         ptx::mma_commit_pair_mc(ss.empty(s), 0x3);
-                        ptx::mma_commit_pair_mc(ss.pfull(p), 0x3);
+                        if (publish)
+                            ptx::mma_commit_pair_mc(ss.pfull(p), 0x3);
                     } else {
                         ptx::mma_commit(ss.empty(s));
-                        ptx::mma_commit(ss.pfull(p));
+                        if (publish)
+                            ptx::mma_commit(ss.pfull(p));
                     }
+                    if constexpr (!PT)
+                        ++pit;
                 }
+                if constexpr (PT)
+                    ++pit;
             }
             // Drain: all MMAs this thread issued complete before TMEM is freed.
             if constexpr (PAIR)
@@ -604,7 +623,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 ptx::mma_commit(ss.drain());
             wait_drain(ss.drain(), 0);
         }
-        if (warp == 2) {
+        if (warp == 2 && !PT) {
             // -------------------------------------------- scale loader
             // Stages each slice's 128 row scales sA[kb][m0 .. m0+127] and the
             // two column-block scales of the tile into a SCALE_SLOTS-deep
@@ -702,6 +721,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const int col_half = wg * 128;
         uint32_t pit = 0, eit = 0;
         bool ok = true;
+        // PT: the two per-tensor scales, one product for every output
+        const float pt_scale = PT ? g.sA[0] * g.sB[0] : 0.0f;
         for (int64_t t = t_first; ok && t < ntiles; t += t_stride) {
             const Tile tl = tile_at<GROUPED, PAIR>(g, ss, t, rank);
             const int64_t gm = tl.m0 + row;
@@ -710,10 +731,39 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             // (the padding of a partial M-block) skips its TMEM reads and FMAs
             const bool warp_live = !GROUPED || tl.m0 + quarter * 32 < tl.m_end;
             float2 acc2[64];
+            if constexpr (PT) {
+                // the tile's whole-K accumulator, read once and scaled
+                const int p = pit & 1;
+                const uint32_t pph = (pit >> 1) & 1u;
+                ++pit;
+                if (!warp_wait(ss, g, ss.pfull(p), pph)) { ok = false; break; }
+                ptx::tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(p * BN + col_half);
+                const float2 s2 = make_float2(pt_scale, pt_scale);
+                uint32_t r[64];
+                ptx::tmem_ld_32x32b_x64(taddr, r);
+                ptx::tmem_ld_wait(r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    acc2[j] = __fmul2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), s2);
+                ptx::tmem_ld_32x32b_x64(taddr + 64, r);
+                ptx::tmem_ld_wait(r);
+                ptx::tc_fence_before();
+                __syncwarp();                            // the warp's accumulator is in registers
+                if constexpr (PAIR)
+                    ptx::mbar_arrive_cluster_if(ptx::mapa_shared(ss.pempty(p), 0), lane == 0);
+                else
+                    ptx::mbar_arrive_cluster_if(ss.pempty(p), lane == 0);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    acc2[32 + j] =
+                        __fmul2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), s2);
+            } else {
 #pragma unroll
             for (int j = 0; j < 64; ++j)
                 acc2[j] = make_float2(0.0f, 0.0f);
-            for (int kb = 0; kb < g.KB; ++kb, ++pit) {
+            }
+            for (int kb = 0; !PT && kb < g.KB; ++kb, ++pit) {
                 // this slice's scales from the shared ring (staged by warp 2)
                 const int slot = (int)(pit % SCALE_SLOTS);
                 if (!warp_wait(ss, g, ss.sready(slot), (pit / SCALE_SLOTS) & 1u)) { ok = false; break; }

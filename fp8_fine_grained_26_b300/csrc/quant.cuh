@@ -432,6 +432,186 @@ __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_act_w_kernel(
     qdrain(r, j, issued);
 }
 
+// ---------------------------------------------------------------------------
+// Per-tensor scaling, the contrast to the fine-grained groups: one scale for
+// the whole tensor ["qqstock.cn walkthrough", FP8 section: fine-grained rather
+// than per-tensor quantisation; "DeepSeek-V3 Technical Report digest",
+// section 3, fine-grained quantisation bullet].  Same rules with the group
+// being the tensor: s = fp32(amax / 448), q = E4M3_RNE_sat(fp32(x / s)).
+//
+// Divisor of a float amax: a BF16-representable amax (every amax of a BF16
+// tensor is one) takes the proven reciprocal path of make_divisor; any other
+// value (a caller's own history amax) uses IEEE division for every element.
+__device__ __forceinline__ Divisor make_divisor_f32(float amax)
+{
+    const uint32_t bits = __float_as_uint(fabsf(amax));
+    if ((bits & 0xFFFFu) == 0u)
+        return make_divisor(bits >> 16);
+    Divisor d;
+    d.s = __fdiv_rn(fabsf(amax), 448.0f);
+    d.mode = d.s == 0.0f ? 0 : 1;                  // a zero scale encodes x itself, as for a zero group
+    d.r = 0.0f;
+    return d;
+}
+
+// Pass 1 of current scaling: the amax (BF16 magnitude bits) of every 128x128
+// unit of the tensor into ws[unit], through the same TMA ring as the weight
+// quantiser.  Rows past R are the tensor map's zero fill and do not change a
+// maximum of magnitudes.
+__global__ void __launch_bounds__(QUANT_THREADS, 3) amax_units_kernel(
+    const __grid_constant__ CUtensorMap tmX, int64_t CB, uint32_t *__restrict__ ws, int64_t units,
+    uint64_t wait_ns)
+{
+    const QRing r = qring_setup(wait_ns);
+    const int tid = threadIdx.x;
+    const int chunk = tid & 15;
+    const int r0 = tid >> 4;
+    const int64_t mine = (int64_t)blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    int64_t issued = 0;
+    if (tid == 0)
+        for (; issued < mine && issued < QSTAGES; ++issued)
+            qissue(r, &tmX, issued, CB);
+    int64_t j = 0;
+    for (; j < mine; ++j) {
+        if (!qwait(r, j))
+            break;
+        const uint32_t st = r.stage((int)(j % QSTAGES));
+        uint32_t a = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint4 v;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(st + (uint32_t)((r0 + 16 * i) * 256 + chunk * 16)));
+            a = max(a, absmax_bits8(v));
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+        uint32_t *wmax = r.red_u((int)(j & 1));
+        if ((tid & 31) == 0)
+            wmax[tid >> 5] = a;
+        __syncthreads();                                   // stage read, warp maxima written
+        if (tid == 0 && issued < mine && issued < j + 1 + QSTAGES) {
+            qissue(r, &tmX, issued, CB);
+            ++issued;
+        }
+        if (tid == 0) {
+            uint32_t m = wmax[0];
+#pragma unroll
+            for (int i = 1; i < 8; ++i)
+                m = max(m, wmax[i]);
+            ws[(int64_t)blockIdx.x + j * gridDim.x] = m;
+        }
+    }
+    qdrain(r, j, issued);
+}
+
+// Pass 2: one CTA reduces the unit maxima ws[0 .. U) to the tensor's amax,
+// stores it as a float in ws[U] and the scale fp32(amax / 448) in *scale.
+constexpr int REDUCE_THREADS = 1024;
+
+__global__ void __launch_bounds__(REDUCE_THREADS) amax_reduce_kernel(uint32_t *__restrict__ ws, int64_t U,
+                                                                    float *__restrict__ scale)
+{
+    __shared__ uint32_t part[REDUCE_THREADS / 32];
+    uint32_t a = 0;
+    for (int64_t i = threadIdx.x; i < U; i += REDUCE_THREADS)
+        a = max(a, ws[i]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if ((threadIdx.x & 31) == 0)
+        part[threadIdx.x >> 5] = a;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t m = part[0];
+        for (int i = 1; i < REDUCE_THREADS / 32; ++i)
+            m = max(m, part[i]);
+        const float amax = __uint_as_float(m << 16);
+        ws[U] = __float_as_uint(amax);
+        *scale = make_divisor(m).s;
+    }
+}
+
+// Every 128x128 unit encoded with ONE divisor, formed from the amax at
+// *amax_src (pass 3 of current scaling: ws[U]; delayed scaling: the caller's
+// history amax).  RECORD (delayed scaling): also the tensor's own amax, kept
+// per thread over all its units and merged with one atomicMax per CTA into
+// *amax_rec (float bits: monotone for non-negative floats), which the host
+// has zeroed.  CTA 0 stores the scale.
+template <bool RECORD>
+__global__ void __launch_bounds__(QUANT_THREADS, 3) quant_fixed_kernel(
+    const __grid_constant__ CUtensorMap tmX, int64_t R, int64_t CB, uint8_t *__restrict__ q, int64_t ldq,
+    const float *__restrict__ amax_src, float *__restrict__ scale_out, uint32_t *__restrict__ amax_rec,
+    int64_t units, uint64_t wait_ns)
+{
+    const QRing r = qring_setup(wait_ns);
+    const int tid = threadIdx.x;
+    const int chunk = tid & 15;
+    const int r0 = tid >> 4;
+    const Divisor d = make_divisor_f32(*amax_src);
+    if (blockIdx.x == 0 && tid == 0)
+        *scale_out = d.s;
+    const int64_t mine = (int64_t)blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    int64_t issued = 0;
+    if (tid == 0)
+        for (; issued < mine && issued < QSTAGES; ++issued)
+            qissue(r, &tmX, issued, CB);
+    uint32_t seen = 0;                                     // RECORD: max magnitude bits seen by this thread
+    int64_t j = 0;
+    for (; j < mine; ++j) {
+        if (!qwait(r, j))
+            break;
+        const uint32_t st = r.stage((int)(j % QSTAGES));
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w)
+                         : "r"(st + (uint32_t)((r0 + 16 * i) * 256 + chunk * 16)));
+        __syncthreads();                                   // the stage is free again
+        if (tid == 0 && issued < mine && issued < j + 1 + QSTAGES) {
+            qissue(r, &tmX, issued, CB);
+            ++issued;
+        }
+        int64_t rb, cb;
+        qunit(j, CB, rb, cb);
+        if constexpr (RECORD) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                seen = max(seen, absmax_bits8(v[i]));      // rows past R are zero fill
+        }
+        const int64_t col = cb * 128 + chunk * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int64_t row = rb * 128 + r0 + 16 * i;
+            if (row < R) {
+                const uint2 c = quant_8(v[i], d);
+                ptx::st_v2(q + row * ldq + col, c.x, c.y);
+            }
+        }
+    }
+    if constexpr (RECORD) {
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+            seen = max(seen, __shfl_xor_sync(0xffffffffu, seen, o));
+        uint32_t *wmax = r.red_u(0);
+        __syncthreads();
+        if ((tid & 31) == 0)
+            wmax[tid >> 5] = seen;
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t m = wmax[0];
+#pragma unroll
+            for (int i = 1; i < 8; ++i)
+                m = max(m, wmax[i]);
+            atomicMax(amax_rec, m << 16);
+        }
+    }
+    qdrain(r, j, issued);
+}
+
 // Gather + 1x128 activation quantisation for expert dispatch: output row i
 // is the quantisation of input row rows[i] (the token routed to that expert
 // slot).  Quantising then gathering equals gathering then quantising, so

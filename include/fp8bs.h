@@ -241,6 +241,69 @@ int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA,
                                  void *C, int c_dtype, int64_t ldc, cudaStream_t stream);
 
 /*
+ * Per-tensor FP8 quantisation, the contrast variant: ONE scale for the whole
+ * tensor instead of one per 1x128 tile or 128x128 block.  The pages present
+ * their fine-grained groups as the alternative to this, because a single
+ * outlier sets the scale of every element of the tensor ("qqstock.cn
+ * walkthrough", FP8 section: fine-grained rather than per-tensor
+ * quantisation; "DeepSeek-V3 Technical Report digest", section 3,
+ * fine-grained quantisation bullet).  The rules are the library's rules with
+ * the group being the tensor: scale = fp32(amax / 448) over all R x C
+ * elements, q = E4M3_RNE_sat(fp32(x / scale)); an all-zero tensor has scale 0
+ * and codes 0x00 / 0x80.
+ *   x_bf16 : [R][C] BF16, row stride ldx (elements); C a multiple of 128.
+ *   q_e4m3 : [R][C] E4M3 codes, row stride ldq (bytes).
+ *   scale  : one FP32 on the device.
+ *   workspace : device scratch of at least the size that
+ *            fp8_quant_per_tensor_workspace_size(R, C) reports (4 bytes per
+ *            128x128 unit, plus 4), 4-byte aligned, owned by the caller; its
+ *            contents on entry do not matter and on return are unspecified.
+ *            Calls that share one workspace must not overlap on the GPU.
+ * Three kernels on `stream`: the amax of every 128x128 unit into the
+ * workspace, one CTA that reduces them to the tensor's amax and scale, and
+ * the encoding pass (which reads the tensor a second time).  R == 0 or
+ * C == 0 is a no-op.  A workspace smaller than required: FP8BS_ERR_ARG.
+ * Other rules and errors as fp8_quant_w_128x128.
+ */
+int fp8_quant_per_tensor_workspace_size(int64_t R, int64_t C, int64_t *bytes);
+int fp8_quant_per_tensor(const void *x_bf16, int64_t R, int64_t C, int64_t ldx, void *q_e4m3, int64_t ldq,
+                         float *scale, void *workspace, int64_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Per-tensor FP8 quantisation with DELAYED scaling: the scale comes from an
+ * amax the caller supplies (the usual choice is the largest amax recorded
+ * over earlier steps), so the tensor is encoded in one pass while its own
+ * amax is recorded for later steps.
+ *   amax_in  : one FP32 on the device, finite and >= 0; scale =
+ *              fp32(amax_in / 448) is stored in *scale.  Elements with
+ *              |x| / scale >= 464 saturate to +-448; amax_in == 0 gives scale 0
+ *              and codes E4M3(x).
+ *   amax_out : one FP32 on the device (not the same word as amax_in): set to
+ *              max |x| over this tensor (the call first zeroes it, on
+ *              `stream`).
+ * Other arguments, rules and errors as fp8_quant_per_tensor (no workspace).
+ */
+int fp8_quant_per_tensor_delayed(const void *x_bf16, int64_t R, int64_t C, int64_t ldx, const float *amax_in,
+                                 void *q_e4m3, int64_t ldq, float *scale, float *amax_out, cudaStream_t stream);
+
+/*
+ * GEMM over per-tensor quantised operands:
+ *   C[m][n] = sA * sB * sum_k qA[m][k] * qB(n, k)
+ * with the WHOLE K sum accumulated by the tensor cores in their FP32
+ * accumulator (no per-128 promotion: with one scale per tensor there is
+ * nothing to apply per slice), then multiplied by fp32(sA * sB) and rounded
+ * to the output type.  This is the scheme the fine-grained GEMM is compared
+ * with.
+ *   sA, sB : one FP32 each, on the device (from fp8_quant_per_tensor or
+ *            fp8_quant_per_tensor_delayed).
+ *   qB     : [N][K] (b_major == FP8BS_B_KMAJOR) or stored [K][N]
+ *            (FP8BS_B_MNMAJOR, N a multiple of 16).
+ * Other arguments, rules and errors as fp8_gemm_blockscaled.
+ */
+int fp8_gemm_per_tensor(const void *qA, const float *sA, const void *qB, const float *sB, int64_t M, int64_t N,
+                        int64_t K, int b_major, void *C, int c_dtype, int64_t ldc, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reports and clears one condition of the current
  * device's error word: FP8BS_OK (no condition), FP8BS_ERR_TIMEOUT (a kernel's
  * pipeline wait exceeded its time limit; that kernel's outputs are

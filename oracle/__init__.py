@@ -53,6 +53,8 @@ def _load():
         lib.oracle_gemm_f64_per_tensor.argtypes = [p, ctypes.c_float, i64, p, ctypes.c_float, i64, ctypes.c_int,
                                                    i64, i64, i64, p, i64]
         lib.oracle_gemm_f64_per_tensor.restype = ctypes.c_int
+        lib.oracle_gemm_bf16_f64.argtypes = [p, i64, p, i64, ctypes.c_int, i64, i64, i64, p, i64]
+        lib.oracle_gemm_bf16_f64.restype = ctypes.c_int
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         lib.oracle_set_threads.restype = None
         lib.oracle_get_threads.argtypes = []
@@ -263,6 +265,20 @@ def gemm_f64_per_tensor(qA, sA, qB, sB, b_major: int = 0) -> np.ndarray:
     return C
 
 
+def gemm_bf16_f64(a_bits, b_bits, b_major: int = 0) -> np.ndarray:
+    """float64 product of the UNQUANTISED BF16 inputs (uint16 bits): ``a [M,
+    K]`` times ``b [N, K]`` (b_major 0) or stored ``[K, N]`` (b_major 1)."""
+    a, b = _as_c(a_bits, np.uint16), _as_c(b_bits, np.uint16)
+    M, K = a.shape
+    N = b.shape[0] if b_major == 0 else b.shape[1]
+    if (b.shape[1] if b_major == 0 else b.shape[0]) != K:
+        raise ValueError("K mismatch")
+    C = np.empty((M, N), np.float64)
+    _check(_load().oracle_gemm_bf16_f64(_ptr(a), K, _ptr(b), b.shape[1], b_major, M, N, K, _ptr(C), N),
+           "gemm_bf16")
+    return C
+
+
 def act_row_norms(qA, sA) -> np.ndarray:
     """||A^[m, :]||_2 of the dequantised activation rows."""
     qA, sA = _as_c(qA, np.uint8), _as_c(sA, np.float32)
@@ -287,4 +303,4 @@ def b_row_norms(qB, sB, b_major: int = 0) -> np.ndarray:
 __all__ = ["set_threads", "get_threads", "e4m3_encode", "e4m3_decode", "e4m3_encode_array", "e4m3_decode_table",
            "quant_act_1x128", "quant_w_128x128", "gemm_f64", "gemm_f64_at",
            "grouped_gemm_f64", "act_row_norms", "b_row_norms", "quant_per_tensor",
-           "quant_per_tensor_delayed", "gemm_f64_per_tensor"]
+           "quant_per_tensor_delayed", "gemm_f64_per_tensor", "gemm_bf16_f64"]

@@ -471,3 +471,25 @@ int oracle_gemm_f64_per_tensor(const uint8_t *qA, float sA, int64_t lda,
         }
     return 0;
 }
+
+/* The unquantised product of the BF16 inputs, in float64:
+ *   C[m][n] = sum_k a[m][k] * b(n, k)
+ * (b [N][K] for b_major 0, stored [K][N] for b_major 1).  It is the value
+ * both FP8 schemes approximate; the pages judge FP8 training against BF16
+ * ["DeepSeek-V3 Technical Report digest", section 3: relative loss error of
+ * FP8 against BF16 below 0.25%]. */
+int oracle_gemm_bf16_f64(const uint16_t *a, int64_t lda, const uint16_t *b, int64_t ldb, int b_major,
+                         int64_t M, int64_t N, int64_t K, double *C, int64_t ldc)
+{
+#pragma omp parallel for schedule(dynamic, 1) num_threads(oracle_get_threads())
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const uint16_t bb = b_major == 0 ? b[n * ldb + k] : b[k * ldb + n];
+                acc += (double)bf16_bits_to_float(a[m * lda + k]) * (double)bf16_bits_to_float(bb);
+            }
+            C[m * ldc + n] = acc;
+        }
+    return 0;
+}

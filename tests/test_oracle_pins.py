@@ -674,3 +674,13 @@ def test_per_tensor_gemm_matches_numpy_and_block_gemm_with_constant_scales(b_maj
         sb_grid = np.full((KB, 256 // 128), sb, np.float32)
     blk = oracle.gemm_f64(qa, np.full((KB, 9), sa, np.float32), qb, sb_grid, b_major=b_major)
     np.testing.assert_array_equal(got, blk)
+
+
+@pytest.mark.parametrize("b_major", [0, 1])
+def test_unquantised_bf16_product_matches_numpy(b_major):
+    g = generator(97, "cpu")
+    a = normal_bf16((7, 256), 1.0, g, "cpu", outlier_p=0.02, outlier_scale=50.0)
+    w = normal_bf16((130, 256) if b_major == 0 else (256, 130), 0.02, g, "cpu")
+    got = oracle.gemm_bf16_f64(bf16_bits(a), bf16_bits(w), b_major=b_major)
+    A, W = a.double().numpy(), w.double().numpy()
+    np.testing.assert_allclose(got, A @ (W.T if b_major == 0 else W), rtol=1e-12, atol=1e-300)
