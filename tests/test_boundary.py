@@ -23,7 +23,9 @@ def test_header_declares_the_entry_points():
         "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8_gemm_blockscaled",
         "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
         "fp8_quant_act_1x128_gather", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
-        "fp8bs_selftest_wait_timeout", "fp8bs_selftest_set_wait_limit"])
+        "fp8bs_selftest_wait_timeout", "fp8bs_selftest_set_wait_limit",
+        "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor", "fp8_quant_per_tensor_delayed",
+        "fp8_gemm_per_tensor"])
 
 
 def test_library_loads_and_exports_every_declared_symbol():
@@ -170,6 +172,30 @@ def test_gather_quantiser_rejects_bad_arguments():
     assert g(P(16), 8, 128, 64, P(16), 4, P(16), 128, P(16), P(0)) == -2     # ldx < K
     assert g(P(16), 8, 128, 128, P(18), 4, P(16), 128, P(16), P(0)) == -3    # rows align
     assert g(P(16), 8, 128, 132, P(16), 4, P(16), 128, P(16), P(0)) == -3    # ldx * 2 % 16
+
+
+def test_per_tensor_calls_reject_bad_arguments():
+    lib = _raw()
+    n = ctypes.c_int64(0)
+    assert lib.fp8_quant_per_tensor_workspace_size(300, 384, ctypes.byref(n)) == 0
+    assert n.value == 4 * (3 * 3 + 1)                                   # one word per 128x128 unit, plus one
+    assert lib.fp8_quant_per_tensor_workspace_size(300, 100, ctypes.byref(n)) == -2
+    assert lib.fp8_quant_per_tensor_workspace_size(300, 128, None) == -1
+    q = lib.fp8_quant_per_tensor
+    assert q(P(16), 4, 100, 128, P(16), 128, P(16), P(16), 64, P(0)) == -2         # C % 128
+    assert q(P(16), 0, 128, 128, P(16), 128, P(16), P(16), 0, P(0)) == 0           # empty: no-op
+    assert q(P(16), 4, 128, 128, P(16), 128, P(16), P(0), 64, P(0)) == -1          # no workspace
+    assert q(P(16), 4, 128, 128, P(16), 128, P(16), P(18), 64, P(0)) == -3         # workspace align
+    assert q(P(16), 300, 384, 384, P(16), 384, P(16), P(16), 39, P(0)) == -4      # workspace too small
+    d = lib.fp8_quant_per_tensor_delayed
+    assert d(P(16), 4, 128, 128, P(0), P(16), 128, P(16), P(32), P(0)) == -1       # no amax_in
+    assert d(P(16), 4, 128, 128, P(32), P(16), 128, P(16), P(32), P(0)) == -4      # amax_in == amax_out
+    assert d(P(16), 4, 128, 128, P(34), P(16), 128, P(16), P(32), P(0)) == -3      # amax_in align
+    g = lib.fp8_gemm_per_tensor
+    assert g(P(16), P(16), P(16), P(16), 4, 4, 128, 2, P(16), 0, 8, P(0)) == -4      # b_major
+    assert g(P(16), P(16), P(16), P(16), 4, 4, 100, 0, P(16), 0, 8, P(0)) == -2      # K % 128
+    assert g(P(16), P(16), P(16), P(16), 4, 20, 128, 1, P(16), 0, 20, P(0)) == -2    # MN-major N % 16
+    assert g(P(16), P(0), P(16), P(16), 4, 4, 128, 0, P(16), 0, 8, P(0)) == -1       # NULL sA
 
 
 def test_selftest_rejects_out_of_range_limits():
