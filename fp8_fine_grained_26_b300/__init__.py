@@ -24,6 +24,7 @@ FP8BS_ERR_LAUNCH = -5
 FP8BS_ERR_DEVICE = -6
 FP8BS_ERR_TIMEOUT = -7
 FP8BS_ERR_INDEX = -8
+FP8BS_ERR_SCRATCH = -9
 OUT_BF16, OUT_FP32 = 0, 1
 B_KMAJOR, B_MNMAJOR = 0, 1
 
@@ -32,6 +33,7 @@ _STATUS_NAMES = {
     FP8BS_ERR_ALIGN: "FP8BS_ERR_ALIGN", FP8BS_ERR_ARG: "FP8BS_ERR_ARG",
     FP8BS_ERR_LAUNCH: "FP8BS_ERR_LAUNCH", FP8BS_ERR_DEVICE: "FP8BS_ERR_DEVICE",
     FP8BS_ERR_TIMEOUT: "FP8BS_ERR_TIMEOUT", FP8BS_ERR_INDEX: "FP8BS_ERR_INDEX",
+    FP8BS_ERR_SCRATCH: "FP8BS_ERR_SCRATCH",
 }
 
 EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8_gemm_blockscaled",
@@ -39,7 +41,7 @@ EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp
             "fp8_quant_act_1x128_gather", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
             "fp8bs_selftest_wait_timeout", "fp8bs_selftest_set_wait_limit",
             "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor", "fp8_quant_per_tensor_delayed",
-            "fp8_gemm_per_tensor")
+            "fp8_gemm_per_tensor", "fp8_quant_per_tensor_noalloc")
 
 
 class Fp8bsError(RuntimeError):
@@ -71,6 +73,7 @@ def _load():
         "fp8_quant_per_tensor": [p, i64, i64, i64, p, i64, p, p, i64, p],
         "fp8_quant_per_tensor_delayed": [p, i64, i64, i64, p, p, i64, p, p, p],
         "fp8_gemm_per_tensor": [p, p, p, p, i64, i64, i64, i32, p, i32, i64, p],
+        "fp8_quant_per_tensor_noalloc": [p, i64, i64, i64, p, i64, p, p],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)

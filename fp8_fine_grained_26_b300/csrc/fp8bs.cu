@@ -831,3 +831,75 @@ int fp8bs_selftest_set_wait_limit(int64_t limit_ns)
 }
 
 } // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free per-tensor quantisation.
+//
+// The scratch that fp8_quant_per_tensor takes from its caller (one word per
+// 128x128 unit plus one) lives here instead, in a fixed array that every GPU
+// holds from the moment it loads this library until the process exits.  In
+// host code the name g_noalloc_scratch is only a host-side stand-in for the
+// array, not a device address: it is never passed to a kernel.  The device
+// address is looked up once per device, with that device current, by
+// cudaGetSymbolAddress (on the first call of fp8_quant_per_tensor_noalloc on
+// that device), and that address is what the kernels receive.
+//
+// Every call on a device uses the same array and leaves its contents behind.
+// Nothing in it has to start at zero: the unit pass writes every word the
+// reduction reads, and the reduction writes the word the encoding pass reads.
+// Two calls whose kernels overlap on the GPU (on different streams) race on
+// the array.
+static __device__ __align__(256) uint32_t g_noalloc_scratch[FP8BS_NOALLOC_MAX_UNITS + 1];
+
+namespace {
+std::mutex g_noalloc_mutex;
+uint32_t *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device `dev`.
+int noalloc_scratch(int dev, uint32_t **out)
+{
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return FP8BS_ERR_DEVICE;
+        }
+        g_noalloc_ptr[dev] = static_cast<uint32_t *>(ptr);
+    }
+    *out = g_noalloc_ptr[dev];
+    return FP8BS_OK;
+}
+} // namespace
+
+extern "C" int fp8_quant_per_tensor_noalloc(const void *x_bf16, int64_t R, int64_t C, int64_t ldx, void *q_e4m3,
+                                            int64_t ldq, float *scale, cudaStream_t stream)
+{
+    const int st = check_quant_operand(x_bf16, R, C, ldx, q_e4m3, ldq, scale);
+    if (st < 0)
+        return st;
+    if (st == 1)
+        return FP8BS_OK;
+    const int64_t CB = C / 128, U = ((R + 127) / 128) * CB;
+    if (U > FP8BS_NOALLOC_MAX_UNITS)
+        return FP8BS_ERR_SCRATCH;
+    DeviceInfo *dev = nullptr;
+    if (int s = current_device(&dev))
+        return s;
+    int ordinal = 0;
+    if (cudaGetDevice(&ordinal) != cudaSuccess)
+        return FP8BS_ERR_DEVICE;
+    uint32_t *ws = nullptr;
+    if (int s = noalloc_scratch(ordinal, &ws))
+        return s;
+    CUtensorMap tmX;
+    if (!encode_bf16_units(&tmX, x_bf16, (uint64_t)C, (uint64_t)R, (uint64_t)ldx))
+        return FP8BS_ERR_ARG;
+    const int grid = (int)std::min<int64_t>(U, 3 * (int64_t)dev->num_sms);
+    amax_units_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(tmX, CB, ws, U, wait_limit_single());
+    amax_reduce_kernel<<<1, REDUCE_THREADS, 0, stream>>>(ws, U, scale);
+    quant_fixed_kernel<false><<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
+        tmX, R, CB, static_cast<uint8_t *>(q_e4m3), ldq, reinterpret_cast<const float *>(ws + U), scale, nullptr, U,
+        wait_limit_single());
+    return launch_status();
+}

@@ -60,7 +60,8 @@ typedef enum {
     FP8BS_ERR_LAUNCH = -5,      /* the CUDA runtime refused a launch                  */
     FP8BS_ERR_DEVICE = -6,      /* the current device is not sm_103                   */
     FP8BS_ERR_TIMEOUT = -7,     /* (fp8bs_last_error only) a device-side wait timed out */
-    FP8BS_ERR_INDEX = -8        /* (fp8bs_last_error only) a device-side row index was out of range */
+    FP8BS_ERR_INDEX = -8,       /* (fp8bs_last_error only) a device-side row index was out of range */
+    FP8BS_ERR_SCRATCH = -9      /* the size needs more than the library's fixed scratch holds */
 } fp8bs_status;
 
 enum { FP8BS_OUT_BF16 = 0, FP8BS_OUT_FP32 = 1 };
@@ -302,6 +303,35 @@ int fp8_quant_per_tensor_delayed(const void *x_bf16, int64_t R, int64_t C, int64
  */
 int fp8_gemm_per_tensor(const void *qA, const float *sA, const void *qB, const float *sB, int64_t M, int64_t N,
                         int64_t K, int b_major, void *C, int c_dtype, int64_t ldc, cudaStream_t stream);
+
+/*
+ * fp8_quant_per_tensor without a workspace argument: the same result, bit
+ * for bit (same scale, same codes), from the same kernels, with the scratch
+ * held by the library itself.  The pages have no counterpart to this call;
+ * it exists for callers that cannot allocate device memory around a call --
+ * for example code embedded in a host application that owns every device
+ * buffer and grants none for scratch, or a serving loop that forbids any
+ * allocation once it has started -- and so cannot provide the workspace
+ * that fp8_quant_per_tensor needs.  The call itself allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *   Scratch: a fixed array of FP8BS_NOALLOC_MAX_UNITS + 1 32-bit words
+ *   (64 KiB) that every GPU which loads the library holds until the process
+ *   exits.  A tensor of more than FP8BS_NOALLOC_MAX_UNITS 128x128 units
+ *   (ceil(R/128) * C/128) is refused with FP8BS_ERR_SCRATCH before anything
+ *   is enqueued.
+ *   Set-up: the first call on a device, with that device current, looks up
+ *   the array's device address (cudaGetSymbolAddress) and keeps it; make that
+ *   first call before any stream capture.
+ *   Sharing: every call on a device uses the same array and leaves its
+ *   contents there; nothing in it needs to start at zero, because each call
+ *   writes every word it later reads.  Calls whose kernels overlap on the GPU
+ *   (e.g. on two streams) race on the array and must be serialised by the
+ *   caller.
+ * Arguments, other rules and errors as fp8_quant_per_tensor.
+ */
+enum { FP8BS_NOALLOC_MAX_UNITS = 16384 };
+int fp8_quant_per_tensor_noalloc(const void *x_bf16, int64_t R, int64_t C, int64_t ldx, void *q_e4m3, int64_t ldq,
+                                 float *scale, cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reports and clears one condition of the current
