@@ -41,7 +41,8 @@ EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp
             "fp8_quant_act_1x128_gather", "fp8_grouped_gemm_blockscaled", "fp8bs_last_error",
             "fp8bs_selftest_wait_timeout", "fp8bs_selftest_set_wait_limit",
             "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor", "fp8_quant_per_tensor_delayed",
-            "fp8_gemm_per_tensor", "fp8_quant_per_tensor_noalloc")
+            "fp8_gemm_per_tensor", "fp8_quant_per_tensor_noalloc", "fp8_ep_dispatch_pack", "fp8_ep_unpack",
+            "fp8bs_gather_rows")
 
 
 class Fp8bsError(RuntimeError):
@@ -74,6 +75,9 @@ def _load():
         "fp8_quant_per_tensor_delayed": [p, i64, i64, i64, p, p, i64, p, p, p],
         "fp8_gemm_per_tensor": [p, p, p, p, i64, i64, i64, i32, p, i32, i64, p],
         "fp8_quant_per_tensor_noalloc": [p, i64, i64, i64, p, i64, p, p],
+        "fp8_ep_dispatch_pack": [p, i64, i64, i64, p, i64, p, i64, p],
+        "fp8_ep_unpack": [p, i64, i64, i64, p, i64, p, i64, p, p],
+        "fp8bs_gather_rows": [p, i64, i64, p, i64, i64, p, i64, p],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -431,6 +435,79 @@ def fp8_gemm_per_tensor(qA, sA, qB, sB, b_major=B_KMAJOR, out_dtype=torch.bfloat
     return C
 
 
+def packed_row_bytes(K):
+    """Row stride (bytes) of a packed dispatch row: K codes + K/128 FP32
+    scales, rounded up to 16."""
+    return (K + 4 * (K // 128) + 15) // 16 * 16
+
+
+def fp8_ep_dispatch_pack(x, rows, packed=None, stream=None):
+    """Gather + 1x128 quantisation of the routed rows ``x[rows]`` into packed
+    rows ``[M, packed_row_bytes(K)]`` (codes, then the row's scales)."""
+    _need(x, torch.bfloat16, "x", 2)
+    _row_major(x, "x")
+    if rows.dtype != torch.int32 or rows.dim() != 1 or not rows.is_cuda:
+        raise TypeError("rows: expected a 1-D CUDA int32 tensor")
+    T, K = x.shape
+    M = rows.numel()
+    if packed is None:
+        packed = torch.empty((M, packed_row_bytes(K)), dtype=torch.uint8, device=x.device)
+    _need(packed, torch.uint8, "packed", 2)
+    _row_major(packed, "packed")
+    if packed.shape[0] != M:
+        raise ValueError("packed must have one row per routed copy")
+    ldx = x.stride(0) if T > 0 else K
+    ld = packed.stride(0) if M > 0 else packed.shape[1]
+    _check(lib.fp8_ep_dispatch_pack(_ptr(x), T, K, ldx, _ptr(rows.contiguous()), M, _ptr(packed), ld,
+                                    _stream(stream)), "fp8_ep_dispatch_pack")
+    return packed
+
+
+def fp8_ep_unpack(packed, K, perm, q=None, sA=None, stream=None):
+    """Packed rows, reordered by ``perm``: ``q[i], sA[:, i]`` = codes and
+    scales of ``packed[perm[i]]``.  Returns ``(q uint8 [M, K], sA [K/128, M])``."""
+    _need(packed, torch.uint8, "packed", 2)
+    _row_major(packed, "packed")
+    if perm.dtype != torch.int32 or perm.dim() != 1 or not perm.is_cuda:
+        raise TypeError("perm: expected a 1-D CUDA int32 tensor")
+    M = perm.numel()
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.uint8, device=packed.device)
+    if sA is None:
+        sA = torch.empty((K // 128, M), dtype=torch.float32, device=packed.device)
+    _need(q, torch.uint8, "q", 2)
+    if not sA.is_contiguous() or sA.numel() != (K // 128) * M:
+        raise ValueError("sA must be a contiguous [K/128, M] tensor")
+    ld = packed.stride(0) if packed.shape[0] > 0 else packed.shape[1]
+    ldq = q.stride(0) if M > 0 else K
+    _check(lib.fp8_ep_unpack(_ptr(packed), packed.shape[0], ld, K, _ptr(perm.contiguous()), M, _ptr(q), ldq,
+                             _ptr(sA), _stream(stream)), "fp8_ep_unpack")
+    return q, sA
+
+
+def fp8bs_gather_rows(src, rows, dst=None, stream=None):
+    """``dst[i] = src[rows[i]]`` for the rows of a 2-D CUDA tensor (any dtype;
+    a row must be a multiple of 16 bytes)."""
+    if src.dim() != 2 or not src.is_cuda:
+        raise TypeError("src: expected a 2-D CUDA tensor")
+    _row_major(src, "src")
+    if rows.dtype != torch.int32 or rows.dim() != 1 or not rows.is_cuda:
+        raise TypeError("rows: expected a 1-D CUDA int32 tensor")
+    M = rows.numel()
+    if dst is None:
+        dst = torch.empty((M, src.shape[1]), dtype=src.dtype, device=src.device)
+    if dst.dtype != src.dtype or dst.dim() != 2 or dst.shape[1] != src.shape[1] or dst.shape[0] != M:
+        raise ValueError("dst must be [len(rows), src.shape[1]] of src's dtype")
+    _row_major(dst, "dst")
+    es = src.element_size()
+    row_bytes = src.shape[1] * es
+    ld_src = (src.stride(0) if src.shape[0] > 0 else src.shape[1]) * es
+    ld_dst = (dst.stride(0) if M > 0 else dst.shape[1]) * es
+    _check(lib.fp8bs_gather_rows(_ptr(src), src.shape[0], ld_src, _ptr(rows.contiguous()), M, row_bytes, _ptr(dst),
+                                 ld_dst, _stream(stream)), "fp8bs_gather_rows")
+    return dst
+
+
 def fp8bs_last_error(stream=None):
     """Synchronise the stream and return (and clear) the device error status."""
     return lib.fp8bs_last_error(_stream(stream))
@@ -454,5 +531,6 @@ __all__ = ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8
            "fp8_quant_act_1x128_gather", "FP8BS_ERR_INDEX",
            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout",
            "fp8bs_selftest_set_wait_limit", "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor",
-           "fp8_quant_per_tensor_delayed", "fp8_gemm_per_tensor", "Fp8bsError", "lib",
+           "fp8_quant_per_tensor_delayed", "fp8_gemm_per_tensor", "packed_row_bytes", "fp8_ep_dispatch_pack",
+           "fp8_ep_unpack", "fp8bs_gather_rows", "Fp8bsError", "lib",
            "LIB_PATH", "EXPORTED", "B_KMAJOR", "B_MNMAJOR", "OUT_BF16", "OUT_FP32"]

@@ -603,8 +603,82 @@ int fp8_quant_act_1x128_gather(const void *x_bf16, int64_t T, int64_t K, int64_t
     const int64_t tasks = M * ((KB + GATHER_TILES - 1) / GATHER_TILES);
     const int64_t blocks = std::min<int64_t>((tasks * 32 + GATHER_THREADS - 1) / GATHER_THREADS,
                                              8 * (int64_t)dev->num_sms);
-    quant_act_gather_kernel<<<(unsigned)blocks, GATHER_THREADS, 0, stream>>>(
+    quant_act_gather_kernel<false><<<(unsigned)blocks, GATHER_THREADS, 0, stream>>>(
         static_cast<const uint16_t *>(x_bf16), T, ldx, rows, M, KB, static_cast<uint8_t *>(q_e4m3), ldq, sA);
+    return launch_status();
+}
+
+int fp8_ep_dispatch_pack(const void *x_bf16, int64_t T, int64_t K, int64_t ldx, const int32_t *rows, int64_t M,
+                         void *packed, int64_t ld_packed, cudaStream_t stream)
+{
+    if (T < 0 || M < 0 || K < 0 || K % 128 != 0)
+        return FP8BS_ERR_SHAPE;
+    if (M == 0 || K == 0)
+        return FP8BS_OK;
+    if (!x_bf16 || !rows || !packed)
+        return FP8BS_ERR_NULL;
+    const int64_t KB = K / 128;
+    if (ldx < K || ld_packed < K + 4 * KB)
+        return FP8BS_ERR_SHAPE;
+    if (!aligned16(x_bf16) || !aligned16(packed) || !aligned4(rows) || (ldx * 2) % 16 != 0 || ld_packed % 16 != 0)
+        return FP8BS_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    const int64_t tasks = M * ((KB + GATHER_TILES - 1) / GATHER_TILES);
+    const int64_t blocks = std::min<int64_t>((tasks * 32 + GATHER_THREADS - 1) / GATHER_THREADS,
+                                             8 * (int64_t)dev->num_sms);
+    quant_act_gather_kernel<true><<<(unsigned)blocks, GATHER_THREADS, 0, stream>>>(
+        static_cast<const uint16_t *>(x_bf16), T, ldx, rows, M, KB, static_cast<uint8_t *>(packed), ld_packed,
+        nullptr);
+    return launch_status();
+}
+
+int fp8_ep_unpack(const void *packed, int64_t n_src, int64_t ld_packed, int64_t K, const int32_t *perm, int64_t M,
+                  void *q_e4m3, int64_t ldq, float *sA, cudaStream_t stream)
+{
+    if (n_src < 0 || M < 0 || K < 0 || K % 128 != 0)
+        return FP8BS_ERR_SHAPE;
+    if (M == 0 || K == 0)
+        return FP8BS_OK;
+    if (!packed || !perm || !q_e4m3 || !sA)
+        return FP8BS_ERR_NULL;
+    const int64_t KB = K / 128;
+    if (ld_packed < K + 4 * KB || ldq < K)
+        return FP8BS_ERR_SHAPE;
+    if (!aligned16(packed) || !aligned16(q_e4m3) || !aligned4(sA) || !aligned4(perm) || ld_packed % 16 != 0 ||
+        ldq % 16 != 0)
+        return FP8BS_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    const int64_t blocks = (M + UNPACK_ROWS - 1) / UNPACK_ROWS;
+    if (blocks > INT32_MAX)
+        return FP8BS_ERR_SHAPE;
+    ep_unpack_kernel<<<(unsigned)blocks, UNPACK_THREADS, 0, stream>>>(
+        static_cast<const uint8_t *>(packed), ld_packed, n_src, KB, perm, M, static_cast<uint8_t *>(q_e4m3), ldq, sA);
+    return launch_status();
+}
+
+int fp8bs_gather_rows(const void *src, int64_t n_src, int64_t ld_src, const int32_t *rows, int64_t M,
+                      int64_t row_bytes, void *dst, int64_t ld_dst, cudaStream_t stream)
+{
+    if (n_src < 0 || M < 0 || row_bytes < 0 || row_bytes % 16 != 0)
+        return FP8BS_ERR_SHAPE;
+    if (M == 0 || row_bytes == 0)
+        return FP8BS_OK;
+    if (!src || !rows || !dst)
+        return FP8BS_ERR_NULL;
+    if (ld_src < row_bytes || ld_dst < row_bytes)
+        return FP8BS_ERR_SHAPE;
+    if (!aligned16(src) || !aligned16(dst) || !aligned4(rows) || ld_src % 16 != 0 || ld_dst % 16 != 0)
+        return FP8BS_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    const int64_t blocks = std::min<int64_t>((M * 32 + 255) / 256, 8 * (int64_t)dev->num_sms);
+    gather_rows_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint8_t *>(src), n_src, ld_src, rows,
+                                                             M, row_bytes / 16, static_cast<uint8_t *>(dst), ld_dst);
     return launch_status();
 }
 

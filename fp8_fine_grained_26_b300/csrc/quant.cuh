@@ -627,6 +627,10 @@ __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_fixed_kernel(
 constexpr int GATHER_THREADS = 256;
 constexpr int GATHER_TILES = 8;                                  // tiles per warp task
 
+// PACKED (expert-parallel dispatch): row i of q holds the row's K codes
+// followed by its KB scales (FP32, row-major), so that one all-to-all moves a
+// routed row and its scales together; sA is unused.
+template <bool PACKED = false>
 __global__ void __launch_bounds__(GATHER_THREADS) quant_act_gather_kernel(
     const uint16_t *__restrict__ x, int64_t T, int64_t ldx, const int32_t *__restrict__ rows, int64_t M,
     int64_t KB, uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ sA)
@@ -697,9 +701,103 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_gather_kernel(
             if (kb < KB) {
                 const uint2 c = recip ? quant_8_recip(v[t], d) : quant_8(v[t], d);
                 ptx::st_v2_cs(qrow + kb * 128, c.x, c.y);
-                if (l16 == 0)
-                    sA[kb * M + i] = d.s;
+                if (l16 == 0) {
+                    if constexpr (PACKED)
+                        reinterpret_cast<float *>(q + i * ldq + KB * 128)[kb] = d.s;
+                    else
+                        sA[kb * M + i] = d.s;
+                }
             }
+        }
+    }
+}
+
+// Expert-parallel receive side: rows packed as [K codes | KB FP32 scales]
+// arrive grouped by source rank; output row i is packed row perm[i], its
+// codes into q[i] and its scales into the grouped GEMM's column layout
+// sA[kb][i].  A block takes 32 output rows: its warps copy the codes (16-byte
+// loads and stores), then the 32 x KB scales go through shared memory so
+// that each sA run of 32 rows is one 128-byte store.  An index outside
+// [0, n_src) gives zero codes and scales and sets bit 1 of the error word.
+constexpr int UNPACK_THREADS = 256;
+constexpr int UNPACK_ROWS = 32;
+constexpr int UNPACK_KB_CHUNK = 64;
+
+__global__ void __launch_bounds__(UNPACK_THREADS) ep_unpack_kernel(
+    const uint8_t *__restrict__ packed, int64_t ld_packed, int64_t n_src, int64_t KB, const int32_t *__restrict__ perm,
+    int64_t M, uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ sA)
+{
+    __shared__ float tile[UNPACK_KB_CHUNK][UNPACK_ROWS + 1];
+    __shared__ int64_t src_row[UNPACK_ROWS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t i0 = (int64_t)blockIdx.x * UNPACK_ROWS;
+    if (threadIdx.x < UNPACK_ROWS) {
+        const int64_t i = i0 + threadIdx.x;
+        int64_t s = -1;
+        if (i < M) {
+            const int32_t p = perm[i];
+            if (p >= 0 && (int64_t)p < n_src)
+                s = p;
+            else
+                atomicOr(&g_error_word, 2u);
+        }
+        src_row[threadIdx.x] = s;
+    }
+    __syncthreads();
+    const int64_t chunks = KB * 8;                                   // 16-byte chunks of codes per row
+    for (int r = warp; r < UNPACK_ROWS; r += UNPACK_THREADS / 32) {
+        const int64_t i = i0 + r;
+        if (i >= M)
+            break;
+        const int64_t s = src_row[r];
+        uint8_t *dst = q + i * ldq;
+        for (int64_t c = lane; c < chunks; c += 32) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (s >= 0)
+                v = *reinterpret_cast<const uint4 *>(packed + s * ld_packed + c * 16);
+            ptx::st_v4(dst + c * 16, v.x, v.y, v.z, v.w);
+        }
+    }
+    for (int64_t kb0 = 0; kb0 < KB; kb0 += UNPACK_KB_CHUNK) {
+        const int nkb = (int)min((int64_t)UNPACK_KB_CHUNK, KB - kb0);
+        __syncthreads();
+        for (int e = threadIdx.x; e < UNPACK_ROWS * nkb; e += UNPACK_THREADS) {
+            const int r = e / nkb, kb = e - r * nkb;
+            const int64_t s = src_row[r];
+            tile[kb][r] = s >= 0 ? reinterpret_cast<const float *>(packed + s * ld_packed + KB * 128)[kb0 + kb] : 0.0f;
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < UNPACK_ROWS * nkb; e += UNPACK_THREADS) {
+            const int kb = e / UNPACK_ROWS, r = e - kb * UNPACK_ROWS;
+            if (i0 + r < M)
+                sA[(kb0 + kb) * M + i0 + r] = tile[kb][r];
+        }
+    }
+}
+
+// Row gather of byte rows: dst row i = src row rows[i] (row_bytes a multiple
+// of 16, both row starts 16-byte aligned).  One warp per row, 16-byte copies.
+// An index outside [0, n_src) gives a zero row and sets bit 1 of the error
+// word.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t *__restrict__ src, int64_t n_src,
+                                                          int64_t ld_src, const int32_t *__restrict__ rows, int64_t M,
+                                                          int64_t chunks, uint8_t *__restrict__ dst, int64_t ld_dst)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = w0; i < M; i += nw) {
+        const int32_t p = rows[i];
+        const bool ok = p >= 0 && (int64_t)p < n_src;
+        if (!ok && lane == 0)
+            atomicOr(&g_error_word, 2u);
+        const uint8_t *s = src + (ok ? (int64_t)p : 0) * ld_src;
+        uint8_t *d = dst + i * ld_dst;
+        for (int64_t c = lane; c < chunks; c += 32) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (ok)
+                v = *reinterpret_cast<const uint4 *>(s + c * 16);
+            ptx::st_v4(d + c * 16, v.x, v.y, v.z, v.w);
         }
     }
 }

@@ -179,6 +179,58 @@ int fp8_quant_act_1x128_gather(const void *x_bf16, int64_t T, int64_t K, int64_t
                                int64_t M, void *q_e4m3, int64_t ldq, float *sA, cudaStream_t stream);
 
 /*
+ * Expert-parallel dispatch, sending side: the routed copies of token rows,
+ * gathered and quantised per 1x128 tile exactly as
+ * fp8_quant_act_1x128_gather does, but each output row PACKED with its own
+ * scales so that one all-to-all moves a routed row in FP8 together with the
+ * FP32 scales it needs.  The pages dispatch activations to the experts on
+ * other devices in FP8 over an all-to-all ("DeepSeek-V3 training
+ * walkthrough", section 二, cross-node all-to-all / expert parallelism, and
+ * section 二(四), last item: activations cached and dispatched in FP8;
+ * qqstock.cn walkthrough, FP8 section, report figure 10).
+ *   x_bf16 : [T][K] BF16 token rows, row stride ldx (elements).
+ *   rows   : [M] int32 on the device: the token row of each routed copy, in
+ *            send order.
+ *   packed : [M] rows of ld_packed bytes: bytes [0, K) are row i's E4M3
+ *            codes, bytes [K, K + 4*K/128) its K/128 FP32 scales (tile kb's
+ *            scale at float index kb).  ld_packed >= K + 4*K/128 and a
+ *            multiple of 16.
+ * Codes and scales equal fp8_quant_act_1x128 of the gathered rows, bit for
+ * bit.  Index errors and alignment rules as fp8_quant_act_1x128_gather.
+ */
+int fp8_ep_dispatch_pack(const void *x_bf16, int64_t T, int64_t K, int64_t ldx, const int32_t *rows, int64_t M,
+                         void *packed, int64_t ld_packed, cudaStream_t stream);
+
+/*
+ * Expert-parallel dispatch, receiving side: packed rows (fp8_ep_dispatch_pack
+ * layout) as they arrive from the all-to-all, grouped by source rank, are
+ * reordered into expert-major order for the grouped GEMM: output row i is
+ * packed row perm[i]; its codes go to q_e4m3[i] and its scales to
+ * sA[kb][i] (the [K/128][M] layout the GEMMs read).
+ *   packed : [n_src] rows, row stride ld_packed bytes.
+ *   perm   : [M] int32 on the device, each in [0, n_src).
+ *   q_e4m3 : [M][K] E4M3, row stride ldq bytes; sA : [K/128][M] FP32.
+ * An index outside [0, n_src) gives a zero row and zero scales and makes the
+ * next fp8bs_last_error report FP8BS_ERR_INDEX.  Pure data movement: the
+ * output is bit-identical to the packed input.
+ */
+int fp8_ep_unpack(const void *packed, int64_t n_src, int64_t ld_packed, int64_t K, const int32_t *perm, int64_t M,
+                  void *q_e4m3, int64_t ldq, float *sA, cudaStream_t stream);
+
+/*
+ * Row gather of byte rows, the data movement of the expert-parallel return
+ * path (expert outputs back to their source rank, then into token/slot
+ * order): dst row i = src row rows[i], row_bytes bytes each.
+ *   src : [n_src] rows, row stride ld_src bytes;  dst : [M] rows, ld_dst.
+ *   rows: [M] int32 on the device.
+ * row_bytes, ld_src, ld_dst multiples of 16; src and dst 16-byte aligned.
+ * An index outside [0, n_src) gives a zero row and FP8BS_ERR_INDEX at the
+ * next fp8bs_last_error.
+ */
+int fp8bs_gather_rows(const void *src, int64_t n_src, int64_t ld_src, const int32_t *rows, int64_t M,
+                      int64_t row_bytes, void *dst, int64_t ld_dst, cudaStream_t stream);
+
+/*
  * Token-dimension 1x128 quantisation, for the operands of the weight-gradient
  * GEMM dW = dY^T . X, whose contraction runs over tokens.  The pages run all
  * three GEMM kinds (forward, data gradient, weight gradient) in FP8 with
