@@ -9,7 +9,8 @@ configurations that fit one GPU; A and W are quantised in one launch
 (``--quant split`` runs the two single-operand quantisers concurrently
 instead).  The default run adds, in the same JSON line, one sub-record per
 other configuration (MLA q, MLA kv, routed experts, weight gradient, tiny),
-each timed in its own region, and the quantisers-alone table.
+each timed in its own region, the per-tensor contrast scheme on the dgrad and
+MLA q shapes, and the quantisers-alone table.
 ``--workload`` selects another headline shape (mla_q, mla_kv, wgrad,
 experts, tiny, experts_small) and then measures only that one.  For ``experts`` a step is the gather +
 quantisation of the routed token rows plus the grouped GEMM (expert weights
@@ -153,6 +154,7 @@ class ClockSampler:
 # ---------------------------------------------------------------- workloads
 def make_workload(name, device):
     import synthetic
+    name = name.replace("_per_tensor", "")
     if name == "mla_q":
         return synthetic.mla_q(device=device)
     if name == "mla_kv":
@@ -297,6 +299,62 @@ class DenseStep:
                                             qC=outs[0], sC=outs[1])
         else:
             f.fp8_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major, C=outs[0])
+
+
+class PerTensorStep:
+    """The per-tensor contrast scheme on a dense workload: quantise A and W
+    with one scale each (fp8_quant_per_tensor: unit amaxes, reduction,
+    encoding -- it reads each operand twice) -> GEMM accumulating the whole K
+    on the tensor cores (fp8_gemm_per_tensor), over rotating input sets."""
+
+    def __init__(self, case, fp8, torch):
+        self.fp8, self.torch, self.case = fp8, torch, case
+        M, K, N = case.M, case.K, case.N
+        self.M, self.N, self.K, self.b_major = M, N, K, case.b_major
+        in_bytes = (case.a.numel() + case.w.numel()) * 2
+        self.nsets = max(1, min(8, -(-2 * L2_BYTES // in_bytes) + 1))
+        self.sets = [(case.a, case.w)] + [(case.a.clone(), case.w.clone()) for _ in range(self.nsets - 1)]
+        dev = case.a.device
+        R, C = case.w.shape
+        self.qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        self.qb = torch.empty((R, C), dtype=torch.uint8, device=dev)
+        self.sa = torch.empty((1,), dtype=torch.float32, device=dev)
+        self.sb = torch.empty((1,), dtype=torch.float32, device=dev)
+        self.wsa = torch.empty((fp8.fp8_quant_per_tensor_workspace_size(M, K),), dtype=torch.uint8, device=dev)
+        self.wsb = torch.empty((fp8.fp8_quant_per_tensor_workspace_size(R, C),), dtype=torch.uint8, device=dev)
+        self.c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.flops = 2.0 * M * N * K
+        self.kernels = ["quant_a_per_tensor", "quant_w_per_tensor", "gemm"]
+        # two reads (the amax pass, then the encoding pass) and one write per element
+        self.kernel_bytes = {"quant_a_per_tensor": M * K * 5, "quant_w_per_tensor": R * C * 5,
+                             "gemm": M * K + R * C + 8 + M * N * 2}
+        self.h2d_bytes = in_bytes
+        self.d2h_bytes = M * N * 2
+        self.launches_per_step = 7
+        self.schedule = "quant_per_tensor(A) -> quant_per_tensor(W) -> gemm_per_tensor (whole K on the tensor cores)"
+
+    def run(self, i, events=None):
+        a, w = self.sets[i % self.nsets]
+        self.compute([a, w], [self.c], events)
+
+    def host_inputs(self):
+        return [self.case.a.cpu().pin_memory(), self.case.w.cpu().pin_memory()]
+
+    def out_buffers(self):
+        return [torch_empty_like(self.torch, self.c)]
+
+    def compute(self, dev_in, outs, events=None):
+        a, w = dev_in
+        f = self.fp8
+        if events: events[0].record()
+        f.fp8_quant_per_tensor(a, self.qa, self.sa, self.wsa)
+        if events: events[1].record()
+        if events: events[2].record()
+        f.fp8_quant_per_tensor(w, self.qb, self.sb, self.wsb)
+        if events: events[3].record()
+        if events: events[4].record()
+        f.fp8_gemm_per_tensor(self.qa, self.sa, self.qb, self.sb, b_major=self.b_major, C=outs[0])
+        if events: events[5].record()
 
 
 class WgradStep:
@@ -573,7 +631,7 @@ def gemm_traffic(kernel, workload):
 SUSTAINED_MIN_S = 1.0
 
 HEADLINE = "dgrad"                                  # the largest configuration that fits one GPU
-SUBRECORD_WORKLOADS = ("mla_q", "mla_kv", "experts", "wgrad", "tiny")
+SUBRECORD_WORKLOADS = ("mla_q", "mla_kv", "experts", "wgrad", "tiny", "dgrad_per_tensor", "mla_q_per_tensor")
 
 
 def choose_peaks(peaks, region_s, clk):
@@ -590,6 +648,8 @@ def choose_peaks(peaks, region_s, clk):
 
 
 def build_step(name, case, fp8, torch, args):
+    if name.endswith("_per_tensor"):
+        return PerTensorStep(case, fp8, torch)
     if name in ("experts", "experts_small"):
         return ExpertsStep(case, fp8, torch)
     if name == "wgrad":
@@ -602,7 +662,7 @@ def measure(args, name, fp8, torch, peaks, peak_src, world, rank, local, device,
     every kernel), end to end from host buffers, rooflines.  Returns the
     record (the JSON line's body for the headline, a sub-record otherwise)."""
     case = make_workload(name, device)
-    if args.e4m3_out and name in ("experts", "experts_small", "wgrad"):
+    if args.e4m3_out and (name in ("experts", "experts_small", "wgrad") or name.endswith("_per_tensor")):
         raise SystemExit("--e4m3-out applies to the dense forward workloads")
     step = build_step(name, case, fp8, torch, args)
     stream = torch.cuda.current_stream()
@@ -714,7 +774,7 @@ def measure(args, name, fp8, torch, peaks, peak_src, world, rank, local, device,
         import oracle
         if name == "wgrad":
             flops, secs, desc = oracle_sample_wgrad(case)
-        elif name not in ("experts", "experts_small"):
+        elif name not in ("experts", "experts_small") and not name.endswith("_per_tensor"):
             flops, secs, desc = oracle_sample(name, lambda: dense_host_inputs(case))
         else:
             flops = None
@@ -944,7 +1004,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=["mla_q", "mla_kv", "dgrad", "experts", "tiny", "wgrad", "experts_small"],
+                    choices=["mla_q", "mla_kv", "dgrad", "experts", "tiny", "wgrad", "experts_small",
+                             "dgrad_per_tensor", "mla_q_per_tensor", "mla_kv_per_tensor"],
                     help="the headline workload (default: dgrad, the largest configuration)")
     ap.add_argument("--no-subrecords", action="store_true",
                     help="with the default workload, skip the other configurations' sub-records and the "
