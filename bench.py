@@ -12,8 +12,9 @@ other configuration (MLA q, MLA kv, routed experts, weight gradient, tiny),
 each timed in its own region, the per-tensor contrast scheme on the dgrad and
 MLA q shapes, and the quantisers-alone table.
 ``--workload`` selects another headline shape (mla_q, mla_kv, wgrad,
-experts, tiny, experts_small) and then measures only that one.  For ``experts`` a step is the gather +
-quantisation of the routed token rows plus the grouped GEMM (expert weights
+experts, tiny, experts_small) and then measures only that one.  For ``experts`` a step is the dispatch
+quantisation (each token row encoded once and its codes written to each of
+its routed rows) plus the grouped GEMM (expert weights
 are quantised once, before timing, as they are once per weight update); for
 ``wgrad`` it is the token-dimension quantisation of dY and X plus the
 weight-gradient GEMM.
@@ -441,30 +442,34 @@ class ExpertsStep:
         case.w = None                       # the BF16 weights are not needed any more
         torch.cuda.empty_cache()
         self.x = case.x                      # [tokens, K] BF16, before the dispatch
-        self.rows = case.token_of_row.to(torch.int32)
         T = self.x.shape[0]
+        # dest[t, j]: the j-th routed row that holds token t (the scatter form of the dispatch)
+        import numpy as np
+        tok = case.token_of_row.cpu().numpy()
+        self.topk = tok.shape[0] // T
+        self.dest = torch.from_numpy(np.argsort(tok, kind="stable").reshape(T, self.topk).astype(np.int32)).to(dev)
         case.x_sorted = None
         self.qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
         self.sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
         self.c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         self.nsets = 1                      # 3.76 GB of expert weights stream per step (> L2)
         self.flops = 2.0 * M * N * K
-        self.kernels = ["quant_gather", "grouped_gemm"]
+        self.kernels = ["quant_scatter", "grouped_gemm"]
         self.kernel_bytes = {
             # each token row read once, every routed copy written once
-            "quant_gather": T * K * 2 + M * 4 + M * K + (K // 128) * M * 4,
+            "quant_scatter": T * K * 2 + M * 4 + M * K + (K // 128) * M * 4,
             "grouped_gemm": M * K + E * N * K + (self.sa.numel() + self.sb.numel()) * 4 + M * N * 2,
         }
         self.h2d_bytes = T * K * 2 + M * 4
         self.d2h_bytes = M * N * 2
         self.launches_per_step = 2
-        self.schedule = "quant_gather(X, routed rows) -> grouped_gemm"
+        self.schedule = "quant_scatter(X -> its routed rows) -> grouped_gemm"
 
     def run(self, i, events=None):
         """events: (start, end) per kernel in `kernels` order, or None."""
         f = self.fp8
         if events: events[0].record()
-        f.fp8_quant_act_1x128_gather(self.x, self.rows, self.qa, self.sa)
+        f.fp8_quant_act_1x128_scatter(self.x, self.dest, self.M, self.qa, self.sa)
         if events: events[1].record()
         if events: events[2].record()
         f.fp8_grouped_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, self.case.offsets,
@@ -472,16 +477,16 @@ class ExpertsStep:
         if events: events[3].record()
 
     def host_inputs(self):
-        # the token rows and the routed row list come from the host every step
-        return [self.x.cpu().pin_memory(), self.rows.cpu().pin_memory()]
+        # the token rows and their routed destinations come from the host every step
+        return [self.x.cpu().pin_memory(), self.dest.cpu().pin_memory()]
 
     def out_buffers(self):
         return [torch_empty_like(self.torch, self.c)]
 
     def compute(self, dev_in, outs):
-        x, rows = dev_in
+        x, dest = dev_in
         f = self.fp8
-        f.fp8_quant_act_1x128_gather(x, rows, self.qa, self.sa)
+        f.fp8_quant_act_1x128_scatter(x, dest, self.M, self.qa, self.sa)
         f.fp8_grouped_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, self.case.offsets, C=outs[0])
 
 

@@ -42,7 +42,7 @@ EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp
             "fp8bs_selftest_wait_timeout", "fp8bs_selftest_set_wait_limit",
             "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor", "fp8_quant_per_tensor_delayed",
             "fp8_gemm_per_tensor", "fp8_quant_per_tensor_noalloc", "fp8_ep_dispatch_pack", "fp8_ep_unpack",
-            "fp8bs_gather_rows")
+            "fp8bs_gather_rows", "fp8_quant_act_1x128_scatter")
 
 
 class Fp8bsError(RuntimeError):
@@ -78,6 +78,7 @@ def _load():
         "fp8_ep_dispatch_pack": [p, i64, i64, i64, p, i64, p, i64, p],
         "fp8_ep_unpack": [p, i64, i64, i64, p, i64, p, i64, p, p],
         "fp8bs_gather_rows": [p, i64, i64, p, i64, i64, p, i64, p],
+        "fp8_quant_act_1x128_scatter": [p, i64, i64, i64, p, i32, i64, p, i64, p, p],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -435,6 +436,31 @@ def fp8_gemm_per_tensor(qA, sA, qB, sB, b_major=B_KMAJOR, out_dtype=torch.bfloat
     return C
 
 
+def fp8_quant_act_1x128_scatter(x, dest, M, q=None, sA=None, stream=None):
+    """Token row t of BF16 ``x [T, K]`` quantised once per 1x128 tile and
+    written to rows ``dest[t, j]`` of ``q [M, K]`` / columns of ``sA [K/128, M]``
+    (``dest``: CUDA int32 ``[T, topk]``)."""
+    _need(x, torch.bfloat16, "x", 2)
+    _row_major(x, "x")
+    if dest.dtype != torch.int32 or dest.dim() != 2 or not dest.is_cuda or dest.shape[0] != x.shape[0]:
+        raise TypeError("dest: expected a CUDA int32 tensor [T, topk]")
+    T, K = x.shape
+    topk = dest.shape[1]
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if sA is None:
+        sA = torch.empty((K // 128, M), dtype=torch.float32, device=x.device)
+    _need(q, torch.uint8, "q", 2)
+    _row_major(q, "q")
+    if tuple(q.shape) != (M, K) or not sA.is_contiguous() or sA.numel() != (K // 128) * M:
+        raise ValueError("output shapes do not match")
+    ldx = x.stride(0) if T > 0 else K
+    ldq = q.stride(0) if M > 0 else K
+    _check(lib.fp8_quant_act_1x128_scatter(_ptr(x), T, K, ldx, _ptr(dest.contiguous()), topk, M, _ptr(q), ldq,
+                                           _ptr(sA), _stream(stream)), "fp8_quant_act_1x128_scatter")
+    return q, sA
+
+
 def packed_row_bytes(K):
     """Row stride (bytes) of a packed dispatch row: K codes + K/128 FP32
     scales, rounded up to 16."""
@@ -531,6 +557,6 @@ __all__ = ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8
            "fp8_quant_act_1x128_gather", "FP8BS_ERR_INDEX",
            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout",
            "fp8bs_selftest_set_wait_limit", "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor",
-           "fp8_quant_per_tensor_delayed", "fp8_gemm_per_tensor", "packed_row_bytes", "fp8_ep_dispatch_pack",
+           "fp8_quant_per_tensor_delayed", "fp8_gemm_per_tensor", "fp8_quant_act_1x128_scatter", "packed_row_bytes", "fp8_ep_dispatch_pack",
            "fp8_ep_unpack", "fp8bs_gather_rows", "Fp8bsError", "lib",
            "LIB_PATH", "EXPORTED", "B_KMAJOR", "B_MNMAJOR", "OUT_BF16", "OUT_FP32"]

@@ -608,6 +608,34 @@ int fp8_quant_act_1x128_gather(const void *x_bf16, int64_t T, int64_t K, int64_t
     return launch_status();
 }
 
+int fp8_quant_act_1x128_scatter(const void *x_bf16, int64_t T, int64_t K, int64_t ldx, const int32_t *dest, int topk,
+                                int64_t M, void *q_e4m3, int64_t ldq, float *sA, cudaStream_t stream)
+{
+    if (T < 0 || M < 0 || K < 0 || K % 128 != 0)
+        return FP8BS_ERR_SHAPE;
+    if (topk < 1 || topk > SCATTER_MAX_TOPK)
+        return FP8BS_ERR_ARG;
+    if (T == 0 || K == 0)
+        return FP8BS_OK;
+    if (!x_bf16 || !dest || !q_e4m3 || !sA)
+        return FP8BS_ERR_NULL;
+    if (ldx < K || ldq < K)
+        return FP8BS_ERR_SHAPE;
+    if (!aligned16(x_bf16) || !aligned16(q_e4m3) || !aligned4(sA) || !aligned4(dest) || (ldx * 2) % 16 != 0 ||
+        ldq % 16 != 0)
+        return FP8BS_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    const int64_t KB = K / 128;
+    const int64_t tasks = T * ((KB + GATHER_TILES - 1) / GATHER_TILES);
+    const int64_t blocks = std::min<int64_t>((tasks * 32 + GATHER_THREADS - 1) / GATHER_THREADS,
+                                             8 * (int64_t)dev->num_sms);
+    quant_act_scatter_kernel<<<(unsigned)blocks, GATHER_THREADS, 0, stream>>>(
+        static_cast<const uint16_t *>(x_bf16), T, ldx, dest, topk, M, KB, static_cast<uint8_t *>(q_e4m3), ldq, sA);
+    return launch_status();
+}
+
 int fp8_ep_dispatch_pack(const void *x_bf16, int64_t T, int64_t K, int64_t ldx, const int32_t *rows, int64_t M,
                          void *packed, int64_t ld_packed, cudaStream_t stream)
 {

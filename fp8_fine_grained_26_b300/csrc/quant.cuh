@@ -712,6 +712,98 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_gather_kernel(
     }
 }
 
+// Scatter + 1x128 activation quantisation, the dispatch written from the
+// token side: token row t is read and encoded ONCE and its codes and scales
+// are stored to each of its topk destination rows dest[t * topk + j].  The
+// result is the gather form's (quantising before or after the copy gives the
+// same bytes), with a topk-th of the loads and of the encoding work.  A warp
+// task is one token row x GATHER_TILES consecutive 1x128 tiles, as in the
+// gather kernel; lane j < topk fetches destination j and the warp broadcasts
+// it.  A destination outside [0, M) is skipped and sets bit 1 of the error
+// word; a row named twice receives one of the tokens (unspecified which).
+constexpr int SCATTER_MAX_TOPK = 32;
+
+__global__ void __launch_bounds__(GATHER_THREADS) quant_act_scatter_kernel(
+    const uint16_t *__restrict__ x, int64_t T, int64_t ldx, const int32_t *__restrict__ dest, int topk, int64_t M,
+    int64_t KB, uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ sA)
+{
+    const int lane = threadIdx.x & 31;
+    const int half = lane >> 4;
+    const int l16 = lane & 15;
+    const int hbase = lane & 16;
+    const int64_t chunks = (KB + GATHER_TILES - 1) / GATHER_TILES;
+    const int64_t warp0 = ((int64_t)blockIdx.x * GATHER_THREADS + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * GATHER_THREADS) >> 5;
+    const int64_t step_t = nwarps / chunks, step_c = nwarps - step_t * chunks;
+    int64_t t = warp0 / chunks, chunk = warp0 - t * chunks;
+    for (; t < T; t += step_t, chunk += step_c) {
+        if (chunk >= chunks) {
+            chunk -= chunks;
+            if (++t >= T)
+                break;
+        }
+        const int64_t kb0 = chunk * GATHER_TILES;
+        int32_t my_dst = -1;
+        if (lane < topk) {
+            my_dst = dest[t * topk + lane];
+            if (my_dst < 0 || (int64_t)my_dst >= M) {
+                if (chunk == 0)
+                    atomicOr(&g_error_word, 2u);
+                my_dst = -1;
+            }
+        }
+        constexpr int TPH = GATHER_TILES / 2;                     // tiles per half-warp
+        uint4 v[TPH];
+#pragma unroll
+        for (int i = 0; i < TPH; ++i) {
+            const int64_t kb = kb0 + 2 * i + half;
+            v[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (kb < KB)
+                v[i] = ptx::ld_nc_v4(x + t * ldx + kb * 128 + l16 * 8);
+        }
+        uint32_t am[TPH];
+#pragma unroll
+        for (int i = 0; i < TPH; ++i) {
+            uint32_t a = absmax_bits8(v[i]);
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1)
+                a = max(a, __shfl_xor_sync(0xffffffffu, a, o, 16));
+            am[i] = a;
+        }
+        uint32_t mine = am[0];
+#pragma unroll
+        for (int i = 1; i < TPH; ++i)
+            mine = (l16 & (TPH - 1)) == i ? am[i] : mine;
+        const Divisor dm = make_divisor(mine);
+        uint2 codes[TPH];
+        float scale[TPH];
+#pragma unroll
+        for (int i = 0; i < TPH; ++i) {
+            Divisor d;
+            d.s = __shfl_sync(0xffffffffu, dm.s, hbase + i);
+            d.r = __shfl_sync(0xffffffffu, dm.r, hbase + i);
+            d.mode = divisor_mode(am[i]);
+            codes[i] = quant_8(v[i], d);
+            scale[i] = d.s;
+        }
+        for (int j = 0; j < topk; ++j) {
+            const int32_t row = __shfl_sync(0xffffffffu, my_dst, j);
+            if (row < 0)
+                continue;
+            uint8_t *qrow = q + (int64_t)row * ldq + l16 * 8;
+#pragma unroll
+            for (int i = 0; i < TPH; ++i) {
+                const int64_t kb = kb0 + 2 * i + half;
+                if (kb < KB) {
+                    ptx::st_v2_cs(qrow + kb * 128, codes[i].x, codes[i].y);
+                    if (l16 == 0)
+                        sA[kb * M + row] = scale[i];
+                }
+            }
+        }
+    }
+}
+
 // Expert-parallel receive side: rows packed as [K codes | KB FP32 scales]
 // arrive grouped by source rank; output row i is packed row perm[i], its
 // codes into q[i] and its scales into the grouped GEMM's column layout

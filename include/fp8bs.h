@@ -179,6 +179,28 @@ int fp8_quant_act_1x128_gather(const void *x_bf16, int64_t T, int64_t K, int64_t
                                int64_t M, void *q_e4m3, int64_t ldq, float *sA, cudaStream_t stream);
 
 /*
+ * Scatter + 1x128 activation quantisation: the expert dispatch written from
+ * the token side.  Token row t is quantised ONCE and its codes and scales are
+ * written to each of its topk destination rows: output row dest[t*topk + j]
+ * (j < topk) is the 1x128 quantisation of x row t.  The pages quantise
+ * activations to FP8 before dispatching them to the routed experts
+ * ("DeepSeek-V3 training walkthrough", section 二(四), last item; qqstock.cn
+ * walkthrough, FP8 section, report figure 10), so every routed copy of a
+ * token carries the same bytes; this call produces them with one read and
+ * one encoding per token instead of one per copy, and its output equals
+ * fp8_quant_act_1x128_gather with rows[dest[t*topk + j]] = t, bit for bit.
+ *   x_bf16 : [T][K] BF16 token rows, row stride ldx (elements).
+ *   dest   : [T][topk] int32 on the device; 1 <= topk <= 32.
+ *   q_e4m3 : [M][K] E4M3, row stride ldq (bytes); sA : [K/128][M] FP32.
+ * Output rows that no dest entry names are not written.  A destination
+ * outside [0, M) is skipped and makes the next fp8bs_last_error report
+ * FP8BS_ERR_INDEX; a row named by two entries receives one of the two tokens.
+ * Alignment rules as fp8_quant_act_1x128 (dest 4-byte aligned).
+ */
+int fp8_quant_act_1x128_scatter(const void *x_bf16, int64_t T, int64_t K, int64_t ldx, const int32_t *dest, int topk,
+                                int64_t M, void *q_e4m3, int64_t ldq, float *sA, cudaStream_t stream);
+
+/*
  * Expert-parallel dispatch, sending side: the routed copies of token rows,
  * gathered and quantised per 1x128 tile exactly as
  * fp8_quant_act_1x128_gather does, but each output row PACKED with its own
