@@ -130,7 +130,6 @@ struct QRing {
     {
         return reinterpret_cast<volatile uint32_t *>(gbase + QSMEM_ABORT);
     }
-    __device__ float *red_f(int b) const { return reinterpret_cast<float *>(gbase + QSMEM_RED) + 256 * b; }
     __device__ uint32_t *red_u(int b) const
     {
         return reinterpret_cast<uint32_t *>(gbase + QSMEM_RED) + 256 * b;
@@ -195,7 +194,8 @@ __device__ __forceinline__ void qdrain(const QRing &r, int64_t consumed, int64_t
 // Activation quantiser.  Unit (mb, kb): rows [128 mb, +128) of tile column kb.
 // Warp w owns rows [16 w, 16 w + 16); at step i its two half-warps take rows
 // 16 w + 2 i and 16 w + 2 i + 1 (512 contiguous bytes of the staged unit).
-// The eight row divisors of a half-warp are formed by eight different lanes
+// The eight row divisors of a half-warp are formed by eight different lanes,
+// which also store the rows' scales (the warp's 16 rows are one 64-byte run),
 // and broadcast with shuffles.  `issue_next` runs once the staged unit has
 // been read (the stage is free again) and queues the CTA's next copy.
 template <class Next>
@@ -217,7 +217,6 @@ __device__ __forceinline__ void act_unit(const QRing &r, int64_t j, int64_t mb, 
     }
     __syncthreads();                                   // the stage is free again
     issue_next();
-    float *scales = r.red_f((int)(j & 1));
     // amax of each of this half-warp's 8 rows, known to all its 16 lanes
     uint32_t am[8];
 #pragma unroll
@@ -234,6 +233,13 @@ __device__ __forceinline__ void act_unit(const QRing &r, int64_t j, int64_t mb, 
     for (int i = 1; i < 8; ++i)
         mine_a = (lane16 & 7) == i ? am[i] : mine_a;
     const Divisor dm = make_divisor(mine_a);
+    // lane i < 8 of the half-warp holds row 2 i + half's scale: the warp's 16
+    // consecutive rows, one 64-byte store
+    if (lane16 < 8) {
+        const int64_t gm = mb * 128 + 2 * lane16 + (hw & 1) + 16 * (hw >> 1);
+        if (gm < M)
+            sA[kb * M + gm] = dm.s;
+    }
     const int half_base = (tid & 16);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -247,12 +253,7 @@ __device__ __forceinline__ void act_unit(const QRing &r, int64_t j, int64_t mb, 
             const uint2 c = quant_8(v[i], d);
             ptx::st_v2(q + gm * ldq + kb * 128 + lane16 * 8, c.x, c.y);
         }
-        if (lane16 == 0)
-            scales[row] = d.s;
     }
-    __syncthreads();
-    if (tid < 128 && mb * 128 + tid < M)
-        sA[kb * M + mb * 128 + tid] = scales[tid];
 }
 
 // Weight quantiser.  Unit (rb, cb): one 128x128 block.  Thread t owns the
