@@ -678,19 +678,27 @@ def measure(args, name, fp8, torch, peaks, peak_src, world, rank, local, device,
         raise RuntimeError(f"{name}: device error during warm-up")
 
     # The K timed steps are captured once into a CUDA graph (no host launch
-    # gaps between kernels), with a timing event recorded before and after
-    # every kernel of every step, on the stream that kernel runs on; one
-    # untimed replay uploads the graph.
+    # gaps between kernels, and nothing between consecutive kernels, so a
+    # kernel's on-chip set-up may overlap the end of the one before it).  A
+    # second graph of the same K steps records a timing event before and
+    # after every kernel, on the stream that kernel runs on: it gives the
+    # per-kernel times (each kernel then runs alone between its events).  One
+    # untimed replay of each uploads it.
     nk = len(step.kernels)
     evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2 * nk)]
            for _ in range(args.steps)]
-    graph = None
+    graph = graph_evt = None
     if not args.eager:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for i in range(args.steps):
+                step.run(i)
+        graph_evt = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_evt):
+            for i in range(args.steps):
                 step.run(i, evs[i])
         graph.replay()
+        graph_evt.replay()
         torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -709,6 +717,9 @@ def measure(args, name, fp8, torch, peaks, peak_src, world, rank, local, device,
     t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
+    if graph_evt is not None:
+        graph_evt.replay()                  # per-kernel times
+        torch.cuda.synchronize()
     barrier(world)
     if fp8.fp8bs_last_error() != 0:
         raise RuntimeError(f"{name}: device error in the timed region")
@@ -720,7 +731,7 @@ def measure(args, name, fp8, torch, peaks, peak_src, world, rank, local, device,
         per_kernel[kname] = sum(e[2 * j].elapsed_time(e[2 * j + 1]) for e in evs) / args.steps
     ms_per_step = elapsed_ms / args.steps
     value = world * step.flops / (ms_per_step * 1e-3) / 1e12
-    del graph
+    del graph, graph_evt
 
     # ---- end-to-end through the same C-ABI calls from pinned host buffers
     e2e = None
@@ -798,7 +809,8 @@ def measure(args, name, fp8, torch, peaks, peak_src, world, rank, local, device,
                    "l2": (f"inputs rotate over {step.nsets} sets (> 2x the 126 MB L2)"
                           if step.nsets > 1 else "inputs larger than L2"),
                    "parallelism": f"replicas x{world}",
-                   "launch": "eager" if args.eager else "CUDA graph of the timed steps"},
+                   "launch": "eager" if args.eager else
+                   "CUDA graph of the timed steps; per-kernel times from a second replay with events around each kernel"},
         "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": step.launches_per_step * args.steps * world,
         "clocks": clk,

@@ -165,6 +165,39 @@ int launch_status()
     return cudaGetLastError() == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
 }
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the previous kernel on the stream finishes; it runs only its on-chip
+// set-up before grid_dep_wait, so stream order is kept for every access to
+// global memory.  cluster > 1 also sets the cluster dimension.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cluster,
+               Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int n = 1;
+    if (cluster > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_LAUNCH;
+    }
+    return launch_status();
+}
+
 // Row-major uint8 matrix [rows][cols] (row stride ld bytes) as a 2-D tensor
 // map with a box of box_cols x box_rows and 128-byte swizzle.
 bool encode_2d_u8(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld,
@@ -319,62 +352,48 @@ int launch_dense(DeviceInfo *dev, const void *qA, const float *sA, const void *q
     }
     if (pair) {
         g.num_tiles = (int64_t)g.num_m_pair * g.num_n_blk;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(2 * std::min<int64_t>(g.num_tiles, dev->max_pairs)));
-        cfg.blockDim = dim3(GEMM_THREADS);
-        cfg.dynamicSmemBytes = tok ? gemm_smem_bytes<false, PAIR_STAGES, B_STAGE_BYTES / 2, SCALE_SLOT_FLOATS_TOK>()
-                                   : gemm_smem_bytes<false, PAIR_STAGES, B_STAGE_BYTES / 2>();
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        cudaError_t e;
+        const dim3 grid2((unsigned)(2 * std::min<int64_t>(g.num_tiles, dev->max_pairs)));
+        const size_t psmem = tok ? gemm_smem_bytes<false, PAIR_STAGES, B_STAGE_BYTES / 2, SCALE_SLOT_FLOATS_TOK>()
+                                 : gemm_smem_bytes<false, PAIR_STAGES, B_STAGE_BYTES / 2>();
+        const dim3 blk(GEMM_THREADS);
         if (tok)
-            e = cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES, false, true>, tmA, tmB, tmC, g);
-        else if (pt)
-            e = b_major == FP8BS_B_KMAJOR
-                    ? cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES, false, false, true>,
-                                         tmA, tmB, tmC, g)
-                    : cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, true, true, PAIR_STAGES, false, false, true>,
-                                         tmA, tmB, tmC, g);
-        else if (b_major == FP8BS_B_KMAJOR)
-            e = qout ? cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES, true>, tmA, tmB, tmC, g)
-                     : cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, false, true, PAIR_STAGES>, tmA, tmB, tmC, g);
-        else
-            e = qout ? cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, true, true, PAIR_STAGES, true>, tmA, tmB, tmC, g)
-                     : cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<false, true, true, PAIR_STAGES>, tmA, tmB, tmC, g);
-        return e == cudaSuccess ? launch_status() : (cudaGetLastError(), FP8BS_ERR_LAUNCH);
+            return launch_pdl(fp8_gemm_kernel<false, false, true, PAIR_STAGES, false, true>, grid2, blk, psmem, stream, 2,
+                              tmA, tmB, tmC, g);
+        if (pt)
+            return b_major == FP8BS_B_KMAJOR
+                       ? launch_pdl(fp8_gemm_kernel<false, false, true, PAIR_STAGES, false, false, true>, grid2, blk,
+                                    psmem, stream, 2, tmA, tmB, tmC, g)
+                       : launch_pdl(fp8_gemm_kernel<false, true, true, PAIR_STAGES, false, false, true>, grid2, blk,
+                                    psmem, stream, 2, tmA, tmB, tmC, g);
+        if (b_major == FP8BS_B_KMAJOR)
+            return qout ? launch_pdl(fp8_gemm_kernel<false, false, true, PAIR_STAGES, true>, grid2, blk, psmem, stream, 2,
+                                     tmA, tmB, tmC, g)
+                        : launch_pdl(fp8_gemm_kernel<false, false, true, PAIR_STAGES>, grid2, blk, psmem, stream, 2, tmA,
+                                     tmB, tmC, g);
+        return qout ? launch_pdl(fp8_gemm_kernel<false, true, true, PAIR_STAGES, true>, grid2, blk, psmem, stream, 2, tmA,
+                                 tmB, tmC, g)
+                    : launch_pdl(fp8_gemm_kernel<false, true, true, PAIR_STAGES>, grid2, blk, psmem, stream, 2, tmA, tmB,
+                                 tmC, g);
     }
     g.num_tiles = (int64_t)g.num_m_blk * g.num_n_blk;
-    const int grid = (int)std::min<int64_t>(g.num_tiles, dev->num_sms);
-    const int smem = gemm_smem_bytes<false, 3>();
-    if (tok) {
-        fp8_gemm_kernel<false, false, false, 3, false, true>
-            <<<grid, GEMM_THREADS, gemm_smem_bytes<false, 3, B_STAGE_BYTES, SCALE_SLOT_FLOATS_TOK>(), stream>>>(
-                tmA, tmB, tmC, g);
-    } else if (pt) {
-        if (b_major == FP8BS_B_KMAJOR)
-            fp8_gemm_kernel<false, false, false, 3, false, false, true><<<grid, GEMM_THREADS, smem, stream>>>(
-                tmA, tmB, tmC, g);
-        else
-            fp8_gemm_kernel<false, true, false, 3, false, false, true><<<grid, GEMM_THREADS, smem, stream>>>(
-                tmA, tmB, tmC, g);
-    } else if (b_major == FP8BS_B_KMAJOR) {
-        if (qout)
-            fp8_gemm_kernel<false, false, false, 3, true><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmC, g);
-        else
-            fp8_gemm_kernel<false, false, false, 3><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmC, g);
-    } else {
-        if (qout)
-            fp8_gemm_kernel<false, true, false, 3, true><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmC, g);
-        else
-            fp8_gemm_kernel<false, true, false, 3><<<grid, GEMM_THREADS, smem, stream>>>(tmA, tmB, tmC, g);
-    }
-    return launch_status();
+    const dim3 grid((unsigned)std::min<int64_t>(g.num_tiles, dev->num_sms));
+    const dim3 blk(GEMM_THREADS);
+    const size_t smem = gemm_smem_bytes<false, 3>();
+    if (tok)
+        return launch_pdl(fp8_gemm_kernel<false, false, false, 3, false, true>, grid, blk,
+                          (size_t)gemm_smem_bytes<false, 3, B_STAGE_BYTES, SCALE_SLOT_FLOATS_TOK>(), stream, 1, tmA, tmB,
+                          tmC, g);
+    if (pt)
+        return b_major == FP8BS_B_KMAJOR
+                   ? launch_pdl(fp8_gemm_kernel<false, false, false, 3, false, false, true>, grid, blk, smem, stream, 1,
+                                tmA, tmB, tmC, g)
+                   : launch_pdl(fp8_gemm_kernel<false, true, false, 3, false, false, true>, grid, blk, smem, stream, 1,
+                                tmA, tmB, tmC, g);
+    if (b_major == FP8BS_B_KMAJOR)
+        return qout ? launch_pdl(fp8_gemm_kernel<false, false, false, 3, true>, grid, blk, smem, stream, 1, tmA, tmB, tmC, g)
+                    : launch_pdl(fp8_gemm_kernel<false, false, false, 3>, grid, blk, smem, stream, 1, tmA, tmB, tmC, g);
+    return qout ? launch_pdl(fp8_gemm_kernel<false, true, false, 3, true>, grid, blk, smem, stream, 1, tmA, tmB, tmC, g)
+                : launch_pdl(fp8_gemm_kernel<false, true, false, 3>, grid, blk, smem, stream, 1, tmA, tmB, tmC, g);
 }
 
 } // namespace
@@ -432,9 +451,9 @@ int fp8_quant_act_1x128(const void *x_bf16, int64_t M, int64_t K, int64_t ldx, v
         return FP8BS_ERR_ARG;
     const int64_t units = ((M + 127) / 128) * (K / 128);
     const int grid = (int)std::min<int64_t>(units, 3 * (int64_t)dev->num_sms);
-    quant_act_1x128_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
-        tmX, M, K / 128, static_cast<uint8_t *>(q_e4m3), ldq, sA, units, wait_limit_single());
-    return launch_status();
+    return launch_pdl(quant_act_1x128_kernel, dim3(grid), dim3(QUANT_THREADS), (size_t)quant_smem_bytes(), stream, 1,
+                      tmX, M, (int64_t)(K / 128), static_cast<uint8_t *>(q_e4m3), ldq, sA, units,
+                      wait_limit_single());
 }
 
 int fp8_quant_w_128x128(const void *w_bf16, int64_t R, int64_t C, int64_t ldw, void *q_e4m3,
@@ -460,9 +479,8 @@ int fp8_quant_w_128x128(const void *w_bf16, int64_t R, int64_t C, int64_t ldw, v
         return FP8BS_ERR_ARG;
     const int64_t units = RB * CB;
     const int grid = (int)std::min<int64_t>(units, 3 * (int64_t)dev->num_sms);
-    quant_w_128x128_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
-        tmW, R, CB, static_cast<uint8_t *>(q_e4m3), ldq, sW, units, wait_limit_single());
-    return launch_status();
+    return launch_pdl(quant_w_128x128_kernel, dim3(grid), dim3(QUANT_THREADS), (size_t)quant_smem_bytes(), stream, 1,
+                      tmW, R, CB, static_cast<uint8_t *>(q_e4m3), ldq, sW, units, wait_limit_single());
 }
 
 // Argument checks shared by the activation and weight quantisers: 0 when the
@@ -526,8 +544,8 @@ int fp8_quant_act_w(const void *x_bf16, int64_t M, int64_t K, int64_t ldx, void 
     a.units = a.units_a + (cw == 0 ? ((R + 127) / 128) * a.CB : 0);
     a.wait_ns = wait_limit_single();
     const int grid = (int)std::min<int64_t>(a.units, 3 * (int64_t)dev->num_sms);
-    quant_act_w_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(tmX, tmW, a);
-    return launch_status();
+    return launch_pdl(quant_act_w_kernel, dim3(grid), dim3(QUANT_THREADS), (size_t)quant_smem_bytes(), stream, 1, tmX,
+                      tmW, a);
 }
 
 int fp8_gemm_blockscaled(const void *qA, const float *sA, const void *qB, const float *sB,
@@ -631,9 +649,9 @@ int fp8_quant_act_1x128_scatter(const void *x_bf16, int64_t T, int64_t K, int64_
     const int64_t tasks = T * ((KB + GATHER_TILES - 1) / GATHER_TILES);
     const int64_t blocks = std::min<int64_t>((tasks * 32 + GATHER_THREADS - 1) / GATHER_THREADS,
                                              8 * (int64_t)dev->num_sms);
-    quant_act_scatter_kernel<<<(unsigned)blocks, GATHER_THREADS, 0, stream>>>(
-        static_cast<const uint16_t *>(x_bf16), T, ldx, dest, topk, M, KB, static_cast<uint8_t *>(q_e4m3), ldq, sA);
-    return launch_status();
+    return launch_pdl(quant_act_scatter_kernel, dim3((unsigned)blocks), dim3(GATHER_THREADS), (size_t)0, stream, 1,
+                      static_cast<const uint16_t *>(x_bf16), T, ldx, dest, topk, M, KB, static_cast<uint8_t *>(q_e4m3),
+                      ldq, sA);
 }
 
 int fp8_ep_dispatch_pack(const void *x_bf16, int64_t T, int64_t K, int64_t ldx, const int32_t *rows, int64_t M,
@@ -732,9 +750,8 @@ int fp8_quant_tokens_1x128(const void *x_bf16, int64_t T, int64_t F, int64_t ldx
     const int64_t FB = (F + 127) / 128;
     const int64_t units = (T / 128) * FB;
     const int grid = (int)std::min<int64_t>(units, 3 * (int64_t)dev->num_sms);
-    quant_tokens_1x128_kernel<<<grid, QUANT_THREADS, quant_smem_bytes(), stream>>>(
-        tmX, T, F, FB, static_cast<uint8_t *>(qT), ldq, s, units, wait_limit_single());
-    return launch_status();
+    return launch_pdl(quant_tokens_1x128_kernel, dim3(grid), dim3(QUANT_THREADS), (size_t)quant_smem_bytes(), stream, 1,
+                      tmX, T, F, FB, static_cast<uint8_t *>(qT), ldq, s, units, wait_limit_single());
 }
 
 int fp8_gemm_wgrad(const void *qA, const float *sA, const void *qB, const float *sB, int64_t M, int64_t N,
@@ -799,8 +816,8 @@ int fp8_grouped_gemm_blockscaled(const void *qA, const float *sA, const void *qB
     g.KB = (int)(K / BK);
     g.NB128 = (int)((N + 127) / 128);
     g.num_tiles = 0;
-    fp8_gemm_kernel<true, false, false, 3><<<dev->num_sms, GEMM_THREADS, gemm_smem_bytes<true, 3>(), stream>>>(tmA, tmB, tmC, g);
-    return launch_status();
+    return launch_pdl(fp8_gemm_kernel<true, false, false, 3>, dim3(dev->num_sms), dim3(GEMM_THREADS),
+                      (size_t)gemm_smem_bytes<true, 3>(), stream, 1, tmA, tmB, tmC, g);
 }
 
 int fp8_quant_per_tensor_workspace_size(int64_t R, int64_t C, int64_t *bytes)

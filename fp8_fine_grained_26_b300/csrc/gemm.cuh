@@ -425,6 +425,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    ptx::grid_dep_launch();                          // the next kernel may start its own set-up
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -462,6 +463,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             ptx::tmem_relinquish();
         }
     }
+    // Everything above touches only this CTA's shared and tensor memory; the
+    // first global reads (expert offsets, operands, scales) wait for the
+    // kernels this one depends on.
+    ptx::grid_dep_wait();
     if constexpr (GROUPED)
         build_tile_prefix(g, ss);                    // ends with __syncthreads
     ptx::tc_fence_before();

@@ -436,6 +436,21 @@ __device__ __forceinline__ void st_v4(void *p, uint32_t a, uint32_t b, uint32_t 
                  : "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel on
+// the stream be scheduled before this one ends (it still waits in
+// grid_dep_wait); grid_dep_wait blocks until every kernel this one depends on
+// has completed and its memory is visible.  Both are no-ops for a kernel
+// launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void grid_dep_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Lane-wise unsigned 16-bit max of two packed pairs.
 __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b)
 {

@@ -139,6 +139,7 @@ struct QRing {
 __device__ __forceinline__ QRing qring_setup(uint64_t wait_ns)
 {
     extern __shared__ uint8_t smem_raw[];
+    ptx::grid_dep_launch();                      // the next kernel may start its own set-up
     QRing r;
     r.wait_ns = wait_ns;
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -151,6 +152,7 @@ __device__ __forceinline__ QRing qring_setup(uint64_t wait_ns)
         ptx::fence_mbarrier_init();
     }
     __syncthreads();
+    ptx::grid_dep_wait();                        // global memory only after the kernels this one depends on
     return r;
 }
 
@@ -728,6 +730,8 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_scatter_kernel(
     const uint16_t *__restrict__ x, int64_t T, int64_t ldx, const int32_t *__restrict__ dest, int topk, int64_t M,
     int64_t KB, uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ sA)
 {
+    ptx::grid_dep_launch();
+    ptx::grid_dep_wait();
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4;
     const int l16 = lane & 15;
