@@ -42,7 +42,7 @@ EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp
             "fp8bs_selftest_wait_timeout", "fp8bs_selftest_set_wait_limit",
             "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor", "fp8_quant_per_tensor_delayed",
             "fp8_gemm_per_tensor", "fp8_quant_per_tensor_noalloc", "fp8_ep_dispatch_pack", "fp8_ep_unpack",
-            "fp8bs_gather_rows", "fp8_quant_act_1x128_scatter")
+            "fp8bs_gather_rows", "fp8_quant_act_1x128_scatter", "fp8_ep_dispatch_pack_scatter")
 
 
 class Fp8bsError(RuntimeError):
@@ -79,6 +79,7 @@ def _load():
         "fp8_ep_unpack": [p, i64, i64, i64, p, i64, p, i64, p, p],
         "fp8bs_gather_rows": [p, i64, i64, p, i64, i64, p, i64, p],
         "fp8_quant_act_1x128_scatter": [p, i64, i64, i64, p, i32, i64, p, i64, p, p],
+        "fp8_ep_dispatch_pack_scatter": [p, i64, i64, i64, p, i32, i64, p, i64, p],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -489,6 +490,27 @@ def fp8_ep_dispatch_pack(x, rows, packed=None, stream=None):
     return packed
 
 
+def fp8_ep_dispatch_pack_scatter(x, dest, M, packed=None, stream=None):
+    """Token row t of BF16 ``x [T, K]`` quantised once and packed (codes, then
+    its scales) into send rows ``dest[t, j]`` of ``packed [M, packed_row_bytes(K)]``."""
+    _need(x, torch.bfloat16, "x", 2)
+    _row_major(x, "x")
+    if dest.dtype != torch.int32 or dest.dim() != 2 or not dest.is_cuda or dest.shape[0] != x.shape[0]:
+        raise TypeError("dest: expected a CUDA int32 tensor [T, topk]")
+    T, K = x.shape
+    if packed is None:
+        packed = torch.empty((M, packed_row_bytes(K)), dtype=torch.uint8, device=x.device)
+    _need(packed, torch.uint8, "packed", 2)
+    _row_major(packed, "packed")
+    if packed.shape[0] != M:
+        raise ValueError("packed must have M rows")
+    ldx = x.stride(0) if T > 0 else K
+    ld = packed.stride(0) if M > 0 else packed.shape[1]
+    _check(lib.fp8_ep_dispatch_pack_scatter(_ptr(x), T, K, ldx, _ptr(dest.contiguous()), dest.shape[1], M,
+                                            _ptr(packed), ld, _stream(stream)), "fp8_ep_dispatch_pack_scatter")
+    return packed
+
+
 def fp8_ep_unpack(packed, K, perm, q=None, sA=None, stream=None):
     """Packed rows, reordered by ``perm``: ``q[i], sA[:, i]`` = codes and
     scales of ``packed[perm[i]]``.  Returns ``(q uint8 [M, K], sA [K/128, M])``."""
@@ -557,6 +579,6 @@ __all__ = ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8
            "fp8_quant_act_1x128_gather", "FP8BS_ERR_INDEX",
            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout",
            "fp8bs_selftest_set_wait_limit", "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor",
-           "fp8_quant_per_tensor_delayed", "fp8_gemm_per_tensor", "fp8_quant_act_1x128_scatter", "packed_row_bytes", "fp8_ep_dispatch_pack",
+           "fp8_quant_per_tensor_delayed", "fp8_gemm_per_tensor", "fp8_quant_act_1x128_scatter", "packed_row_bytes", "fp8_ep_dispatch_pack", "fp8_ep_dispatch_pack_scatter",
            "fp8_ep_unpack", "fp8bs_gather_rows", "Fp8bsError", "lib",
            "LIB_PATH", "EXPORTED", "B_KMAJOR", "B_MNMAJOR", "OUT_BF16", "OUT_FP32"]

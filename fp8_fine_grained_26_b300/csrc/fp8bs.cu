@@ -649,7 +649,7 @@ int fp8_quant_act_1x128_scatter(const void *x_bf16, int64_t T, int64_t K, int64_
     const int64_t tasks = T * ((KB + GATHER_TILES - 1) / GATHER_TILES);
     const int64_t blocks = std::min<int64_t>((tasks * 32 + GATHER_THREADS - 1) / GATHER_THREADS,
                                              8 * (int64_t)dev->num_sms);
-    return launch_pdl(quant_act_scatter_kernel, dim3((unsigned)blocks), dim3(GATHER_THREADS), (size_t)0, stream, 1,
+    return launch_pdl(quant_act_scatter_kernel<false>, dim3((unsigned)blocks), dim3(GATHER_THREADS), (size_t)0, stream, 1,
                       static_cast<const uint16_t *>(x_bf16), T, ldx, dest, topk, M, KB, static_cast<uint8_t *>(q_e4m3),
                       ldq, sA);
 }
@@ -678,6 +678,33 @@ int fp8_ep_dispatch_pack(const void *x_bf16, int64_t T, int64_t K, int64_t ldx, 
         static_cast<const uint16_t *>(x_bf16), T, ldx, rows, M, KB, static_cast<uint8_t *>(packed), ld_packed,
         nullptr);
     return launch_status();
+}
+
+int fp8_ep_dispatch_pack_scatter(const void *x_bf16, int64_t T, int64_t K, int64_t ldx, const int32_t *dest, int topk,
+                                 int64_t M, void *packed, int64_t ld_packed, cudaStream_t stream)
+{
+    if (T < 0 || M < 0 || K < 0 || K % 128 != 0)
+        return FP8BS_ERR_SHAPE;
+    if (topk < 1 || topk > SCATTER_MAX_TOPK)
+        return FP8BS_ERR_ARG;
+    if (T == 0 || K == 0)
+        return FP8BS_OK;
+    if (!x_bf16 || !dest || !packed)
+        return FP8BS_ERR_NULL;
+    const int64_t KB = K / 128;
+    if (ldx < K || ld_packed < K + 4 * KB)
+        return FP8BS_ERR_SHAPE;
+    if (!aligned16(x_bf16) || !aligned16(packed) || !aligned4(dest) || (ldx * 2) % 16 != 0 || ld_packed % 16 != 0)
+        return FP8BS_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    const int64_t tasks = T * ((KB + GATHER_TILES - 1) / GATHER_TILES);
+    const int64_t blocks = std::min<int64_t>((tasks * 32 + GATHER_THREADS - 1) / GATHER_THREADS,
+                                             8 * (int64_t)dev->num_sms);
+    return launch_pdl(quant_act_scatter_kernel<true>, dim3((unsigned)blocks), dim3(GATHER_THREADS), (size_t)0, stream, 1,
+                      static_cast<const uint16_t *>(x_bf16), T, ldx, dest, topk, M, KB, static_cast<uint8_t *>(packed),
+                      ld_packed, static_cast<float *>(nullptr));
 }
 
 int fp8_ep_unpack(const void *packed, int64_t n_src, int64_t ld_packed, int64_t K, const int32_t *perm, int64_t M,

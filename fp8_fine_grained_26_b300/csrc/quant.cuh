@@ -726,11 +726,17 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_gather_kernel(
 // word; a row named twice receives one of the tokens (unspecified which).
 constexpr int SCATTER_MAX_TOPK = 32;
 
+// PACKED (expert-parallel dispatch): each destination row holds the row's K
+// codes followed by its KB scales (FP32), as in quant_act_gather_kernel.
+template <bool PACKED = false>
 __global__ void __launch_bounds__(GATHER_THREADS) quant_act_scatter_kernel(
     const uint16_t *__restrict__ x, int64_t T, int64_t ldx, const int32_t *__restrict__ dest, int topk, int64_t M,
     int64_t KB, uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ sA)
 {
-    ptx::grid_dep_launch();
+    // Global memory only after the kernels this one depends on.  (Its grid is
+    // larger than what fits on the GPU at once, so the next kernel is let in
+    // only as blocks finish: launched earlier, its CTAs would take SMs that
+    // this kernel's later blocks still need.)
     ptx::grid_dep_wait();
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4;
@@ -801,12 +807,17 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_scatter_kernel(
                 const int64_t kb = kb0 + 2 * i + half;
                 if (kb < KB) {
                     ptx::st_v2_cs(qrow + kb * 128, codes[i].x, codes[i].y);
-                    if (l16 == 0)
-                        sA[kb * M + row] = scale[i];
+                    if (l16 == 0) {
+                        if constexpr (PACKED)
+                            reinterpret_cast<float *>(q + (int64_t)row * ldq + KB * 128)[kb] = scale[i];
+                        else
+                            sA[kb * M + row] = scale[i];
+                    }
                 }
             }
         }
     }
+    ptx::grid_dep_launch();
 }
 
 // Expert-parallel receive side: rows packed as [K codes | KB FP32 scales]

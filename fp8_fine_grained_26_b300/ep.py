@@ -14,8 +14,9 @@ walkthrough, FP8 section, report figure 10).  One step of a rank:
      grouped by its local experts;
   2. counts exchange: each rank tells every other how many rows it sends to
      each of that rank's experts;
-  3. pack (kernel fp8_ep_dispatch_pack): gather + 1x128 quantisation of the
-     routed rows, each packed with its FP32 scales;
+  3. pack (kernel fp8_ep_dispatch_pack_scatter): 1x128 quantisation of each
+     token row once, its codes packed with its FP32 scales into the send row
+     of every routed copy;
   4. dispatch (all-to-all of the packed FP8 rows);
   5. unpack (kernel fp8_ep_unpack): received rows into expert-major order and
      the GEMM's scale layout;
@@ -43,7 +44,7 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import (fp8_ep_dispatch_pack, fp8_ep_unpack, fp8_grouped_gemm_blockscaled, fp8bs_gather_rows,
+from . import (fp8_ep_dispatch_pack_scatter, fp8_ep_unpack, fp8_grouped_gemm_blockscaled, fp8bs_gather_rows,
                packed_row_bytes)
 
 
@@ -51,9 +52,12 @@ class KernelOps:
     """The data steps of the layer, as the library's CUDA kernels."""
 
     @staticmethod
-    def pack(x, rows, row_bytes):
+    def pack(x, rows, dest, row_bytes):
+        """Send rows: token rows[i] quantised into packed row i; the kernel
+        works from the token side (dest[t, j]: the send row of token t's j-th
+        copy), encoding each token once."""
         packed = torch.empty((rows.numel(), row_bytes), dtype=torch.uint8, device=x.device)
-        return fp8_ep_dispatch_pack(x, rows, packed)
+        return fp8_ep_dispatch_pack_scatter(x, dest, rows.numel(), packed)
 
     @staticmethod
     def unpack(packed, K, perm):
@@ -160,7 +164,11 @@ class FP8ExpertParallel:
         dev = x.device
         plan = plan_send(choice.detach().cpu().numpy(), self.E, self.world)
         rows = torch.from_numpy(plan.tokens.astype(np.int32)).to(dev)
-        packed = self.ops.pack(x, rows, self.row_bytes)
+        n = plan.order.shape[0]
+        send_row = np.empty(n, np.int64)
+        send_row[plan.order] = np.arange(n)                  # (t, k) -> its row in send order
+        dest = torch.from_numpy(send_row.reshape(choice.shape).astype(np.int32)).to(dev)
+        packed = self.ops.pack(x, rows, dest, self.row_bytes)
         return _Step(plan=plan, packed=packed, topk=choice.shape[1], T=x.shape[0],
                      counts_to=plan.expert_counts.reshape(self.world, self.e_local))
 

@@ -224,6 +224,17 @@ int fp8_ep_dispatch_pack(const void *x_bf16, int64_t T, int64_t K, int64_t ldx, 
                          void *packed, int64_t ld_packed, cudaStream_t stream);
 
 /*
+ * The sending side of the expert-parallel dispatch in scatter form: token row
+ * t is quantised once (1x128 tiles) and its codes and scales are packed into
+ * each of its topk send rows dest[t*topk + j], in the fp8_ep_dispatch_pack
+ * layout.  Equal, bit for bit, to fp8_ep_dispatch_pack with rows[dest[t*topk
+ * + j]] = t, with one read and one encoding per token instead of one per
+ * routed copy (fp8_quant_act_1x128_scatter's rules for dest and its errors).
+ */
+int fp8_ep_dispatch_pack_scatter(const void *x_bf16, int64_t T, int64_t K, int64_t ldx, const int32_t *dest, int topk,
+                                 int64_t M, void *packed, int64_t ld_packed, cudaStream_t stream);
+
+/*
  * Expert-parallel dispatch, receiving side: packed rows (fp8_ep_dispatch_pack
  * layout) as they arrive from the all-to-all, grouped by source rank, are
  * reordered into expert-major order for the grouped GEMM: output row i is

@@ -26,7 +26,7 @@ def test_header_declares_the_entry_points():
         "fp8bs_selftest_wait_timeout", "fp8bs_selftest_set_wait_limit",
         "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor", "fp8_quant_per_tensor_delayed",
         "fp8_gemm_per_tensor", "fp8_quant_per_tensor_noalloc", "fp8_ep_dispatch_pack", "fp8_ep_unpack",
-        "fp8bs_gather_rows", "fp8_quant_act_1x128_scatter"])
+        "fp8bs_gather_rows", "fp8_quant_act_1x128_scatter", "fp8_ep_dispatch_pack_scatter"])
 
 
 def test_library_loads_and_exports_every_declared_symbol():

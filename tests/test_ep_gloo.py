@@ -50,7 +50,7 @@ class OracleOps:
     """CPU stand-ins for the four data steps (test infrastructure)."""
 
     @staticmethod
-    def pack(x, rows, row_bytes):
+    def pack(x, rows, dest, row_bytes):
         import oracle
         from synthetic import bf16_bits
         xr = x[rows.long()]

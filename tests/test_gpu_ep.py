@@ -2,7 +2,8 @@
 
 * fp8_ep_dispatch_pack: codes and scales bit-equal to the gather quantiser
   (and so to the oracle's quantisation of the gathered rows), scales packed
-  after the codes of each row.
+  after the codes of each row; fp8_ep_dispatch_pack_scatter (the form the
+  layer uses: each token encoded once) bit-equal to it.
 * fp8_ep_unpack and fp8bs_gather_rows: pure data movement, bit-equal to
   numpy indexing; an out-of-range index gives a zero row and FP8BS_ERR_INDEX.
 * The layer at world size 1 (the exchanges are copies) on the routed-expert
@@ -47,6 +48,22 @@ def test_dispatch_pack_equals_gather_quantiser():
     oq, os_ = oracle.quant_act_1x128(bf16_bits(x[rows.long()]))
     assert np.array_equal(host_u8(packed[:, :K]), oq)
     assert np.array_equal(ps.cpu().numpy().T.copy().view(np.uint32), os_.view(np.uint32))
+
+
+def test_dispatch_pack_scatter_equals_gather_form():
+    g = generator(5, DEV)
+    T, K, topk = 200, 1024, 3
+    x = normal_bf16((T, K), 1.0, g, DEV, outlier_p=0.01, outlier_scale=60.0)
+    M = T * topk
+    send_row = torch.randperm(M, generator=torch.Generator().manual_seed(1)).to(torch.int32)
+    dest = send_row.view(T, topk).to(DEV)
+    rows = torch.empty(M, dtype=torch.int32)
+    rows[send_row.long()] = torch.arange(T, dtype=torch.int32).repeat_interleave(topk)
+    a = fp8.fp8_ep_dispatch_pack_scatter(x, dest, M)
+    b = fp8.fp8_ep_dispatch_pack(x, rows.to(DEV))
+    assert fp8.fp8bs_last_error() == 0
+    KB = K // 128
+    assert torch.equal(a[:, :K + 4 * KB], b[:, :K + 4 * KB])
 
 
 def test_unpack_and_gather_rows_are_exact_data_movement():
