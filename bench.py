@@ -9,15 +9,19 @@ configurations that fit one GPU; A and W are quantised in one launch
 (``--quant split`` runs the two single-operand quantisers concurrently
 instead).  The default run adds, in the same JSON line, one sub-record per
 other configuration (MLA q, MLA kv, routed experts, weight gradient, tiny),
-each timed in its own region, the per-tensor contrast scheme on the dgrad and
-MLA q shapes, and the quantisers-alone table.
+each timed in its own region, the expert-parallel layer's device steps on the
+routed-expert workload, the per-tensor contrast scheme on the dgrad and MLA q
+shapes, and the quantisers-alone table.
 ``--workload`` selects another headline shape (mla_q, mla_kv, wgrad,
-experts, tiny, experts_small) and then measures only that one.  For ``experts`` a step is the dispatch
+experts, experts_ep, tiny, experts_small) and then measures only that one.  For ``experts`` a step is the dispatch
 quantisation (each token row encoded once and its codes written to each of
 its routed rows) plus the grouped GEMM (expert weights
 are quantised once, before timing, as they are once per weight update); for
 ``wgrad`` it is the token-dimension quantisation of dY and X plus the
-weight-gradient GEMM.
+weight-gradient GEMM; ``experts_ep`` runs the device steps of the
+expert-parallel layer at world size 1 on the experts workload (pack, unpack
+into expert order, grouped GEMM, the two row gathers of the return path; the
+all-to-alls move nothing at world size 1).
 
 Printed (rank 0, one JSON line): whole-job GEMM TFLOP/s over the step time,
 per-kernel times from CUDA events on the launching stream, the GEMM's
@@ -164,7 +168,7 @@ def make_workload(name, device):
         return synthetic.dgrad(device=device)
     if name == "tiny":
         return synthetic.tiny(device=device)
-    if name == "experts":
+    if name in ("experts", "experts_ep"):
         return synthetic.experts(device=device, keep_x=True)
     if name == "experts_small":
         return synthetic.experts_small(device=device, keep_x=True)
@@ -490,6 +494,102 @@ class ExpertsStep:
         f.fp8_grouped_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, self.case.offsets, C=outs[0])
 
 
+class ExpertsEPStep:
+    """The device steps of the expert-parallel layer (fp8_fine_grained_26_b300.ep)
+    at world size 1, on the routed-expert workload: pack (each token row
+    quantised once, its codes and scales packed into the send row of every
+    routed copy) -> [all-to-all: at world size 1 the send buffer is the
+    receive buffer] -> unpack into expert order -> grouped GEMM -> row gather
+    back into source order -> [all-to-all] -> row gather into (token, slot)
+    order.  The routing plan (host numpy, once per routing) is made before
+    timing; the weights are quantised once, untimed."""
+
+    def __init__(self, case, fp8, torch):
+        import numpy as np
+        from fp8_fine_grained_26_b300.ep import plan_recv, plan_send
+        self.fp8, self.torch, self.case = fp8, torch, case
+        E, N, K = case.w.shape
+        dev = case.x.device
+        qb, sb = fp8.fp8_quant_w_128x128(case.w.view(E * N, K))
+        self.qb, self.sb = qb.view(E, N, K), sb.view(E, -1, K // 128)
+        case.w = None
+        case.x_sorted = None
+        torch.cuda.empty_cache()
+        self.x = case.x
+        T = self.x.shape[0]
+        # the routing the workload drew: token t's copies, in (expert, token) order
+        tok = case.token_of_row.cpu().numpy()
+        off = case.offsets.cpu().numpy().astype(np.int64)
+        expert_of_row = np.repeat(np.arange(E), np.diff(off))
+        self.topk = tok.shape[0] // T
+        choice = np.empty((T, self.topk), np.int64)
+        fill = np.zeros(T, np.int64)
+        for r in range(tok.shape[0]):
+            choice[tok[r], fill[tok[r]]] = expert_of_row[r]
+            fill[tok[r]] += 1
+        plan = plan_send(choice, E, 1)
+        M = plan.order.shape[0]
+        send_row = np.empty(M, np.int64)
+        send_row[plan.order] = np.arange(M)
+        rp = plan_recv(plan.expert_counts.reshape(1, E))
+        inv = np.empty(M, np.int64)
+        inv[rp.perm] = np.arange(M)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a).astype(np.int32)).to(dev)
+        self.dest, self.perm, self.inv, self.slot = i32(send_row.reshape(T, self.topk)), i32(rp.perm), i32(inv), \
+            i32(send_row)
+        self.offsets = i32(rp.offsets)
+        self.M, self.N, self.K, self.E = M, N, K, E
+        rb = fp8.packed_row_bytes(K)
+        self.packed = torch.empty((M, rb), dtype=torch.uint8, device=dev)
+        self.qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        self.sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.y_src = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.nsets = 1
+        self.flops = 2.0 * M * N * K
+        self.kernels = ["ep_pack", "ep_unpack", "grouped_gemm", "gather_src", "gather_slot"]
+        kb = K // 128
+        self.kernel_bytes = {
+            "ep_pack": T * K * 2 + M * 4 + M * (K + 4 * kb),
+            "ep_unpack": M * 4 + 2 * M * (K + 4 * kb),
+            "grouped_gemm": M * K + E * N * K + (self.sa.numel() + self.sb.numel()) * 4 + M * N * 2,
+            "gather_src": M * 4 + 2 * M * N * 2,
+            "gather_slot": M * 4 + 2 * M * N * 2,
+        }
+        self.h2d_bytes = T * K * 2 + 4 * M * 4
+        self.d2h_bytes = M * N * 2
+        self.launches_per_step = 5
+        self.schedule = ("ep_pack -> [exchange] -> ep_unpack -> grouped_gemm -> gather_src -> [exchange] -> "
+                         "gather_slot (world size 1: the exchanges move nothing)")
+
+    def _steps(self, x, dest, perm, inv, slot, out, events=None):
+        f = self.fp8
+        calls = [
+            lambda: f.fp8_ep_dispatch_pack_scatter(x, dest, self.M, self.packed),
+            lambda: f.fp8_ep_unpack(self.packed, self.K, perm, self.qa, self.sa),
+            lambda: f.fp8_grouped_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, self.offsets, C=self.y),
+            lambda: f.fp8bs_gather_rows(self.y, inv, self.y_src),
+            lambda: f.fp8bs_gather_rows(self.y_src, slot, out),
+        ]
+        for j, call in enumerate(calls):
+            if events: events[2 * j].record()
+            call()
+            if events: events[2 * j + 1].record()
+
+    def run(self, i, events=None):
+        self._steps(self.x, self.dest, self.perm, self.inv, self.slot, self.c, events)
+
+    def host_inputs(self):
+        return [t.cpu().pin_memory() for t in (self.x, self.dest, self.perm, self.inv, self.slot)]
+
+    def out_buffers(self):
+        return [torch_empty_like(self.torch, self.c)]
+
+    def compute(self, dev_in, outs):
+        self._steps(*dev_in, outs[0])
+
+
 def torch_empty_like(torch, t):
     return torch.empty(tuple(t.shape), dtype=t.dtype, device=t.device)
 
@@ -636,7 +736,8 @@ def gemm_traffic(kernel, workload):
 SUSTAINED_MIN_S = 1.0
 
 HEADLINE = "dgrad"                                  # the largest configuration that fits one GPU
-SUBRECORD_WORKLOADS = ("mla_q", "mla_kv", "experts", "wgrad", "tiny", "dgrad_per_tensor", "mla_q_per_tensor")
+SUBRECORD_WORKLOADS = ("mla_q", "mla_kv", "experts", "experts_ep", "wgrad", "tiny", "dgrad_per_tensor",
+                       "mla_q_per_tensor")
 
 
 def choose_peaks(peaks, region_s, clk):
@@ -655,6 +756,8 @@ def choose_peaks(peaks, region_s, clk):
 def build_step(name, case, fp8, torch, args):
     if name.endswith("_per_tensor"):
         return PerTensorStep(case, fp8, torch)
+    if name == "experts_ep":
+        return ExpertsEPStep(case, fp8, torch)
     if name in ("experts", "experts_small"):
         return ExpertsStep(case, fp8, torch)
     if name == "wgrad":
@@ -667,7 +770,7 @@ def measure(args, name, fp8, torch, peaks, peak_src, world, rank, local, device,
     every kernel), end to end from host buffers, rooflines.  Returns the
     record (the JSON line's body for the headline, a sub-record otherwise)."""
     case = make_workload(name, device)
-    if args.e4m3_out and (name in ("experts", "experts_small", "wgrad") or name.endswith("_per_tensor")):
+    if args.e4m3_out and (name in ("experts", "experts_small", "experts_ep", "wgrad") or name.endswith("_per_tensor")):
         raise SystemExit("--e4m3-out applies to the dense forward workloads")
     step = build_step(name, case, fp8, torch, args)
     stream = torch.cuda.current_stream()
@@ -790,7 +893,7 @@ def measure(args, name, fp8, torch, peaks, peak_src, world, rank, local, device,
         import oracle
         if name == "wgrad":
             flops, secs, desc = oracle_sample_wgrad(case)
-        elif name not in ("experts", "experts_small") and not name.endswith("_per_tensor"):
+        elif name not in ("experts", "experts_small", "experts_ep") and not name.endswith("_per_tensor"):
             flops, secs, desc = oracle_sample(name, lambda: dense_host_inputs(case))
         else:
             flops = None
@@ -861,7 +964,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    if args.workload in ("experts", "experts_small", "wgrad"):
+    if args.workload in ("experts", "experts_small", "experts_ep", "wgrad"):
         print(json.dumps({"impl": "reference", "unavailable":
                           "the oracle arm samples the dense forward workloads only"}), flush=True)
         return
@@ -1021,7 +1124,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=["mla_q", "mla_kv", "dgrad", "experts", "tiny", "wgrad", "experts_small",
+                    choices=["mla_q", "mla_kv", "dgrad", "experts", "experts_ep", "tiny", "wgrad", "experts_small",
                              "dgrad_per_tensor", "mla_q_per_tensor", "mla_kv_per_tensor"],
                     help="the headline workload (default: dgrad, the largest configuration)")
     ap.add_argument("--no-subrecords", action="store_true",

@@ -179,3 +179,16 @@ def test_ep_emulated_ranks_equal_world1(experts_world1, world):
     y = _emulate(world, case.x, choice, qw, sw)
     assert fp8.fp8bs_last_error() == 0
     assert torch.equal(y.view(torch.int16), y1.view(torch.int16)), f"world {world}"
+
+
+def test_bench_ep_step_equals_experts_step():
+    """The benchmark's expert-parallel step (world size 1) gives, for routed
+    copy (t, k), the same row as the dispatch + grouped GEMM step gives for
+    that copy's row in (expert, token) order."""
+    import bench
+    s1 = bench.ExpertsStep(synthetic.experts_small(device=DEV, keep_x=True), fp8, torch)
+    s2 = bench.ExpertsEPStep(synthetic.experts_small(device=DEV, keep_x=True), fp8, torch)
+    s1.run(0)
+    s2.run(0)
+    assert fp8.fp8bs_last_error() == 0
+    assert torch.equal(s2.c.view(torch.int16), s1.c[s2.slot.long()].view(torch.int16))
