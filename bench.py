@@ -494,6 +494,36 @@ class ExpertsStep:
         f.fp8_grouped_gemm_blockscaled(self.qa, self.sa, self.qb, self.sb, self.case.offsets, C=outs[0])
 
 
+def ep_world1_plan(token_of_row, offsets, tokens):
+    """The expert-parallel layer's routing plan at world size 1 for a routing
+    given as rows sorted by (expert, token) (token_of_row, expert offsets):
+    dest[t, k] = send row of token t's k-th copy, perm = received row of each
+    expert-major row, inv = its inverse, slot[t*topk + k] = send row of copy
+    (t, k), and the expert offsets.  Host numpy, through the layer's own
+    planning functions."""
+    import numpy as np
+    from fp8_fine_grained_26_b300.ep import plan_recv, plan_send
+    tok = np.asarray(token_of_row, np.int64)
+    off = np.asarray(offsets, np.int64)
+    E = off.shape[0] - 1
+    topk = tok.shape[0] // tokens
+    expert_of_row = np.repeat(np.arange(E), np.diff(off))
+    choice = np.empty((tokens, topk), np.int64)
+    fill = np.zeros(tokens, np.int64)
+    for r in range(tok.shape[0]):                        # experts ascend within each token's copies
+        choice[tok[r], fill[tok[r]]] = expert_of_row[r]
+        fill[tok[r]] += 1
+    plan = plan_send(choice, E, 1)
+    M = plan.order.shape[0]
+    send_row = np.empty(M, np.int64)
+    send_row[plan.order] = np.arange(M)
+    rp = plan_recv(plan.expert_counts.reshape(1, E))
+    inv = np.empty(M, np.int64)
+    inv[rp.perm] = np.arange(M)
+    return {"topk": topk, "dest": send_row.reshape(tokens, topk), "perm": rp.perm, "inv": inv, "slot": send_row,
+            "offsets": rp.offsets, "choice": choice}
+
+
 class ExpertsEPStep:
     """The device steps of the expert-parallel layer (fp8_fine_grained_26_b300.ep)
     at world size 1, on the routed-expert workload: pack (each token row
@@ -506,7 +536,6 @@ class ExpertsEPStep:
 
     def __init__(self, case, fp8, torch):
         import numpy as np
-        from fp8_fine_grained_26_b300.ep import plan_recv, plan_send
         self.fp8, self.torch, self.case = fp8, torch, case
         E, N, K = case.w.shape
         dev = case.x.device
@@ -517,27 +546,13 @@ class ExpertsEPStep:
         torch.cuda.empty_cache()
         self.x = case.x
         T = self.x.shape[0]
-        # the routing the workload drew: token t's copies, in (expert, token) order
-        tok = case.token_of_row.cpu().numpy()
-        off = case.offsets.cpu().numpy().astype(np.int64)
-        expert_of_row = np.repeat(np.arange(E), np.diff(off))
-        self.topk = tok.shape[0] // T
-        choice = np.empty((T, self.topk), np.int64)
-        fill = np.zeros(T, np.int64)
-        for r in range(tok.shape[0]):
-            choice[tok[r], fill[tok[r]]] = expert_of_row[r]
-            fill[tok[r]] += 1
-        plan = plan_send(choice, E, 1)
-        M = plan.order.shape[0]
-        send_row = np.empty(M, np.int64)
-        send_row[plan.order] = np.arange(M)
-        rp = plan_recv(plan.expert_counts.reshape(1, E))
-        inv = np.empty(M, np.int64)
-        inv[rp.perm] = np.arange(M)
+        plan = ep_world1_plan(case.token_of_row.cpu().numpy(), case.offsets.cpu().numpy(), T)
+        self.topk = plan["topk"]
+        M = plan["slot"].shape[0]
         i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a).astype(np.int32)).to(dev)
-        self.dest, self.perm, self.inv, self.slot = i32(send_row.reshape(T, self.topk)), i32(rp.perm), i32(inv), \
-            i32(send_row)
-        self.offsets = i32(rp.offsets)
+        self.dest, self.perm, self.inv, self.slot = (i32(plan["dest"]), i32(plan["perm"]), i32(plan["inv"]),
+                                                     i32(plan["slot"]))
+        self.offsets = i32(plan["offsets"])
         self.M, self.N, self.K, self.E = M, N, K, E
         rb = fp8.packed_row_bytes(K)
         self.packed = torch.empty((M, rb), dtype=torch.uint8, device=dev)

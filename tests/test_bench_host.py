@@ -86,3 +86,32 @@ def test_default_headline_is_the_largest_configuration():
     # the expert GEMM has the most FLOPs but is HBM-bound on weights; of the
     # dense GEMMs dgrad is the largest
     assert max((v, k) for k, v in flops.items() if k != "experts")[1] == bench.HEADLINE
+
+
+def test_ep_world1_plan_maps_every_routed_copy_to_its_row():
+    """The expert-parallel bench step's routing plan, on a small synthetic
+    routing: copy (t, k) goes to a row of token t under expert choice[t, k],
+    every row is used once, and at world size 1 the receive permutation is
+    the identity and the expert offsets are the routing's own."""
+    import numpy as np
+    import torch
+    import synthetic
+    g = synthetic.generator(2, "cpu")
+    T, E, topk = 64, 16, 4
+    logits = torch.randn((T, E), generator=g)
+    bias = torch.rand((E,), generator=g) * 0.2 - 0.1
+    choice = synthetic.route_topk(logits, bias, topk)
+    token_of_row, offsets = synthetic.segments_from_choice(choice, E)
+    tok, off = token_of_row.numpy(), offsets.numpy()
+    plan = bench.ep_world1_plan(tok, off, T)
+    M = T * topk
+    slot = plan["slot"]
+    assert plan["topk"] == topk
+    assert np.array_equal(np.sort(slot), np.arange(M))
+    assert np.array_equal(plan["dest"].reshape(-1), slot)
+    assert np.array_equal(plan["perm"], np.arange(M)) and np.array_equal(plan["inv"], np.arange(M))
+    assert np.array_equal(plan["offsets"], off)
+    expert_of_row = np.repeat(np.arange(E), np.diff(off))
+    assert np.array_equal(tok[slot], np.repeat(np.arange(T), topk))
+    assert np.array_equal(expert_of_row[slot].reshape(T, topk), plan["choice"])
+    assert np.array_equal(np.sort(choice.numpy(), axis=1), plan["choice"])
