@@ -830,6 +830,29 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_scatter_kernel(
 constexpr int UNPACK_THREADS = 256;
 constexpr int UNPACK_ROWS = 32;
 constexpr int UNPACK_KB_CHUNK = 64;
+constexpr int COPY_UNROLL = 8;          // 16-byte loads in flight per lane in a row copy
+
+// One warp copies `chunks` 16-byte chunks of a row (zeros when !ok): each
+// lane issues COPY_UNROLL loads before their stores, so a row is not a chain
+// of dependent load -> store round trips.
+__device__ __forceinline__ void warp_copy_row16(uint8_t *__restrict__ dst, const uint8_t *__restrict__ src,
+                                                int64_t chunks, bool ok, int lane)
+{
+    int64_t c = lane;
+    for (; c + 32 * (COPY_UNROLL - 1) < chunks; c += 32 * COPY_UNROLL) {
+        uint4 v[COPY_UNROLL];
+#pragma unroll
+        for (int u = 0; u < COPY_UNROLL; ++u)
+            v[u] = ok ? ptx::ld_nc_v4(src + (c + 32 * u) * 16) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < COPY_UNROLL; ++u)
+            ptx::st_v4(dst + (c + 32 * u) * 16, v[u].x, v[u].y, v[u].z, v[u].w);
+    }
+    for (; c < chunks; c += 32) {
+        const uint4 v = ok ? ptx::ld_nc_v4(src + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+        ptx::st_v4(dst + c * 16, v.x, v.y, v.z, v.w);
+    }
+}
 
 __global__ void __launch_bounds__(UNPACK_THREADS) ep_unpack_kernel(
     const uint8_t *__restrict__ packed, int64_t ld_packed, int64_t n_src, int64_t KB, const int32_t *__restrict__ perm,
@@ -858,13 +881,7 @@ __global__ void __launch_bounds__(UNPACK_THREADS) ep_unpack_kernel(
         if (i >= M)
             break;
         const int64_t s = src_row[r];
-        uint8_t *dst = q + i * ldq;
-        for (int64_t c = lane; c < chunks; c += 32) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (s >= 0)
-                v = *reinterpret_cast<const uint4 *>(packed + s * ld_packed + c * 16);
-            ptx::st_v4(dst + c * 16, v.x, v.y, v.z, v.w);
-        }
+        warp_copy_row16(q + i * ldq, packed + (s >= 0 ? s : 0) * ld_packed, chunks, s >= 0, lane);
     }
     for (int64_t kb0 = 0; kb0 < KB; kb0 += UNPACK_KB_CHUNK) {
         const int nkb = (int)min((int64_t)UNPACK_KB_CHUNK, KB - kb0);
@@ -899,14 +916,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t *__restr
         const bool ok = p >= 0 && (int64_t)p < n_src;
         if (!ok && lane == 0)
             atomicOr(&g_error_word, 2u);
-        const uint8_t *s = src + (ok ? (int64_t)p : 0) * ld_src;
-        uint8_t *d = dst + i * ld_dst;
-        for (int64_t c = lane; c < chunks; c += 32) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (ok)
-                v = *reinterpret_cast<const uint4 *>(s + c * 16);
-            ptx::st_v4(d + c * 16, v.x, v.y, v.z, v.w);
-        }
+        warp_copy_row16(dst + i * ld_dst, src + (ok ? (int64_t)p : 0) * ld_src, chunks, ok, lane);
     }
 }
 
