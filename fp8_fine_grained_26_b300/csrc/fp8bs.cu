@@ -725,9 +725,7 @@ int fp8_ep_unpack(const void *packed, int64_t n_src, int64_t ld_packed, int64_t 
     DeviceInfo *dev = nullptr;
     if (int st = current_device(&dev))
         return st;
-    const int64_t blocks = (M + UNPACK_ROWS - 1) / UNPACK_ROWS;
-    if (blocks > INT32_MAX)
-        return FP8BS_ERR_SHAPE;
+    const int64_t blocks = std::min<int64_t>((M + UNPACK_ROWS - 1) / UNPACK_ROWS, 4 * (int64_t)dev->num_sms);
     ep_unpack_kernel<<<(unsigned)blocks, UNPACK_THREADS, 0, stream>>>(
         static_cast<const uint8_t *>(packed), ld_packed, n_src, KB, perm, M, static_cast<uint8_t *>(q_e4m3), ldq, sA);
     return launch_status();

@@ -823,9 +823,9 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_scatter_kernel(
 // Expert-parallel receive side: rows packed as [K codes | KB FP32 scales]
 // arrive grouped by source rank; output row i is packed row perm[i], its
 // codes into q[i] and its scales into the grouped GEMM's column layout
-// sA[kb][i].  A block takes 32 output rows: its warps copy the codes (16-byte
-// loads and stores), then the 32 x KB scales go through shared memory so
-// that each sA run of 32 rows is one 128-byte store.  An index outside
+// sA[kb][i].  Blocks take runs of 32 output rows in turn: a block's warps copy
+// the run's codes (16-byte loads and stores), then its 32 x KB scales go
+// through shared memory so that each sA run of 32 rows is one 128-byte store.  An index outside
 // [0, n_src) gives zero codes and scales and sets bit 1 of the error word.
 constexpr int UNPACK_THREADS = 256;
 constexpr int UNPACK_ROWS = 32;
@@ -861,41 +861,48 @@ __global__ void __launch_bounds__(UNPACK_THREADS) ep_unpack_kernel(
     __shared__ float tile[UNPACK_KB_CHUNK][UNPACK_ROWS + 1];
     __shared__ int64_t src_row[UNPACK_ROWS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t i0 = (int64_t)blockIdx.x * UNPACK_ROWS;
-    if (threadIdx.x < UNPACK_ROWS) {
-        const int64_t i = i0 + threadIdx.x;
-        int64_t s = -1;
-        if (i < M) {
-            const int32_t p = perm[i];
-            if (p >= 0 && (int64_t)p < n_src)
-                s = p;
-            else
-                atomicOr(&g_error_word, 2u);
-        }
-        src_row[threadIdx.x] = s;
-    }
-    __syncthreads();
+    const int64_t nblk = (M + UNPACK_ROWS - 1) / UNPACK_ROWS;
     const int64_t chunks = KB * 8;                                   // 16-byte chunks of codes per row
-    for (int r = warp; r < UNPACK_ROWS; r += UNPACK_THREADS / 32) {
-        const int64_t i = i0 + r;
-        if (i >= M)
-            break;
-        const int64_t s = src_row[r];
-        warp_copy_row16(q + i * ldq, packed + (s >= 0 ? s : 0) * ld_packed, chunks, s >= 0, lane);
-    }
-    for (int64_t kb0 = 0; kb0 < KB; kb0 += UNPACK_KB_CHUNK) {
-        const int nkb = (int)min((int64_t)UNPACK_KB_CHUNK, KB - kb0);
-        __syncthreads();
-        for (int e = threadIdx.x; e < UNPACK_ROWS * nkb; e += UNPACK_THREADS) {
-            const int r = e / nkb, kb = e - r * nkb;
-            const int64_t s = src_row[r];
-            tile[kb][r] = s >= 0 ? reinterpret_cast<const float *>(packed + s * ld_packed + KB * 128)[kb0 + kb] : 0.0f;
+    // persistent: block b takes row blocks b, b + gridDim.x, ... so that the
+    // blocks of an SM are at different phases (code copy, scale transpose)
+    for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+        const int64_t i0 = blk * UNPACK_ROWS;
+        __syncthreads();                                             // the previous block's rows are done
+        if (threadIdx.x < UNPACK_ROWS) {
+            const int64_t i = i0 + threadIdx.x;
+            int64_t s = -1;
+            if (i < M) {
+                const int32_t p = perm[i];
+                if (p >= 0 && (int64_t)p < n_src)
+                    s = p;
+                else
+                    atomicOr(&g_error_word, 2u);
+            }
+            src_row[threadIdx.x] = s;
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < UNPACK_ROWS * nkb; e += UNPACK_THREADS) {
-            const int kb = e / UNPACK_ROWS, r = e - kb * UNPACK_ROWS;
-            if (i0 + r < M)
-                sA[(kb0 + kb) * M + i0 + r] = tile[kb][r];
+        for (int r = warp; r < UNPACK_ROWS; r += UNPACK_THREADS / 32) {
+            const int64_t i = i0 + r;
+            if (i >= M)
+                break;
+            const int64_t s = src_row[r];
+            warp_copy_row16(q + i * ldq, packed + (s >= 0 ? s : 0) * ld_packed, chunks, s >= 0, lane);
+        }
+        for (int64_t kb0 = 0; kb0 < KB; kb0 += UNPACK_KB_CHUNK) {
+            const int nkb = (int)min((int64_t)UNPACK_KB_CHUNK, KB - kb0);
+            __syncthreads();
+            for (int e = threadIdx.x; e < UNPACK_ROWS * nkb; e += UNPACK_THREADS) {
+                const int r = e / nkb, kb = e - r * nkb;
+                const int64_t s = src_row[r];
+                tile[kb][r] = s >= 0 ? reinterpret_cast<const float *>(packed + s * ld_packed + KB * 128)[kb0 + kb]
+                                     : 0.0f;
+            }
+            __syncthreads();
+            for (int e = threadIdx.x; e < UNPACK_ROWS * nkb; e += UNPACK_THREADS) {
+                const int kb = e / UNPACK_ROWS, r = e - kb * UNPACK_ROWS;
+                if (i0 + r < M)
+                    sA[(kb0 + kb) * M + i0 + r] = tile[kb][r];
+            }
         }
     }
 }
