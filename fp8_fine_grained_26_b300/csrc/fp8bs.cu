@@ -254,6 +254,20 @@ bool encode_bf16_units(CUtensorMap *m, const void *base, uint64_t cols, uint64_t
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Activation units: two 64 x 128 boxes per unit with the 128-byte swizzle
+// (the activation quantiser's conflict-free shared-memory reads).
+bool encode_bf16_units_sw128(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld)
+{
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {ld * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int c_vector_ok(const void *C, int c_dtype, int64_t ldc)
 {
     const int64_t es = c_dtype == FP8BS_OUT_FP32 ? 4 : 2;
@@ -447,7 +461,7 @@ int fp8_quant_act_1x128(const void *x_bf16, int64_t M, int64_t K, int64_t ldx, v
     if (int st = current_device(&dev))
         return st;
     CUtensorMap tmX;
-    if (!encode_bf16_units(&tmX, x_bf16, (uint64_t)K, (uint64_t)M, (uint64_t)ldx))
+    if (!encode_bf16_units_sw128(&tmX, x_bf16, (uint64_t)K, (uint64_t)M, (uint64_t)ldx))
         return FP8BS_ERR_ARG;
     const int64_t units = ((M + 127) / 128) * (K / 128);
     const int grid = (int)std::min<int64_t>(units, 3 * (int64_t)dev->num_sms);
@@ -519,7 +533,7 @@ int fp8_quant_act_w(const void *x_bf16, int64_t M, int64_t K, int64_t ldx, void 
     CUtensorMap tmX, tmW;
     QuantPairArgs a = {};
     if (ca == 0) {
-        if (!encode_bf16_units(&tmX, x_bf16, (uint64_t)K, (uint64_t)M, (uint64_t)ldx))
+        if (!encode_bf16_units_sw128(&tmX, x_bf16, (uint64_t)K, (uint64_t)M, (uint64_t)ldx))
             return FP8BS_ERR_ARG;
         a.M = M;
         a.KB = K / 128;

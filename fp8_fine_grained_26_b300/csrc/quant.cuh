@@ -4,19 +4,17 @@
 // tile, weights per 128x128 block.]
 //
 // Both kernels are HBM-bound streams: 2 bytes read + 1 byte written per
-// element plus 4 bytes per scale.  They are persistent (two 256-thread CTAs
+// element plus 4 bytes per scale.  They are persistent (three 256-thread CTAs
 // per SM) and stream 128 x 128 BF16 units (32 KiB: 128 rows of one 128-column
 // K-block) through a QSTAGES-deep ring of TMA loads in shared memory, so each
 // SM keeps several units in flight while it encodes another.  A unit is one
 // 128x128 weight block, or 128 activation rows x one 1x128 tile column.
-// A 1x128 tile is one 256-byte row segment handled by a half-warp (16 bytes
-// per lane); its amax is an integer max over the BF16 magnitude bits
-// (monotone for finite values) reduced with four xor-shuffles; a weight
-// block's amax adds a warp and a CTA reduction.  scale = amax / 448 is one
-// IEEE division; x / scale is formed exactly (see Divisor below) and encoded
-// with the hardware RNE-satfinite E4M3 conversion; codes are stored 8 bytes
-// per lane (128 contiguous bytes per half-warp), scales of a unit's 128 rows
-// are staged in shared memory and stored as one coalesced 512-byte run.
+// An amax is an integer max over the BF16 magnitude bits (monotone for
+// finite values): a 1x128 tile's over the four lanes that hold it (two
+// xor-shuffles), a weight block's over its warps and the CTA.  scale =
+// amax / 448 is one IEEE division; x / scale is formed exactly (see Divisor
+// below) and encoded with the hardware RNE-satfinite E4M3 conversion; codes
+// are stored 8 bytes per lane in runs of 32 or 128 contiguous bytes.
 #pragma once
 #include "common.cuh"
 
@@ -175,6 +173,27 @@ __device__ __forceinline__ void qissue(const QRing &r, const CUtensorMap *tm, in
     ptx::tma_load_2d(r.stage(s), tm, r.full(s), (int32_t)(cb * 128), (int32_t)(rb * 128));
 }
 
+// An activation unit is staged as two 64-column boxes with the 128-byte
+// swizzle (16-byte chunk c of row r of a half at r * 128 + ((c ^ (r & 7)) * 16)),
+// so that the four lanes reading one row and the eight rows a warp reads at
+// once fall on different banks.
+__device__ __forceinline__ void qissue_act_at(const QRing &r, const CUtensorMap *tm, int64_t j, int64_t rb,
+                                              int64_t cb)
+{
+    const int s = (int)(j % QSTAGES);
+    ptx::fence_proxy_async_smem();             // earlier generic reads of the stage come first
+    ptx::mbar_arrive_expect_tx(r.full(s), QUNIT_BYTES);
+    ptx::tma_load_2d(r.stage(s), tm, r.full(s), (int32_t)(cb * 128), (int32_t)(rb * 128));
+    ptx::tma_load_2d(r.stage(s) + QUNIT_BYTES / 2, tm, r.full(s), (int32_t)(cb * 128 + 64), (int32_t)(rb * 128));
+}
+
+__device__ __forceinline__ void qissue_act(const QRing &r, const CUtensorMap *tm, int64_t j, int64_t cols_blocks)
+{
+    int64_t rb, cb;
+    qunit(j, cols_blocks, rb, cb);
+    qissue_act_at(r, tm, j, rb, cb);
+}
+
 // Waits for unit j's stage; every thread of the CTA agrees on the outcome.
 __device__ __forceinline__ bool qwait(const QRing &r, int64_t j)
 {
@@ -193,67 +212,58 @@ __device__ __forceinline__ void qdrain(const QRing &r, int64_t consumed, int64_t
             wait_drain(r.full((int)(j % QSTAGES)), (uint32_t)((j / QSTAGES) & 1));
 }
 
-// Activation quantiser.  Unit (mb, kb): rows [128 mb, +128) of tile column kb.
-// Warp w owns rows [16 w, 16 w + 16); at step i its two half-warps take rows
-// 16 w + 2 i and 16 w + 2 i + 1 (512 contiguous bytes of the staged unit).
-// The eight row divisors of a half-warp are formed by eight different lanes,
-// which also store the rows' scales (the warp's 16 rows are one 64-byte run),
-// and broadcast with shuffles.  `issue_next` runs once the staged unit has
-// been read (the stage is free again) and queues the CTA's next copy.
+// Activation quantiser.  Unit (mb, kb): rows [128 mb, +128) of tile column kb,
+// staged swizzled (qissue_act).  A 1x128 tile is held by four adjacent lanes:
+// lane quarter g (lane & 3) takes the 8-column chunks g, g + 4, g + 8, g + 12
+// of the row, so the four lanes' codes of each step form one 32-byte run.
+// Warp w owns rows [16 w, 16 w + 16), eight at a time (lane >> 2 within the
+// eight).  The row's amax takes two xor-shuffles within the four lanes; each
+// of them forms the row's divisor itself, and lane quarter 0 stores the
+// scale (eight consecutive rows: one 32-byte run).  `issue_next` runs once
+// the staged unit has been read (the stage is free again) and queues the
+// CTA's next copy.
 template <class Next>
 __device__ __forceinline__ void act_unit(const QRing &r, int64_t j, int64_t mb, int64_t kb, int64_t M,
                                          uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ sA,
                                          Next &&issue_next)
 {
     const int tid = threadIdx.x;
-    const int lane16 = tid & 15;
-    const int hw = tid >> 4;
+    const int lane = tid & 31;
+    const int g = lane & 3;
+    const int rsub = lane >> 2;
     const uint32_t st = r.stage((int)(j % QSTAGES));
-    uint4 v[8];
+    uint4 v[2][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = 2 * i + (hw & 1) + 16 * (hw >> 1);
-        const uint32_t a = st + (uint32_t)(row * 256 + lane16 * 16);
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w) : "r"(a));
+    for (int p = 0; p < 2; ++p) {
+        const int row = 16 * (tid >> 5) + 8 * p + rsub;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int chunk = g + 4 * c;                                  // 16-byte chunk of the 256-byte row
+            const uint32_t a = st + (uint32_t)((chunk >> 3) * (QUNIT_BYTES / 2) + row * 128 +
+                                               (((chunk & 7) ^ (row & 7)) << 4));
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v[p][c].x), "=r"(v[p][c].y), "=r"(v[p][c].z), "=r"(v[p][c].w) : "r"(a));
+        }
     }
     __syncthreads();                                   // the stage is free again
     issue_next();
-    // amax of each of this half-warp's 8 rows, known to all its 16 lanes
-    uint32_t am[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t a = absmax_bits8(v[i]);
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1)
-            a = max(a, __shfl_xor_sync(0xffffffffu, a, o, 16));
-        am[i] = a;
-    }
-    // lane i of the half-warp forms row i's divisor once; the others fetch it
-    uint32_t mine_a = am[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i)
-        mine_a = (lane16 & 7) == i ? am[i] : mine_a;
-    const Divisor dm = make_divisor(mine_a);
-    // lane i < 8 of the half-warp holds row 2 i + half's scale: the warp's 16
-    // consecutive rows, one 64-byte store
-    if (lane16 < 8) {
-        const int64_t gm = mb * 128 + 2 * lane16 + (hw & 1) + 16 * (hw >> 1);
-        if (gm < M)
-            sA[kb * M + gm] = dm.s;
-    }
-    const int half_base = (tid & 16);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        Divisor d;
-        d.s = __shfl_sync(0xffffffffu, dm.s, half_base + i);
-        d.r = __shfl_sync(0xffffffffu, dm.r, half_base + i);
-        d.mode = divisor_mode(am[i]);
-        const int row = 2 * i + (hw & 1) + 16 * (hw >> 1);
-        const int64_t gm = mb * 128 + row;
+    for (int p = 0; p < 2; ++p) {
+        uint32_t a = max(max(absmax_bits8(v[p][0]), absmax_bits8(v[p][1])),
+                         max(absmax_bits8(v[p][2]), absmax_bits8(v[p][3])));
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        const Divisor d = make_divisor(a);
+        const int64_t gm = mb * 128 + 16 * (tid >> 5) + 8 * p + rsub;
         if (gm < M) {
-            const uint2 c = quant_8(v[i], d);
-            ptx::st_v2(q + gm * ldq + kb * 128 + lane16 * 8, c.x, c.y);
+            if (g == 0)
+                sA[kb * M + gm] = d.s;
+            uint8_t *qrow = q + gm * ldq + kb * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint2 codes = quant_8(v[p][c], d);
+                ptx::st_v2(qrow + (g + 4 * c) * 8, codes.x, codes.y);
+            }
         }
     }
 }
@@ -317,7 +327,7 @@ __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_act_1x128_kernel(
     int64_t issued = 0;
     if (tid == 0)
         for (; issued < mine && issued < QSTAGES; ++issued)
-            qissue(r, &tmX, issued, KB);
+            qissue_act(r, &tmX, issued, KB);
     int64_t j = 0;
     for (; j < mine; ++j) {
         if (!qwait(r, j))
@@ -326,7 +336,7 @@ __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_act_1x128_kernel(
         qunit(j, KB, mb, kb);
         act_unit(r, j, mb, kb, M, q, ldq, sA, [&] {
             if (tid == 0 && issued < mine && issued < j + 1 + QSTAGES) {
-                qissue(r, &tmX, issued, KB);
+                qissue_act(r, &tmX, issued, KB);
                 ++issued;
             }
         });
@@ -385,16 +395,14 @@ __device__ __forceinline__ void qissue_pair(const QRing &r, const CUtensorMap *t
 {
     const int64_t u = (int64_t)blockIdx.x + j * gridDim.x;
     int64_t rb, cb;
-    const CUtensorMap *tm;
     if (u < a.units_a) {
         rb = u / a.KB;
-        cb = u - rb * a.KB;
-        tm = tmX;
-    } else {
-        rb = (u - a.units_a) / a.CB;
-        cb = (u - a.units_a) - rb * a.CB;
-        tm = tmW;
+        qissue_act_at(r, tmX, j, rb, u - rb * a.KB);
+        return;
     }
+    rb = (u - a.units_a) / a.CB;
+    cb = (u - a.units_a) - rb * a.CB;
+    const CUtensorMap *tm = tmW;
     const int s = (int)(j % QSTAGES);
     ptx::fence_proxy_async_smem();             // earlier generic reads of the stage come first
     ptx::mbar_arrive_expect_tx(r.full(s), QUNIT_BYTES);
