@@ -630,8 +630,11 @@ __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_fixed_kernel(
 // matrix, without materialising it.  The rows are arbitrary, so the loads
 // are plain read-only 16-byte loads, kept in L2 (each token row is read once
 // per routed copy); the codes are streamed out.  A warp takes one output row
-// and eight consecutive 1x128 tiles, four per half-warp; every lane issues
-// its four loads before any use.  An index outside [0, T) is not read: the
+// and eight consecutive 1x128 tiles, four adjacent lanes per tile (lane
+// quarter g loads the tile's 16-byte chunks g, g + 4, g + 8, g + 12, all four
+// before any use, and stores their codes: each step of the four lanes is one
+// 32-byte run); a tile's amax takes two xor-shuffles and every lane forms its
+// tile's divisor.  An index outside [0, T) is not read: the
 // row encodes as zeros with a zero scale and bit 1 of the error word is set.
 // (A version staging 16-row units through bulk copies into a shared-memory
 // ring measured slower.)
@@ -647,9 +650,8 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_gather_kernel(
     int64_t KB, uint8_t *__restrict__ q, int64_t ldq, float *__restrict__ sA)
 {
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4;
-    const int l16 = lane & 15;
-    const int hbase = lane & 16;
+    const int tt = lane >> 2;                                     // tile of the task
+    const int g = lane & 3;                                       // lane quarter of the tile
     const uint64_t keep = ptx::policy_evict_last();
     const int64_t chunks = (KB + GATHER_TILES - 1) / GATHER_TILES;
     const int64_t warp0 = ((int64_t)blockIdx.x * GATHER_THREADS + threadIdx.x) >> 5;
@@ -664,60 +666,37 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_gather_kernel(
             if (++i >= M)
                 break;
         }
-        const int64_t kb0 = chunk * GATHER_TILES;
+        const int64_t kb = chunk * GATHER_TILES + tt;
         const int32_t src = rows[i];
         const bool valid = src >= 0 && (int64_t)src < T;
         if (!valid && lane == 0)
             atomicOr(&g_error_word, 2u);
-        constexpr int TPH = GATHER_TILES / 2;                     // tiles per half-warp
-        uint4 v[TPH];
+        uint4 v[4];
 #pragma unroll
-        for (int t = 0; t < TPH; ++t) {
-            const int64_t kb = kb0 + 2 * t + half;
-            v[t] = make_uint4(0u, 0u, 0u, 0u);
+        for (int c = 0; c < 4; ++c) {
+            v[c] = make_uint4(0u, 0u, 0u, 0u);
             if (valid && kb < KB)
-                v[t] = ptx::ld_nc_v4_hint(x + (int64_t)src * ldx + kb * 128 + l16 * 8, keep);
+                v[c] = ptx::ld_nc_v4_hint(x + (int64_t)src * ldx + kb * 128 + (g + 4 * c) * 8, keep);
         }
-        // amax of each of the half-warp's tiles, known to all its 16 lanes
-        uint32_t am[TPH];
-#pragma unroll
-        for (int t = 0; t < TPH; ++t) {
-            uint32_t a = absmax_bits8(v[t]);
-#pragma unroll
-            for (int o = 8; o >= 1; o >>= 1)
-                a = max(a, __shfl_xor_sync(0xffffffffu, a, o, 16));
-            am[t] = a;
-        }
-        // lane t of the half-warp forms tile t's divisor; the others fetch it
-        uint32_t mine = am[0];
-#pragma unroll
-        for (int t = 1; t < TPH; ++t)
-            mine = (l16 & (TPH - 1)) == t ? am[t] : mine;
-        const Divisor dm = make_divisor(mine);
+        uint32_t a = max(max(absmax_bits8(v[0]), absmax_bits8(v[1])), max(absmax_bits8(v[2]), absmax_bits8(v[3])));
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        const Divisor d = make_divisor(a);
         // the usual case, every tile of the task on the reciprocal path,
         // encodes without a per-tile branch
-        bool recip = true;
+        const bool recip = __all_sync(0xffffffffu, d.mode == 2);
+        if (kb < KB) {
+            uint8_t *qrow = q + i * ldq + kb * 128;
 #pragma unroll
-        for (int t = 0; t < TPH; ++t)
-            recip = recip && divisor_mode(am[t]) == 2;
-        recip = __all_sync(0xffffffffu, recip);
-        uint8_t *qrow = q + i * ldq + l16 * 8;
-#pragma unroll
-        for (int t = 0; t < TPH; ++t) {
-            const int64_t kb = kb0 + 2 * t + half;
-            Divisor d;
-            d.s = __shfl_sync(0xffffffffu, dm.s, hbase + t);
-            d.r = __shfl_sync(0xffffffffu, dm.r, hbase + t);
-            d.mode = divisor_mode(am[t]);
-            if (kb < KB) {
-                const uint2 c = recip ? quant_8_recip(v[t], d) : quant_8(v[t], d);
-                ptx::st_v2_cs(qrow + kb * 128, c.x, c.y);
-                if (l16 == 0) {
-                    if constexpr (PACKED)
-                        reinterpret_cast<float *>(q + i * ldq + KB * 128)[kb] = d.s;
-                    else
-                        sA[kb * M + i] = d.s;
-                }
+            for (int c = 0; c < 4; ++c) {
+                const uint2 codes = recip ? quant_8_recip(v[c], d) : quant_8(v[c], d);
+                ptx::st_v2_cs(qrow + (g + 4 * c) * 8, codes.x, codes.y);
+            }
+            if (g == 0) {
+                if constexpr (PACKED)
+                    reinterpret_cast<float *>(q + i * ldq + KB * 128)[kb] = d.s;
+                else
+                    sA[kb * M + i] = d.s;
             }
         }
     }
@@ -728,9 +707,9 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_gather_kernel(
 // are stored to each of its topk destination rows dest[t * topk + j].  The
 // result is the gather form's (quantising before or after the copy gives the
 // same bytes), with a topk-th of the loads and of the encoding work.  A warp
-// task is one token row x GATHER_TILES consecutive 1x128 tiles, as in the
-// gather kernel; lane j < topk fetches destination j and the warp broadcasts
-// it.  A destination outside [0, M) is skipped and sets bit 1 of the error
+// task is one token row x GATHER_TILES consecutive 1x128 tiles, four lanes
+// per tile as in the gather kernel; lane j < topk fetches destination j and
+// the warp broadcasts it.  A destination outside [0, M) is skipped and sets bit 1 of the error
 // word; a row named twice receives one of the tokens (unspecified which).
 constexpr int SCATTER_MAX_TOPK = 32;
 
@@ -747,9 +726,8 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_scatter_kernel(
     // this kernel's later blocks still need.)
     ptx::grid_dep_wait();
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4;
-    const int l16 = lane & 15;
-    const int hbase = lane & 16;
+    const int tt = lane >> 2;                                     // tile of the task
+    const int g = lane & 3;                                       // lane quarter of the tile
     const int64_t chunks = (KB + GATHER_TILES - 1) / GATHER_TILES;
     const int64_t warp0 = ((int64_t)blockIdx.x * GATHER_THREADS + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * GATHER_THREADS) >> 5;
@@ -761,7 +739,7 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_scatter_kernel(
             if (++t >= T)
                 break;
         }
-        const int64_t kb0 = chunk * GATHER_TILES;
+        const int64_t kb = chunk * GATHER_TILES + tt;
         int32_t my_dst = -1;
         if (lane < topk) {
             my_dst = dest[t * topk + lane];
@@ -771,57 +749,34 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_scatter_kernel(
                 my_dst = -1;
             }
         }
-        constexpr int TPH = GATHER_TILES / 2;                     // tiles per half-warp
-        uint4 v[TPH];
+        uint4 v[4];
 #pragma unroll
-        for (int i = 0; i < TPH; ++i) {
-            const int64_t kb = kb0 + 2 * i + half;
-            v[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int c = 0; c < 4; ++c) {
+            v[c] = make_uint4(0u, 0u, 0u, 0u);
             if (kb < KB)
-                v[i] = ptx::ld_nc_v4(x + t * ldx + kb * 128 + l16 * 8);
+                v[c] = ptx::ld_nc_v4(x + t * ldx + kb * 128 + (g + 4 * c) * 8);
         }
-        uint32_t am[TPH];
+        uint32_t a = max(max(absmax_bits8(v[0]), absmax_bits8(v[1])), max(absmax_bits8(v[2]), absmax_bits8(v[3])));
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        const Divisor d = make_divisor(a);
+        uint2 codes[4];
 #pragma unroll
-        for (int i = 0; i < TPH; ++i) {
-            uint32_t a = absmax_bits8(v[i]);
-#pragma unroll
-            for (int o = 8; o >= 1; o >>= 1)
-                a = max(a, __shfl_xor_sync(0xffffffffu, a, o, 16));
-            am[i] = a;
-        }
-        uint32_t mine = am[0];
-#pragma unroll
-        for (int i = 1; i < TPH; ++i)
-            mine = (l16 & (TPH - 1)) == i ? am[i] : mine;
-        const Divisor dm = make_divisor(mine);
-        uint2 codes[TPH];
-        float scale[TPH];
-#pragma unroll
-        for (int i = 0; i < TPH; ++i) {
-            Divisor d;
-            d.s = __shfl_sync(0xffffffffu, dm.s, hbase + i);
-            d.r = __shfl_sync(0xffffffffu, dm.r, hbase + i);
-            d.mode = divisor_mode(am[i]);
-            codes[i] = quant_8(v[i], d);
-            scale[i] = d.s;
-        }
+        for (int c = 0; c < 4; ++c)
+            codes[c] = quant_8(v[c], d);
         for (int j = 0; j < topk; ++j) {
             const int32_t row = __shfl_sync(0xffffffffu, my_dst, j);
-            if (row < 0)
+            if (row < 0 || kb >= KB)
                 continue;
-            uint8_t *qrow = q + (int64_t)row * ldq + l16 * 8;
+            uint8_t *qrow = q + (int64_t)row * ldq + kb * 128;
 #pragma unroll
-            for (int i = 0; i < TPH; ++i) {
-                const int64_t kb = kb0 + 2 * i + half;
-                if (kb < KB) {
-                    ptx::st_v2_cs(qrow + kb * 128, codes[i].x, codes[i].y);
-                    if (l16 == 0) {
-                        if constexpr (PACKED)
-                            reinterpret_cast<float *>(q + (int64_t)row * ldq + KB * 128)[kb] = scale[i];
-                        else
-                            sA[kb * M + row] = scale[i];
-                    }
-                }
+            for (int c = 0; c < 4; ++c)
+                ptx::st_v2_cs(qrow + (g + 4 * c) * 8, codes[c].x, codes[c].y);
+            if (g == 0) {
+                if constexpr (PACKED)
+                    reinterpret_cast<float *>(q + (int64_t)row * ldq + KB * 128)[kb] = d.s;
+                else
+                    sA[kb * M + row] = d.s;
             }
         }
     }
