@@ -16,8 +16,9 @@ import fp8_fine_grained_26_b300 as fp8  # a missing or broken build fails loudly
 DEV = "cuda"
 
 
-# K in tiles: 1, 3, 9, 56 (= 32 + 24), 33 (= 32 + 1), 64 (= 2 x 32): one lane
-# per tile and up to 32 tiles per warp task, so every partial last task shape
+# K in tiles: 1, 3, 9 (= 8 + 1), 56 (= 7 x 8), 33 (= 4 x 8 + 1), 64 (= 8 x 8):
+# a warp task is eight tiles, four lanes each, so partial last tasks of 1 and
+# 3 tiles and whole ones are all covered
 @pytest.mark.parametrize("T,K,M", [(64, 128, 100), (300, 384, 777), (50, 1152, 64), (4096, 7168, 256),
                                    (100, 4224, 50), (20, 8192, 40)])
 def test_gather_quantiser_matches_oracle(T, K, M):
