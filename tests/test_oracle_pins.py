@@ -684,3 +684,17 @@ def test_unquantised_bf16_product_matches_numpy(b_major):
     got = oracle.gemm_bf16_f64(bf16_bits(a), bf16_bits(w), b_major=b_major)
     A, W = a.double().numpy(), w.double().numpy()
     np.testing.assert_allclose(got, A @ (W.T if b_major == 0 else W), rtol=1e-12, atol=1e-300)
+
+
+def test_array_encoder_does_not_depend_on_thread_count():
+    """The array encoder spreads independent elements over threads: 1 thread
+    and many give the same codes, equal to the one-value encoder."""
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 2**32, size=200_000, dtype=np.uint64).astype(np.uint32)
+    v = bits.view(np.float32)
+    v = v[np.isfinite(v)]
+    one = _with_threads(1, lambda: oracle.e4m3_encode_array(v))
+    many = _with_threads(0, lambda: oracle.e4m3_encode_array(v))
+    assert np.array_equal(one, many)
+    idx = rng.integers(0, v.shape[0], size=2000)
+    assert all(int(one[i]) == oracle.e4m3_encode(float(v[i])) for i in idx)
