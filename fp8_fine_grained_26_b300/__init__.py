@@ -42,7 +42,8 @@ EXPORTED = ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp
             "fp8bs_selftest_wait_timeout", "fp8bs_selftest_set_wait_limit",
             "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor", "fp8_quant_per_tensor_delayed",
             "fp8_gemm_per_tensor", "fp8_quant_per_tensor_noalloc", "fp8_ep_dispatch_pack", "fp8_ep_unpack",
-            "fp8bs_gather_rows", "fp8_quant_act_1x128_scatter", "fp8_ep_dispatch_pack_scatter")
+            "fp8bs_gather_rows", "fp8_quant_act_1x128_scatter", "fp8_ep_dispatch_pack_scatter",
+            "fp8bs_selftest_encode_e4m3")
 
 
 class Fp8bsError(RuntimeError):
@@ -70,6 +71,7 @@ def _load():
         "fp8bs_last_error": [p],
         "fp8bs_selftest_wait_timeout": [i64, p],
         "fp8bs_selftest_set_wait_limit": [i64],
+        "fp8bs_selftest_encode_e4m3": [ctypes.c_uint32, i64, p, p],
         "fp8_quant_per_tensor_workspace_size": [i64, i64, p],
         "fp8_quant_per_tensor": [p, i64, i64, i64, p, i64, p, p, i64, p],
         "fp8_quant_per_tensor_delayed": [p, i64, i64, i64, p, p, i64, p, p, p],
@@ -574,11 +576,24 @@ def fp8bs_selftest_set_wait_limit(limit_ns):
     _check(lib.fp8bs_selftest_set_wait_limit(int(limit_ns)), "fp8bs_selftest_set_wait_limit")
 
 
+def fp8bs_selftest_encode_e4m3(first_bits, n, q=None, stream=None):
+    """Test hook: ``q[i]`` = the E4M3 code the quantisers' conversion gives
+    the fp32 value with bit pattern ``first_bits + i`` (uint8 CUDA tensor of
+    ``n`` codes)."""
+    if q is None:
+        q = torch.empty(int(n), dtype=torch.uint8, device="cuda")
+    if q.dtype != torch.uint8 or not q.is_cuda or not q.is_contiguous() or q.numel() < n:
+        raise TypeError("q: expected a contiguous uint8 CUDA tensor of at least n elements")
+    _check(lib.fp8bs_selftest_encode_e4m3(int(first_bits), int(n), _ptr(q), _stream(stream)),
+           "fp8bs_selftest_encode_e4m3")
+    return q
+
+
 __all__ = ["fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_act_w", "fp8_gemm_blockscaled",
            "fp8_gemm_blockscaled_e4m3_out", "fp8_quant_tokens_1x128", "fp8_gemm_wgrad",
            "fp8_quant_act_1x128_gather", "FP8BS_ERR_INDEX",
            "fp8_grouped_gemm_blockscaled", "fp8bs_last_error", "fp8bs_selftest_wait_timeout",
            "fp8bs_selftest_set_wait_limit", "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor",
            "fp8_quant_per_tensor_delayed", "fp8_gemm_per_tensor", "fp8_quant_act_1x128_scatter", "packed_row_bytes", "fp8_ep_dispatch_pack", "fp8_ep_dispatch_pack_scatter",
-           "fp8_ep_unpack", "fp8bs_gather_rows", "Fp8bsError", "lib",
+           "fp8_ep_unpack", "fp8bs_gather_rows", "fp8bs_selftest_encode_e4m3", "Fp8bsError", "lib",
            "LIB_PATH", "EXPORTED", "B_KMAJOR", "B_MNMAJOR", "OUT_BF16", "OUT_FP32"]

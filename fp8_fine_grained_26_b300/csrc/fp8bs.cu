@@ -432,6 +432,24 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns)
     __syncwarp();
 }
 
+// E4M3 codes of the fp32 values with bit patterns first, first + 1, ...,
+// first + n - 1, two at a time through the conversion every quantiser uses
+// (ptx::cvt_e4m3x2: cvt.rn.satfinite.e4m3x2.f32).
+__global__ void selftest_encode_kernel(uint32_t first, int64_t n, uint8_t *__restrict__ q)
+{
+    const int64_t pairs = (n + 1) / 2;
+    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < pairs;
+         p += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = 2 * p;
+        const float a = __uint_as_float(first + (uint32_t)i);
+        const float b = __uint_as_float(first + (uint32_t)(i + 1));
+        const uint32_t c = ptx::cvt_e4m3x2(a, b);
+        q[i] = (uint8_t)(c & 0xFFu);
+        if (i + 1 < n)
+            q[i + 1] = (uint8_t)(c >> 8);
+    }
+}
+
 // Clears the given bits of the error word, atomically with respect to kernels
 // on other streams that may set bits meanwhile.
 __global__ void clear_error_bits_kernel(unsigned int bits)
@@ -978,6 +996,23 @@ int fp8bs_last_error(cudaStream_t stream)
     if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(stream) != cudaSuccess)
         return FP8BS_ERR_LAUNCH;
     return bit == 1u ? FP8BS_ERR_TIMEOUT : FP8BS_ERR_INDEX;
+}
+
+int fp8bs_selftest_encode_e4m3(uint32_t first_bits, int64_t n, uint8_t *q, cudaStream_t stream)
+{
+    if (n < 0 || n > ((int64_t)1 << 32) - (int64_t)first_bits)
+        return FP8BS_ERR_ARG;
+    if (n == 0)
+        return FP8BS_OK;
+    if (!q)
+        return FP8BS_ERR_NULL;
+    DeviceInfo *dev = nullptr;
+    if (int st = current_device(&dev))
+        return st;
+    const int64_t pairs = (n + 1) / 2;
+    const int64_t blocks = std::min<int64_t>((pairs + 255) / 256, 16 * (int64_t)dev->num_sms);
+    selftest_encode_kernel<<<(unsigned)blocks, 256, 0, stream>>>(first_bits, n, q);
+    return launch_status();
 }
 
 int fp8bs_selftest_set_wait_limit(int64_t limit_ns)

@@ -466,6 +466,21 @@ int fp8bs_selftest_wait_timeout(int64_t limit_us, cudaStream_t stream);
  */
 int fp8bs_selftest_set_wait_limit(int64_t limit_ns);
 
+/*
+ * Test hook for the E4M3 encoder (the pages fix no FP8 format; the reading
+ * taken is OCP E4M3 "FN", round to nearest even, saturating to +-448).
+ * q[i] = the code of the fp32 value whose bit pattern is first_bits + i,
+ * for i in [0, n), formed by the same conversion instruction every quantiser
+ * of the library encodes with (cvt.rn.satfinite.e4m3x2.f32), so that a test
+ * can compare it with an independent encoder over every fp32 pattern.
+ *   q : [n] bytes on the device.
+ * n >= 0 and first_bits + n <= 2^32 (else FP8BS_ERR_ARG); non-finite
+ * patterns are converted too (their codes are the hardware's, not part of
+ * the library's contract).  Asynchronous on `stream`; returns FP8BS_OK,
+ * FP8BS_ERR_NULL, FP8BS_ERR_DEVICE or FP8BS_ERR_LAUNCH.
+ */
+int fp8bs_selftest_encode_e4m3(uint32_t first_bits, int64_t n, uint8_t *q, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

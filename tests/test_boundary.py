@@ -26,7 +26,8 @@ def test_header_declares_the_entry_points():
         "fp8bs_selftest_wait_timeout", "fp8bs_selftest_set_wait_limit",
         "fp8_quant_per_tensor_workspace_size", "fp8_quant_per_tensor", "fp8_quant_per_tensor_delayed",
         "fp8_gemm_per_tensor", "fp8_quant_per_tensor_noalloc", "fp8_ep_dispatch_pack", "fp8_ep_unpack",
-        "fp8bs_gather_rows", "fp8_quant_act_1x128_scatter", "fp8_ep_dispatch_pack_scatter"])
+        "fp8bs_gather_rows", "fp8_quant_act_1x128_scatter", "fp8_ep_dispatch_pack_scatter",
+        "fp8bs_selftest_encode_e4m3"])
 
 
 def test_library_loads_and_exports_every_declared_symbol():
@@ -207,6 +208,11 @@ def test_selftest_rejects_out_of_range_limits():
     s = lib.fp8bs_selftest_set_wait_limit
     assert s(-1) == -4 and s(2000000001) == -4
     assert s(0) == 0                                  # the default; host-only
+    e = lib.fp8bs_selftest_encode_e4m3
+    e.argtypes = [ctypes.c_uint32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    assert e(0, -1, P(16), P(0)) == -4
+    assert e(0xFFFFFFF0, 17, P(16), P(0)) == -4       # past the last pattern
+    assert e(5, 0, P(0), P(0)) == 0                   # nothing to do; host-only
 
 
 @pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="checks the no-GPU answer")
