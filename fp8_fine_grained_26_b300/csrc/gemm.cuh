@@ -497,10 +497,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             // first).
             const uint64_t keep = ptx::policy_evict_last();
             const uint64_t stream = ptx::policy_evict_first();
-            // Grouped: the expert weights stream from HBM once, so the shared-
-            // memory ring alone keeps too few bytes in flight.  A cursor runs
-            // B_PREFETCH_SLICES slices ahead of the loads and prefetches each
-            // slice's weight box into L2, where the ring's TMA load finds it.
+            // Grouped: a cursor runs B_PREFETCH_SLICES slices ahead of the
+            // loads and prefetches each slice's weight box into L2, where the
+            // ring's TMA load finds it (on the routed-expert shape, whose
+            // weights stream from HBM once, it is neutral; it costs one request
+            // per slice).
             int64_t pf_t = t_first;
             int pf_kb = 0;
             Tile pf_tl{};
