@@ -907,6 +907,9 @@ __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_tokens_1x128_kernel(
     const int tid = threadIdx.x;
     const int fp = tid & 63;
     const int qtr = tid >> 6;
+    // a feature's 32 codes of a quarter are one whole 32-byte sector when the
+    // code matrix allows 32-byte stores
+    const bool st32 = ((reinterpret_cast<uintptr_t>(q) | (uintptr_t)ldq) & 31u) == 0;
     const int64_t mine = (int64_t)blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     int64_t issued = 0;
     if (tid == 0)
@@ -954,13 +957,21 @@ __global__ void __launch_bounds__(QUANT_THREADS, 3) quant_tokens_1x128_kernel(
         const int64_t t0 = tb * 128 + qtr * 32;
         if (f0 < F) {
             uint8_t *dst = q + f0 * ldq + t0;
-            ptx::st_v4(dst, c0[0], c0[1], c0[2], c0[3]);
-            ptx::st_v4(dst + 16, c0[4], c0[5], c0[6], c0[7]);
+            if (st32) {
+                ptx::st_v8(dst, c0);
+            } else {
+                ptx::st_v4(dst, c0[0], c0[1], c0[2], c0[3]);
+                ptx::st_v4(dst + 16, c0[4], c0[5], c0[6], c0[7]);
+            }
         }
         if (f0 + 1 < F) {
             uint8_t *dst = q + (f0 + 1) * ldq + t0;
-            ptx::st_v4(dst, c1[0], c1[1], c1[2], c1[3]);
-            ptx::st_v4(dst + 16, c1[4], c1[5], c1[6], c1[7]);
+            if (st32) {
+                ptx::st_v8(dst, c1);
+            } else {
+                ptx::st_v4(dst, c1[0], c1[1], c1[2], c1[3]);
+                ptx::st_v4(dst + 16, c1[4], c1[5], c1[6], c1[7]);
+            }
         }
         if (qtr == 0) {
             float *srow = s + tb * F;
