@@ -411,6 +411,14 @@ __device__ __forceinline__ void st_v2_cs(void *p, uint32_t a, uint32_t b)
     asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
 
+// 32-byte streaming store (one whole sector); p must be 32-byte aligned.
+__device__ __forceinline__ void st_v8_cs(void *p, const uint32_t (&v)[8])
+{
+    asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 // Read-only 16-byte load with an L2 cache-policy hint.
 __device__ __forceinline__ uint4 ld_nc_v4_hint(const void *p, uint64_t policy)
 {

@@ -708,8 +708,10 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_gather_kernel(
 // result is the gather form's (quantising before or after the copy gives the
 // same bytes), with a topk-th of the loads and of the encoding work.  A warp
 // task is one token row x GATHER_TILES consecutive 1x128 tiles, four lanes
-// per tile as in the gather kernel; lane j < topk fetches destination j and
-// the warp broadcasts it.  A destination outside [0, M) is skipped and sets bit 1 of the error
+// per tile, lane quarter g taking the tile's columns [32 g, 32 g + 32) (four
+// 16-byte loads; its 32 codes leave as one 32-byte store per destination when
+// the code matrix allows it); lane j < topk fetches destination j and the
+// warp broadcasts it.  A destination outside [0, M) is skipped and sets bit 1 of the error
 // word; a row named twice receives one of the tokens (unspecified which).
 constexpr int SCATTER_MAX_TOPK = 32;
 
@@ -727,7 +729,8 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_scatter_kernel(
     ptx::grid_dep_wait();
     const int lane = threadIdx.x & 31;
     const int tt = lane >> 2;                                     // tile of the task
-    const int g = lane & 3;                                       // lane quarter of the tile
+    const int g = lane & 3;                                       // lane quarter of the tile: columns [32 g, +32)
+    const bool st32 = ((reinterpret_cast<uintptr_t>(q) | (uintptr_t)ldq) & 31u) == 0;
     const int64_t chunks = (KB + GATHER_TILES - 1) / GATHER_TILES;
     const int64_t warp0 = ((int64_t)blockIdx.x * GATHER_THREADS + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * GATHER_THREADS) >> 5;
@@ -754,24 +757,31 @@ __global__ void __launch_bounds__(GATHER_THREADS) quant_act_scatter_kernel(
         for (int c = 0; c < 4; ++c) {
             v[c] = make_uint4(0u, 0u, 0u, 0u);
             if (kb < KB)
-                v[c] = ptx::ld_nc_v4(x + t * ldx + kb * 128 + (g + 4 * c) * 8);
+                v[c] = ptx::ld_nc_v4(x + t * ldx + kb * 128 + (4 * g + c) * 8);
         }
         uint32_t a = max(max(absmax_bits8(v[0]), absmax_bits8(v[1])), max(absmax_bits8(v[2]), absmax_bits8(v[3])));
         a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
         a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
         const Divisor d = make_divisor(a);
-        uint2 codes[4];
+        uint32_t codes[8];                                        // the lane's 32 columns, in order
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            codes[c] = quant_8(v[c], d);
+        for (int c = 0; c < 4; ++c) {
+            const uint2 cc = quant_8(v[c], d);
+            codes[2 * c] = cc.x;
+            codes[2 * c + 1] = cc.y;
+        }
         for (int j = 0; j < topk; ++j) {
             const int32_t row = __shfl_sync(0xffffffffu, my_dst, j);
             if (row < 0 || kb >= KB)
                 continue;
-            uint8_t *qrow = q + (int64_t)row * ldq + kb * 128;
+            uint8_t *dst = q + (int64_t)row * ldq + kb * 128 + 32 * g;
+            if (st32) {
+                ptx::st_v8_cs(dst, codes);
+            } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                ptx::st_v2_cs(qrow + (g + 4 * c) * 8, codes[c].x, codes[c].y);
+                for (int c = 0; c < 4; ++c)
+                    ptx::st_v2_cs(dst + 8 * c, codes[2 * c], codes[2 * c + 1]);
+            }
             if (g == 0) {
                 if constexpr (PACKED)
                     reinterpret_cast<float *>(q + (int64_t)row * ldq + KB * 128)[kb] = d.s;
