@@ -65,7 +65,6 @@ constexpr int SCALE_SLOT_FLOATS = 132;                   // 128 row scales + 2 c
 constexpr int SCALE_SLOT_FLOATS_TOK = 384;               // weight gradient: 128 row + 256 column scales
 constexpr int SCALE_LOOKAHEAD = 2;                       // loader copy groups in flight
 constexpr uint64_t ABORT_GRACE_NS = 1000000;              // pair kernel: wait after an abort (1 ms)
-constexpr int B_PREFETCH_SLICES = 2;                     // grouped: L2 prefetch distance of expert weights
 
 // Shared-memory layout for S pipeline stages of BSB bytes of B each
 // (offsets from a 1024-byte aligned base): operand stages, the output staging
@@ -497,25 +496,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             // first).
             const uint64_t keep = ptx::policy_evict_last();
             const uint64_t stream = ptx::policy_evict_first();
-            // Grouped: a cursor runs B_PREFETCH_SLICES slices ahead of the
-            // loads and prefetches each slice's weight box into L2, where the
-            // ring's TMA load finds it (on the routed-expert shape, whose
-            // weights stream from HBM once, it is neutral; it costs one request
-            // per slice).
-            int64_t pf_t = t_first;
-            int pf_kb = 0;
-            Tile pf_tl{};
-            if constexpr (GROUPED) {
-                if (pf_t < ntiles)
-                    pf_tl = tile_at<GROUPED, PAIR>(g, ss, pf_t, rank);
-                for (int i = 0; i < B_PREFETCH_SLICES && pf_t < ntiles; ++i)
-                    if (++pf_kb == g.KB) {
-                        pf_kb = 0;
-                        pf_t += t_stride;
-                        if (pf_t < ntiles)
-                            pf_tl = tile_at<GROUPED, PAIR>(g, ss, pf_t, rank);
-                    }
-            }
+            // No separate L2 prefetch of the expert weights: a bulk prefetch
+            // of each slice's weight box ahead of its load made the routed-
+            // expert GEMM slower at every distance tried (0, 2 and 4 slices
+            // ahead, or the next tile's first slices at a tile's end).
             uint32_t it = 0;
             bool ok = true;
             for (int64_t t = t_first; ok && t < ntiles; t += t_stride) {
@@ -545,15 +529,6 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     if constexpr (GROUPED) {
                         ptx::tma_load_3d_hint(sb, &tmB, fb, kb * BK, tl.n0, tl.expert,
                                               tl.m0 + BM < tl.m_end ? keep : stream);
-                        if (pf_t < ntiles) {
-                            ptx::tma_prefetch_3d(&tmB, pf_kb * BK, pf_tl.n0, pf_tl.expert);
-                            if (++pf_kb == g.KB) {
-                                pf_kb = 0;
-                                pf_t += t_stride;
-                                if (pf_t < ntiles)
-                                    pf_tl = tile_at<GROUPED, PAIR>(g, ss, pf_t, rank);
-                            }
-                        }
                     } else if constexpr (B_MN) {
                         ptx::tma_load_2d(sb, &tmB, fb, tl.n0, kb * BK);
                         ptx::tma_load_2d(sb + B_STAGE_BYTES / 2, &tmB, fb, tl.n0 + 128, kb * BK);

@@ -113,21 +113,6 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// Bulk L2 prefetch of one tensor box (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int32_t x, int32_t y, int32_t z)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
-                 ::"l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *m, int32_t x, int32_t y)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 ::"l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y)
-                 : "memory");
-}
-
 // CTA-pair load: the box lands in this CTA's shared memory at `dst`; the
 // bytes complete on the mbarrier at shared::cluster address `bar_cluster`,
 // which may belong to the other CTA of the pair.
