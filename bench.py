@@ -102,58 +102,174 @@ def barrier(world):
 
 
 # ---------------------------------------------------------------- clocks
-class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons, every 200 ms."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+class NvmlReader:
+    """The few NVML calls the clock record needs, through ctypes on the
+    driver's libnvidia-ml (reads only; no GPU setting is touched)."""
+    CLOCK_SM = 1
+    REASON_BITS = {"gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
+                   "hw_slowdown": 0x8, "sync_boost": 0x10, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
+                   "display_clock_setting": 0x100}
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.lines = []
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        try:
+            self._reasons = self.lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self._reasons = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def handle(self, uuid, index):
+        h = self.c.c_void_p()
+        if uuid and self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), self.c.byref(h)) == 0:
+            return h
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(self.c.c_uint(index), self.c.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        return h
+
+    def _clock(self, fn, h):
+        v = self.c.c_uint()
+        if fn(h, self.c.c_int(self.CLOCK_SM), self.c.byref(v)) != 0:
+            raise OSError("NVML clock read failed")
+        return float(v.value)
+
+    def clock_sm(self, h):
+        return self._clock(self.lib.nvmlDeviceGetClockInfo, h)
+
+    def max_clock_sm(self, h):
+        return self._clock(self.lib.nvmlDeviceGetMaxClockInfo, h)
+
+    def reasons(self, h):
+        v = self.c.c_ulonglong()
+        if self._reasons(h, self.c.byref(v)) != 0:
+            raise OSError("NVML reason read failed")
+        names = [n for n, b in self.REASON_BITS.items() if v.value & b]
+        rest = v.value & ~sum(self.REASON_BITS.values())
+        return names + ([f"other_0x{rest:x}"] if rest else [])
+
+    def shutdown(self):
+        self.lib.nvmlShutdown()
+
+
+class ClockSampler:
+    """SM clock and clock-event reasons during a timed region.
+
+    A host thread polls NVML every half millisecond; only the samples taken
+    between mark_start() and mark_end() count, so the record covers the timed
+    region itself even when it lasts a few milliseconds.  Without NVML the
+    fallback is nvidia-smi's 200 ms loop: it is given time for a first sample,
+    and when none lands inside a short region all its samples count."""
+    NVML_POLL_S = 0.0005
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+    REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index: int, uuid=None, nvml_factory=None):
+        self.index, self.uuid = index, uuid
+        self.nvml_factory = nvml_factory or NvmlReader
+        self.proc = self.nvml = self.handle = self.max_mhz = None
+        self.samples = []                   # (host time, sm MHz, reason names)
+        self.window = [None, None]
+        self.stop_flag = threading.Event()
 
     def start(self):
         try:
+            self.nvml = self.nvml_factory()
+            self.handle = self.nvml.handle(self.uuid, self.index)
+            self.max_mhz = self.nvml.max_clock_sm(self.handle)
+            self.thread = threading.Thread(target=self._poll_nvml, daemon=True)
+            self.thread.start()
+            return
+        except Exception:                   # no NVML: nvidia-smi loop
+            self.nvml = None
+        try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.SMI_FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread = threading.Thread(target=self._read_smi, daemon=True)
             self.thread.start()
+            t0 = time.perf_counter()
+            while not self.samples and time.perf_counter() - t0 < 1.0:
+                time.sleep(0.01)            # the first sample, before the region starts
         except (OSError, ValueError):
             self.proc = None
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def mark_start(self):
+        self.window[0] = time.perf_counter()
 
-    def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.thread.join(timeout=5)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
+    def mark_end(self):
+        self.window[1] = time.perf_counter()
+
+    def _poll_nvml(self):
+        nv, h = self.nvml, self.handle
+        while not self.stop_flag.is_set():
+            try:
+                mhz = nv.clock_sm(h)
+                why = nv.reasons(h)
+            except Exception:
+                break
+            self.samples.append((time.perf_counter(), mhz, why))
+            time.sleep(self.NVML_POLL_S)
+
+    def _read_smi(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.strip().split(",")]
             if len(parts) < 7:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
+                mhz, mx = float(parts[0]), float(parts[1])
             except ValueError:
                 continue
-            for name, v in zip(names, parts[3:7]):
-                if v.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+            self.max_mhz = mx
+            self.samples.append((time.perf_counter(), mhz,
+                                 [n for n, v in zip(self.REASON_NAMES, parts[3:7]) if v.lower().startswith("active")]))
+
+    def stop(self):
+        if self.nvml is None and self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        self.stop_flag.set()
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.thread.join(timeout=5)
+        t0, t1 = self.window
+        inside = [x for x in self.samples if (t0 is None or x[0] >= t0) and (t1 is None or x[0] <= t1)]
+        if not inside and self.samples:
+            if self.nvml is None:
+                inside = self.samples        # 200 ms samples can miss a short region: keep them all
+            else:                            # a region shorter than the poll: the samples around it
+                before = [x for x in self.samples if t0 is not None and x[0] < t0][-1:]
+                after = [x for x in self.samples if t1 is not None and x[0] > t1][:1]
+                inside = before + after
+        if self.nvml is not None:
+            try:
+                self.nvml.shutdown()
+            except Exception:
+                pass
+        reasons = sorted({n for x in inside for n in x[2]})
+        return {"sm_mhz": statistics.median(x[1] for x in inside) if inside else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(inside),
+                "source": ("NVML, polled every 0.5 ms inside the timed region" if self.nvml is not None
+                           else "nvidia-smi -lms 200")}
+
+
+def clock_sampler(local):
+    """The sampler for this rank's GPU, found by UUID so that it is the right
+    device whatever CUDA_VISIBLE_DEVICES holds."""
+    import torch
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        uuid = None
+    return ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local, uuid)
 
 
 # ---------------------------------------------------------------- workloads
@@ -820,12 +936,12 @@ def measure(args, name, fp8, torch, peaks, peak_src, world, rank, local, device,
         torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
-                          else local)
+    clocks = clock_sampler(local)
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)                         # the sampler's first sample lands in the region
+    time.sleep(0.05)                        # the sampler is running before the region starts
+    clocks.mark_start()
     t_start.record(stream)
     if graph is not None:
         graph.replay()
@@ -834,6 +950,7 @@ def measure(args, name, fp8, torch, peaks, peak_src, world, rank, local, device,
             step.run(i, evs[i])
     t_end.record(stream)
     torch.cuda.synchronize()
+    clocks.mark_end()
     clk = clocks.stop()
     if graph_evt is not None:
         graph_evt.replay()                  # per-kernel times
@@ -1074,8 +1191,9 @@ def run_quant_alone(args, emit=True):
     g = synthetic.generator(0, dev)
 
     results, tot_bytes, tot_ms = {}, 0.0, 0.0
-    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    clocks = clock_sampler(local)
     clocks.start()
+    clocks.mark_start()
     for label, kind, shape in QUANT_ALONE_CASES:
         shapes = list(shape) if kind == "act+w" else [shape]
         in_bytes = sum(r * c * 2 for r, c in shapes)
@@ -1122,6 +1240,7 @@ def run_quant_alone(args, emit=True):
         tot_ms += ms
         del sets, graph
         torch.cuda.empty_cache()
+    clocks.mark_end()
     clk = clocks.stop()
     value = tot_bytes / (tot_ms * 1e-3) / 1e9
     rec = {

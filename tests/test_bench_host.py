@@ -115,3 +115,63 @@ def test_ep_world1_plan_maps_every_routed_copy_to_its_row():
     assert np.array_equal(tok[slot], np.repeat(np.arange(T), topk))
     assert np.array_equal(expert_of_row[slot].reshape(T, topk), plan["choice"])
     assert np.array_equal(np.sort(choice.numpy(), axis=1), plan["choice"])
+
+
+class _FakeNvml:
+    """Stands in for the NVML reader: a scripted SM clock and reason list."""
+
+    def __init__(self, script):
+        self.script, self.i, self.shut = script, 0, False
+
+    def handle(self, uuid, index):
+        return (uuid, index)
+
+    def max_clock_sm(self, h):
+        return 2032.0
+
+    def clock_sm(self, h):
+        return self.script[min(self.i, len(self.script) - 1)][0]
+
+    def reasons(self, h):
+        why = self.script[min(self.i, len(self.script) - 1)][1]
+        self.i += 1
+        return why
+
+    def shutdown(self):
+        self.shut = True
+
+
+def test_clock_record_keeps_only_samples_inside_the_timed_region():
+    # before the region: idle at full clock; inside: 1800 MHz under the power
+    # cap; after it: a slowdown that must not be counted
+    import time
+    fake = _FakeNvml([(2032.0, [])])
+    s = bench.ClockSampler(0, "GPU-fake", nvml_factory=lambda: fake)
+    s.start()
+    time.sleep(0.02)
+    fake.script, fake.i = [(1800.0, ["sw_power_cap"])], 0
+    time.sleep(0.005)                        # let the poller see the change
+    s.mark_start()
+    time.sleep(0.03)
+    s.mark_end()
+    fake.script, fake.i = [(2032.0, ["hw_slowdown"])], 0
+    time.sleep(0.01)
+    rec = s.stop()
+    assert fake.shut
+    assert rec["sm_mhz"] == 1800 and rec["sm_max_mhz"] == 2032
+    assert rec["reasons"] == ["sw_power_cap"] and rec["samples"] >= 5
+    assert rec["source"].startswith("NVML")
+
+
+def test_clock_record_of_a_region_shorter_than_the_poll_uses_the_samples_around_it():
+    import time
+    fake = _FakeNvml([(1900.0, ["sw_power_cap"])])
+    s = bench.ClockSampler(0, None, nvml_factory=lambda: fake)
+    s.NVML_POLL_S = 0.02
+    s.start()
+    time.sleep(0.05)
+    s.mark_start()
+    s.mark_end()                             # no poll lands inside
+    time.sleep(0.05)
+    rec = s.stop()
+    assert rec["samples"] == 2 and rec["sm_mhz"] == 1900 and rec["reasons"] == ["sw_power_cap"]
