@@ -5,8 +5,14 @@ GEMM acceptance (normalised error against the float64 oracle):
 over the dequantised operands; pass if max e <= 2e-3 and mean e <= 1e-4, and
 rows or columns whose dequantised norm is 0 must be exactly 0 on the GPU.
 The bound on max e covers the BF16 output rounding (|C| <= ||a|| ||w||, so
-rounding adds at most 2^-9 ~ 1.95e-3 in e); the mean bound leaves about half
-of its budget to accumulation error after the BF16 rounding's mean share.
+rounding adds at most 2^-9 ~ 1.95e-3 in e).  The mean bound is for the error
+beyond what the output format itself imposes: when a check passes the
+normalised error of rounding the float64 reference to the output type
+(``output_rounding_errors``), the mean bound is 1e-4 above that error's mean.
+For BF16 output that share is about 2^-9 * 0.72 * E|cos(a, w)|: rounding to an
+8-bit significand errs by a quarter ulp on average, significands spread
+log-uniformly over [1, 2) (mean of 1/m = 0.72), and E|cos| = sqrt(2 / (pi K))
+for independent rows.  That is 1.0e-4 at K = 128 and 2.5e-5 at K = 2048.
 """
 import numpy as np
 import torch
@@ -36,6 +42,17 @@ def gemm_errors(c_gpu: np.ndarray, c_ref: np.ndarray, a_norms: np.ndarray, b_nor
     return e, bad_zero
 
 
+def output_rounding_errors(c_ref: np.ndarray, a_norms: np.ndarray, b_norms: np.ndarray, out_dtype):
+    """Normalised error of rounding the float64 reference itself to the output
+    type (None for FP32 output, whose rounding is far below the bounds)."""
+    if out_dtype != torch.bfloat16:
+        return None
+    denom = np.outer(a_norms, b_norms)
+    nz = denom != 0
+    r = torch.from_numpy(np.ascontiguousarray(c_ref, dtype=np.float64)).to(torch.bfloat16).double().numpy()
+    return np.abs(r - c_ref)[nz] / denom[nz]
+
+
 def sampled_errors(c_gpu_vals, c_ref_vals, a_norm_vals, b_norm_vals):
     denom = a_norm_vals * b_norm_vals
     zero = denom == 0
@@ -44,10 +61,12 @@ def sampled_errors(c_gpu_vals, c_ref_vals, a_norm_vals, b_norm_vals):
     return e, bad_zero
 
 
-def assert_gemm_ok(e: np.ndarray, bad_zero: int, what: str, max_e=MAX_E, mean_e=MEAN_E):
+def assert_gemm_ok(e: np.ndarray, bad_zero: int, what: str, max_e=MAX_E, mean_e=MEAN_E, e_out=None):
     assert bad_zero == 0, f"{what}: {bad_zero} zero-norm outputs are not exactly 0"
     if e.size == 0:
         return
+    if e_out is not None and e_out.size:
+        mean_e = mean_e + float(e_out.mean())
     mx, mn = float(e.max()), float(e.mean())
     assert mx <= max_e and mn <= mean_e, f"{what}: max e {mx:.3e} (<= {max_e}), mean e {mn:.3e} (<= {mean_e})"
 

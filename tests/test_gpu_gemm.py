@@ -13,7 +13,7 @@ import torch
 import oracle
 import synthetic
 from synthetic import bf16_bits, generator, normal_bf16
-from parity import assert_gemm_ok, gemm_errors, host_f64, host_u8
+from parity import assert_gemm_ok, gemm_errors, host_f64, host_u8, output_rounding_errors
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +44,7 @@ def full_check(a, w, b_major, out_dtype, what):
     an = oracle.act_row_norms(oqa, osa)
     bn = oracle.b_row_norms(oqb, osb, b_major=b_major)
     e, bad = gemm_errors(host_f64(c), ref, an, bn)
-    assert_gemm_ok(e, bad, what)
+    assert_gemm_ok(e, bad, what, e_out=output_rounding_errors(ref, an, bn, out_dtype))
     return c, ref
 
 

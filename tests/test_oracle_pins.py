@@ -698,3 +698,24 @@ def test_array_encoder_does_not_depend_on_thread_count():
     assert np.array_equal(one, many)
     idx = rng.integers(0, v.shape[0], size=2000)
     assert all(int(one[i]) == oracle.e4m3_encode(float(v[i])) for i in idx)
+
+
+def test_output_rounding_share_of_the_gemm_error_rule():
+    # The GEMM acceptance rule lets the mean error rise by the normalised error
+    # of rounding the float64 reference itself to BF16.  That share is bounded
+    # by 2^-9 element-wise (|C| <= ||a|| ||w||, half an ulp of an 8-bit
+    # significand) and, for independent random rows, averages about
+    # 2^-9 * 0.72 * E|cos| with E|cos| = sqrt(2 / (pi K)): ~1e-4 at K = 128.
+    import torch
+    from parity import output_rounding_errors
+    rng = np.random.default_rng(5)
+    for K in (128, 2048):
+        a = rng.standard_normal((300, K))
+        w = rng.standard_normal((200, K))
+        ref = a @ w.T
+        an, wn = np.linalg.norm(a, axis=1), np.linalg.norm(w, axis=1)
+        assert output_rounding_errors(ref, an, wn, torch.float32) is None
+        e = output_rounding_errors(ref, an, wn, torch.bfloat16)
+        assert e.max() <= 2.0 ** -9
+        predicted = 2.0 ** -9 * (1.0 - 0.5) / np.log(2.0) * np.sqrt(2.0 / (np.pi * K))
+        assert 0.85 * predicted < e.mean() < 1.15 * predicted, (K, e.mean(), predicted)
