@@ -1,5 +1,5 @@
-"""Seeded random shapes for the dense and grouped GEMMs, every output element
-compared with the float64 oracle.
+"""Seeded random shapes for the GEMMs (every output element against the float64
+oracle) and the quantisers (bit-exact against the oracle).
 
 The fixed-shape tests pin particular tile counts, tails and layouts; these
 draw M, N, K, the B layout, the output type and (grouped) the segment lengths
@@ -15,7 +15,7 @@ import torch
 import oracle
 import synthetic
 from synthetic import bf16_bits, generator, normal_bf16
-from parity import assert_gemm_ok, gemm_errors, host_f64, output_rounding_errors
+from parity import assert_gemm_ok, gemm_errors, host_f64, host_u8, output_rounding_errors
 
 from test_gpu_gemm import full_check, grouped_gpu
 
@@ -86,3 +86,86 @@ def test_grouped_random_segments(i, counts, N, K, out_dtype):
         err, bad = gemm_errors(got[r0:r1], ref[r0:r1], an[r0:r1], bn)
         assert_gemm_ok(err, bad, f"case {i} expert {e} ({counts}, N={N}, K={K})",
                        e_out=output_rounding_errors(ref[r0:r1], an[r0:r1], bn, out_dtype))
+
+
+# ---------------------------------------------------------------- quantisers (bit-exact)
+from test_gpu_quant import check_act, check_w          # noqa: E402
+from test_gpu_quant_pair import check_pair              # noqa: E402
+
+
+def _random_bf16(shape, rng, g):
+    """N(0, s^2) with s drawn over six decades, some outliers and zeroed runs,
+    or Student-t: the value mixes the quantisers see."""
+    kind = rng.integers(0, 3)
+    if kind == 2:
+        x = synthetic.student_t3_bf16(shape, g, DEV)
+    else:
+        x = normal_bf16(shape, float(10.0 ** rng.uniform(-3, 3)), g, DEV,
+                        outlier_p=float(rng.choice([0.0, 0.001, 0.02])), outlier_scale=float(rng.choice([10, 100])))
+    if rng.random() < 0.5 and shape[0] > 1:
+        r = int(rng.integers(0, shape[0]))
+        x[r] = 0                                            # an all-zero row
+    return x
+
+
+def _quant_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    return [(i, int(rng.integers(1, 1500)), 128 * int(rng.integers(1, 17)), int(rng.integers(1, 1500)),
+             128 * int(rng.integers(1, 17))) for i in range(n)]
+
+
+@pytest.mark.parametrize("i,M,K,R,C", _quant_cases(12, 4242))
+def test_quantisers_random_shapes(i, M, K, R, C):
+    rng = np.random.default_rng(9000 + i)
+    g = generator(9000 + i, DEV)
+    x = _random_bf16((M, K), rng, g)
+    w = _random_bf16((R, C), rng, g)
+    check_act(x, f"case {i} act {M}x{K}")
+    check_w(w, f"case {i} weight {R}x{C}")
+    check_pair(x, w, f"case {i} pair")
+
+
+@pytest.mark.parametrize("i", range(6))
+def test_token_quantiser_random_shapes(i):
+    rng = np.random.default_rng(7000 + i)
+    g = generator(7000 + i, DEV)
+    T, F = 128 * int(rng.integers(1, 9)), 8 * int(rng.integers(1, 160))   # F: 16-byte BF16 rows
+    x = _random_bf16((T, F), rng, g)
+    q, s = fp8.fp8_quant_tokens_1x128(x)
+    torch.cuda.synchronize()
+    assert fp8.fp8bs_last_error() == 0
+    oq, os_ = oracle.quant_tokens_1x128(bf16_bits(x))
+    assert np.array_equal(host_u8(q), oq), f"case {i} {T}x{F}"
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), os_.view(np.uint32)), f"case {i} {T}x{F}"
+
+
+@pytest.mark.parametrize("i", range(6))
+def test_dispatch_quantisers_random_routing(i):
+    # gather (a row list with repeats) and scatter (every token to topk
+    # distinct rows of a larger buffer) against the oracle's quantiser of the
+    # gathered rows
+    rng = np.random.default_rng(8000 + i)
+    g = generator(8000 + i, DEV)
+    T, K, topk = int(rng.integers(1, 400)), 128 * int(rng.integers(1, 40)), int(rng.integers(1, 9))
+    x = _random_bf16((T, K), rng, g)
+    oq, os_ = oracle.quant_act_1x128(bf16_bits(x))
+    rows = torch.from_numpy(rng.integers(0, T, size=int(rng.integers(1, 3 * T + 2))).astype(np.int32)).to(DEV)
+    q, s = fp8.fp8_quant_act_1x128_gather(x, rows)
+    assert fp8.fp8bs_last_error() == 0
+    r = rows.cpu().numpy()
+    assert np.array_equal(host_u8(q), oq[r]), f"case {i} gather"
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), os_[:, r].view(np.uint32)), f"case {i} gather scales"
+    M = T * topk + int(rng.integers(0, 7))
+    dest = torch.from_numpy(rng.permutation(M)[: T * topk].astype(np.int32).reshape(T, topk)).to(DEV)
+    q = torch.full((M, K), 0x5A, dtype=torch.uint8, device=DEV)
+    s = torch.full((K // 128, M), -1.25, dtype=torch.float32, device=DEV)
+    fp8.fp8_quant_act_1x128_scatter(x, dest, M, q=q, sA=s)
+    assert fp8.fp8bs_last_error() == 0
+    d = dest.cpu().numpy()
+    qh, sh = host_u8(q), s.cpu().numpy()
+    written = np.zeros(M, bool)
+    for j in range(topk):
+        assert np.array_equal(qh[d[:, j]], oq), f"case {i} scatter copy {j}"
+        assert np.array_equal(sh[:, d[:, j]].view(np.uint32), os_.view(np.uint32)), f"case {i} scatter scales {j}"
+        written[d[:, j]] = True
+    assert np.all(qh[~written] == 0x5A) and np.all(sh[:, ~written] == -1.25)     # untouched rows
