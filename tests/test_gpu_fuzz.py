@@ -169,3 +169,36 @@ def test_dispatch_quantisers_random_routing(i):
         assert np.array_equal(sh[:, d[:, j]].view(np.uint32), os_.view(np.uint32)), f"case {i} scatter scales {j}"
         written[d[:, j]] = True
     assert np.all(qh[~written] == 0x5A) and np.all(sh[:, ~written] == -1.25)     # untouched rows
+
+
+# ---------------------------------------------------------------- weight gradient and E4M3 output
+from test_gpu_wgrad import _check as wgrad_check               # noqa: E402
+
+
+@pytest.mark.parametrize("i", range(6))
+def test_wgrad_random_shapes(i):
+    rng = np.random.default_rng(6000 + i)
+    T = 128 * int(rng.integers(1, 9))
+    M, N = 8 * int(rng.integers(1, 90)), 8 * int(rng.integers(1, 140))     # 16-byte BF16 rows
+    wgrad_check(T, M, N, seed=6000 + i, out_dtype=torch.bfloat16 if rng.random() < 0.6 else torch.float32)
+
+
+@pytest.mark.parametrize("i", range(6))
+def test_e4m3_output_random_shapes(i):
+    # the fused epilogue is bit-equal to the BF16 GEMM followed by the
+    # activation quantiser, whose own parity with the oracle is bit-exact
+    rng = np.random.default_rng(5000 + i)
+    M, N, K = int(rng.integers(1, 700)), 128 * int(rng.integers(1, 9)), 128 * int(rng.integers(1, 12))
+    b_major = int(rng.integers(0, 2))
+    g = generator(5000 + i, DEV)
+    a = normal_bf16((M, K), 1.0, g, DEV, outlier_p=0.002, outlier_scale=40.0)
+    w = normal_bf16((N, K) if b_major == 0 else (K, N), 0.02, g, DEV)
+    qa, sa = fp8.fp8_quant_act_1x128(a)
+    qb, sb = fp8.fp8_quant_w_128x128(w)
+    qc, sc = fp8.fp8_gemm_blockscaled_e4m3_out(qa, sa, qb, sb, b_major=b_major)
+    c = fp8.fp8_gemm_blockscaled(qa, sa, qb, sb, b_major=b_major)
+    q2, s2 = fp8.fp8_quant_act_1x128(c)
+    assert fp8.fp8bs_last_error() == 0
+    assert torch.equal(qc, q2), f"case {i} {M}x{N}x{K}: codes differ"
+    assert torch.equal(sc.view(torch.int32), s2.view(torch.int32)), f"case {i} {M}x{N}x{K}: scales differ"
+    full_check(a, w, b_major, torch.bfloat16, f"case {i} BF16 GEMM under the E4M3 output")
