@@ -13,7 +13,8 @@ each timed in its own region, the expert-parallel layer's device steps on the
 routed-expert workload, the per-tensor contrast scheme on the dgrad and MLA q
 shapes, and the quantisers-alone table.
 ``--workload`` selects another headline shape (mla_q, mla_kv, wgrad,
-experts, experts_ep, tiny, experts_small) and then measures only that one.  For ``experts`` a step is the dispatch
+experts, experts_ep, tiny, and the 64-expert experts_small and
+experts_ep_small that profiler captures run on) and then measures only that one.  For ``experts`` a step is the dispatch
 quantisation (each token row encoded once and its codes written to each of
 its routed rows) plus the grouped GEMM (expert weights
 are quantised once, before timing, as they are once per weight update); for
@@ -286,7 +287,7 @@ def make_workload(name, device):
         return synthetic.tiny(device=device)
     if name in ("experts", "experts_ep"):
         return synthetic.experts(device=device, keep_x=True)
-    if name == "experts_small":
+    if name in ("experts_small", "experts_ep_small"):
         return synthetic.experts_small(device=device, keep_x=True)
     if name == "wgrad":
         return synthetic.wgrad(device=device)
@@ -887,7 +888,7 @@ def choose_peaks(peaks, region_s, clk):
 def build_step(name, case, fp8, torch, args):
     if name.endswith("_per_tensor"):
         return PerTensorStep(case, fp8, torch)
-    if name == "experts_ep":
+    if name in ("experts_ep", "experts_ep_small"):
         return ExpertsEPStep(case, fp8, torch)
     if name in ("experts", "experts_small"):
         return ExpertsStep(case, fp8, torch)
@@ -901,7 +902,8 @@ def measure(args, name, fp8, torch, peaks, peak_src, world, rank, local, device,
     every kernel), end to end from host buffers, rooflines.  Returns the
     record (the JSON line's body for the headline, a sub-record otherwise)."""
     case = make_workload(name, device)
-    if args.e4m3_out and (name in ("experts", "experts_small", "experts_ep", "wgrad") or name.endswith("_per_tensor")):
+    if args.e4m3_out and (name in ("experts", "experts_small", "experts_ep", "experts_ep_small", "wgrad")
+                          or name.endswith("_per_tensor")):
         raise SystemExit("--e4m3-out applies to the dense forward workloads")
     step = build_step(name, case, fp8, torch, args)
     stream = torch.cuda.current_stream()
@@ -1025,7 +1027,7 @@ def measure(args, name, fp8, torch, peaks, peak_src, world, rank, local, device,
         import oracle
         if name == "wgrad":
             flops, secs, desc = oracle_sample_wgrad(case)
-        elif name not in ("experts", "experts_small", "experts_ep") and not name.endswith("_per_tensor"):
+        elif name not in ("experts", "experts_small", "experts_ep", "experts_ep_small") and not name.endswith("_per_tensor"):
             flops, secs, desc = oracle_sample(name, lambda: dense_host_inputs(case))
         else:
             flops = None
@@ -1097,7 +1099,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    if args.workload in ("experts", "experts_small", "experts_ep", "wgrad"):
+    if args.workload in ("experts", "experts_small", "experts_ep", "experts_ep_small", "wgrad"):
         print(json.dumps({"impl": "reference", "unavailable":
                           "the oracle arm samples the dense forward workloads only"}), flush=True)
         return
@@ -1262,6 +1264,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=HEADLINE,
                     choices=["mla_q", "mla_kv", "dgrad", "experts", "experts_ep", "tiny", "wgrad", "experts_small",
+                             "experts_ep_small",
                              "dgrad_per_tensor", "mla_q_per_tensor", "mla_kv_per_tensor"],
                     help="the headline workload (default: dgrad, the largest configuration)")
     ap.add_argument("--no-subrecords", action="store_true",
