@@ -55,7 +55,7 @@ class Fp8bsError(RuntimeError):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
-                          "(python -m fp8_fine_grained_26_b300.build)")
+                          "(python fp8_fine_grained_26_b300/build.py, or __graft_entry__.build())")
     lib = ctypes.CDLL(LIB_PATH)
     i64, p, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
     sigs = {
