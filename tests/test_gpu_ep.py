@@ -151,6 +151,32 @@ def test_ep_world1_matches_oracle(experts_world1):
     st.check()
 
 
+def test_ep_world1_over_nccl_equals_loopback(experts_world1, tmp_path):
+    # The layer's exchanges through torch.distributed with the NCCL backend (a
+    # one-rank group on this GPU): the FP8 payload rows, the per-expert counts
+    # and the BF16 return rows go through NCCL's all-to-all, and the result is
+    # bit-equal to the in-process loopback.  Larger worlds are covered by the
+    # gloo tests on the CPU and the emulated ranks below.
+    import datetime
+    import os
+    import torch.distributed as dist
+    from fp8_fine_grained_26_b300.ep import TorchDistComm
+    case, qw, sw, choice, y = experts_world1
+    E = qw.shape[0]
+    os.environ.setdefault("NCCL_NVLS_ENABLE", "0")
+    store = dist.FileStore(str(tmp_path / "nccl_store"), 1)
+    dist.init_process_group("nccl", store=store, rank=0, world_size=1,
+                            timeout=datetime.timedelta(seconds=120), device_id=torch.device(DEV, 0))
+    try:
+        layer = FP8ExpertParallel(E, 1, 0, qw, sw, comm=TorchDistComm())
+        y2 = layer.forward(case.x, choice)
+        torch.cuda.synchronize()
+        assert fp8.fp8bs_last_error() == 0
+        assert torch.equal(y, y2)
+    finally:
+        dist.destroy_process_group()
+
+
 def _emulate(world, x, choice, qw, sw):
     """Every rank's three phases run in turn; the exchanges are slices."""
     E = qw.shape[0]
