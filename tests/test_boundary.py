@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 import subprocess
+import sys
 
 import pytest
 
@@ -220,3 +221,16 @@ def test_no_gpu_is_reported_as_device_error():
     lib = _raw()
     st = lib.fp8_quant_act_1x128(P(16), 4, 128, 128, P(16), 128, P(16), P(0))
     assert st == -6
+
+
+def test_build_entry_does_not_need_the_library_to_exist():
+    # a fresh checkout has no libfp8bs.so, and the package refuses to import
+    # without it: build() must reach the build script without importing the
+    # package first
+    import subprocess
+    code = ("import sys, __graft_entry__ as g, os; "
+            "m = g._module_from_file('fp8bs_lib_build', os.path.join(g.ROOT, 'fp8_fine_grained_26_b300', 'build.py')); "
+            "assert 'fp8_fine_grained_26_b300' not in sys.modules; "
+            "assert callable(m.build) and m.LIB.endswith('libfp8bs.so'); print('ok')")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT, timeout=120)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", out.stderr[-2000:]
